@@ -1,0 +1,9 @@
+"""GB300-native hot path of DFlash block-diffusion speculative drafting.
+
+libdflash (csrc/, C ABI in include/dflash.h) holds the CUDA kernels; this
+package is the thin Python binding over it.
+"""
+from ._lib import DflashError, lib  # noqa: F401
+from .drafter import Drafter, gemm_bf16, weights_to_device  # noqa: F401
+
+__all__ = ["Drafter", "DflashError", "lib", "gemm_bf16", "weights_to_device"]

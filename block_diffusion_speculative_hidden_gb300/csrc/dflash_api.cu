@@ -1,0 +1,583 @@
+// The libdflash C ABI (include/dflash.h): context set-up, workspace layout
+// and the sequence of kernels behind dflash_inject_kv, dflash_draft_block and
+// dflash_accept.  All device memory is the caller's; nothing here allocates.
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+#include "kernels.cuh"
+
+using namespace dflash;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 4; }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+// Split count of one draft-side GEMM for M activation rows (hi/lo inputs).
+int draft_splits(const dflash_config& g, int M, int N, int K) {
+  if (g.dtype != DFLASH_BF16) return 1;
+  const int tiles = ceil_div(N, kTileN) * ceil_div(M, gemm_bn(M, true));
+  return choose_splits(tiles, gemm_kb(K));
+}
+// Split count of an inject-side GEMM: independent of the row count, so a
+// row's result does not depend on how many rows share the call.
+int inject_splits(const dflash_config& g, int N, int K) {
+  if (g.dtype != DFLASH_BF16) return 1;
+  return choose_splits(ceil_div(N, kTileN), gemm_kb(K));
+}
+
+int attn_max_splits_for(const dflash_config& g, int num_sms) {
+  const int max_keys = g.max_pages_per_seq * kPage + kBlockK;
+  const int by_sms = ceil_div(2 * num_sms, g.n_kv_heads);
+  return std::max(1, std::min(by_sms, ceil_div(max_keys, 32)));
+}
+
+bool config_ok(const dflash_config* g) {
+  if (g == nullptr) return false;
+  if (g->dtype != DFLASH_F32 && g->dtype != DFLASH_BF16) return false;
+  if (g->block_k != kBlockK || g->page_size != kPage) return false;
+  if (g->n_layers < 1 || g->hidden < 8 || g->n_q_heads < 1 || g->n_kv_heads < 1) return false;
+  if (g->n_q_heads % g->n_kv_heads != 0) return false;
+  const int G = g->n_q_heads / g->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+  if (g->head_dim != 32 && g->head_dim != 64 && g->head_dim != 128) return false;
+  if (g->ffn < 8 || g->vocab < 2 || g->mask_id < 0 || g->mask_id >= g->vocab) return false;
+  if (g->n_taps < 1 || g->tap_width < 1) return false;
+  if (g->max_batch < 1 || g->max_batch > 4096 || g->max_pages_per_seq < 1 || g->n_pages < 1) return false;
+  if (g->max_rows < 1 || g->max_inject_rows < g->max_rows) return false;
+  if (!(g->rope_theta > 0.f) || !(g->rms_eps >= 0.f)) return false;
+  // TMA row strides must be multiples of 16 bytes; vector row copies need 16 bytes
+  const int q = elem_bytes(*g) == 2 ? 8 : 4;
+  const int F = g->n_taps * g->tap_width;
+  if (g->hidden % q || F % q || g->ffn % q || (g->n_q_heads * g->head_dim) % q) return false;
+  return true;
+}
+
+struct Carve {
+  char* base;
+  size_t off = 0;
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off += align_up(bytes);
+    return p;
+  }
+};
+
+// Lays the workspace out (base == nullptr: just measure).
+size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
+  Carve w{base};
+  const int e = elem_bytes(g);
+  const size_t R = g.max_inject_rows, M = static_cast<size_t>(g.max_batch) * kBlockK;
+  const int d = g.hidden, F = g.ffn, qd = g.n_q_heads * g.head_dim, kvd = g.n_kv_heads * g.head_dim;
+  const int Fin = g.n_taps * g.tap_width, V = g.vocab, L = g.n_layers;
+  const int n_lm_tiles = ceil_div(V, kTileN);
+  const int rope_rows = g.max_pages_per_seq * kPage + kBlockK;
+  // largest split-K partial
+  size_t part = static_cast<size_t>(inject_splits(g, d, Fin)) * R * d;
+  part = std::max(part, static_cast<size_t>(inject_splits(g, 2 * L * kvd, d)) * R * 2 * L * kvd);
+  for (int B = 1; B <= g.max_batch; ++B) {
+    const int Mb = B * kBlockK;
+    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, qd + 2 * kvd, d)) * Mb * (qd + 2 * kvd));
+    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, d, qd)) * Mb * d);
+    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, 2 * F, d)) * Mb * 2 * F);
+    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, d, F)) * Mb * d);
+  }
+  const int G = g.n_q_heads / g.n_kv_heads;
+  const int amax = attn_max_splits_for(g, num_sms);
+  const size_t attn_rows = static_cast<size_t>(g.max_batch) * g.n_kv_heads * amax * G * kBlockK;
+
+  int* status = static_cast<int*>(w.take(sizeof(int) * 8));
+  auto free_ring = static_cast<int32_t*>(w.take(sizeof(int32_t) * g.n_pages));
+  auto row_seq = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
+  auto row_pos = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
+  auto row_src = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
+  auto rcos = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
+  auto rsin = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
+  const bool lo = g.dtype == DFLASH_BF16;  // GEMM inputs carry a second bf16 term
+  void* fc_in = w.take(R * Fin * e);
+  void* h_fused = w.take(R * d * e);
+  void* h_lo = lo ? w.take(R * d * e) : nullptr;
+  auto partp = static_cast<float*>(w.take(sizeof(float) * part));
+  auto x = static_cast<float*>(w.take(sizeof(float) * M * d));
+  void* a = w.take(M * d * e);
+  void* a_lo = lo ? w.take(M * d * e) : nullptr;
+  auto q = static_cast<float*>(w.take(sizeof(float) * M * qd));
+  auto kb = static_cast<float*>(w.take(sizeof(float) * M * kvd));
+  auto vb = static_cast<float*>(w.take(sizeof(float) * M * kvd));
+  void* o = w.take(M * qd * e);
+  void* o_lo = lo ? w.take(M * qd * e) : nullptr;
+  void* act = w.take(M * F * e);
+  void* act_lo = lo ? w.take(M * F * e) : nullptr;
+  auto attn_o = static_cast<float*>(w.take(sizeof(float) * attn_rows * g.head_dim));
+  auto attn_ml = static_cast<float*>(w.take(sizeof(float) * attn_rows * 2));
+  auto lm_mx = static_cast<float*>(w.take(sizeof(float) * M * n_lm_tiles));
+  auto lm_se = static_cast<float*>(w.take(sizeof(float) * M * n_lm_tiles));
+  auto lm_idx = static_cast<int32_t*>(w.take(sizeof(int32_t) * M * n_lm_tiles));
+  float* logits_ws = g.dtype == DFLASH_F32 ? static_cast<float*>(w.take(sizeof(float) * M * V)) : nullptr;
+  auto tok1 = static_cast<int32_t*>(w.take(sizeof(int32_t) * M));
+  auto conf1 = static_cast<float*>(w.take(sizeof(float) * M));
+  auto commit = static_cast<int32_t*>(w.take(sizeof(int32_t) * M));
+  if (c != nullptr) {
+    c->status = status;
+    c->scal = status + 4;
+    c->free_ring = free_ring;
+    c->row_seq = row_seq;
+    c->row_pos = row_pos;
+    c->row_src = row_src;
+    c->rope_cos = rcos;
+    c->rope_sin = rsin;
+    c->rope_rows = rope_rows;
+    c->fc_in = fc_in;
+    c->h_fused = h_fused;
+    c->h_lo = h_lo;
+    c->part = partp;
+    c->part_floats = part;
+    c->x = x;
+    c->a = a;
+    c->a_lo = a_lo;
+    c->q = q;
+    c->kblk = kb;
+    c->vblk = vb;
+    c->o = o;
+    c->o_lo = o_lo;
+    c->act = act;
+    c->act_lo = act_lo;
+    c->attn_o = attn_o;
+    c->attn_ml = attn_ml;
+    c->attn_max_splits = amax;
+    c->lm = LmPartials{lm_mx, lm_se, lm_idx, n_lm_tiles};
+    c->logits_ws = logits_ws;
+    c->tok1 = tok1;
+    c->conf1 = conf1;
+    c->commit = commit;
+  }
+  return w.off;
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  return n;
+}
+
+#define DF_CHECK(call)                               \
+  do {                                               \
+    if ((call) != cudaSuccess) return DFLASH_ERR_CUDA; \
+  } while (0)
+
+dflash_status run_gemm(dflash_ctx* c, const void* W, int N, int K, const void* X, const void* X_lo, int M,
+                       int M_alloc, int splits, const int* m_valid, cudaStream_t s) {
+  GemmLaunch g{};
+  g.W = W;
+  g.X = X;
+  g.X_lo = X_lo;
+  g.N = N;
+  g.K = K;
+  g.M = M;
+  g.M_alloc = M_alloc;
+  g.splits = splits;
+  g.out = c->part;
+  g.split_stride = static_cast<long long>(M) * N;
+  g.ldo = N;
+  g.m_valid = m_valid;
+  DF_CHECK(gemm_launch(c, g, s));
+  return DFLASH_OK;
+}
+
+// Brackets the launches between its construction and destruction with a
+// pair of events of one timing class (no-op unless profiling is on).
+struct ProfScope {
+  dflash_ctx* c;
+  cudaStream_t s;
+  int cls, launches;
+  cudaEvent_t a = nullptr;
+  static cudaEvent_t get(dflash_ctx* c) {
+    if (!c->prof_pool.empty()) {
+      cudaEvent_t e = c->prof_pool.back();
+      c->prof_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+  ProfScope(dflash_ctx* c_, int cls_, int launches_, cudaStream_t s_) : c(c_), s(s_), cls(cls_), launches(launches_) {
+    if (!c->prof_on) return;
+    a = get(c);
+    if (a != nullptr) cudaEventRecord(a, s);
+  }
+  void close() {
+    if (a == nullptr) return;
+    cudaEvent_t b = get(c);
+    if (b != nullptr) {
+      cudaEventRecord(b, s);
+      c->prof_live.push_back({a, b, cls, launches});
+    } else {
+      c->prof_pool.push_back(a);
+    }
+    a = nullptr;
+  }
+  ~ProfScope() { close(); }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_status_string(dflash_status s) {
+  switch (s) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case DFLASH_ERR_POOL_EXHAUSTED: return "KV page pool exhausted";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_STATE: return "device status word set";
+    case DFLASH_ERR_WORKSPACE: return "workspace or pool buffer too small";
+  }
+  return "unknown";
+}
+
+size_t dflash_workspace_size(const dflash_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return layout(*cfg, device_sms(), nullptr, nullptr);
+}
+
+size_t dflash_kv_pool_size(const dflash_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return 2ull * cfg->n_layers * cfg->n_pages * cfg->n_kv_heads * kPage * cfg->head_dim * sizeof(float);
+}
+
+dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, void* kv_pool, size_t kv_pool_bytes,
+                            int32_t* page_table, int32_t* seq_len, void* workspace, size_t workspace_bytes,
+                            dflash_ctx** out) {
+  if (out == nullptr) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg == nullptr || w == nullptr || kv_pool == nullptr || page_table == nullptr || seq_len == nullptr ||
+      workspace == nullptr)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!config_ok(cfg)) return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  if (w->w_fc == nullptr || w->g_fc == nullptr || w->embed == nullptr || w->g_final == nullptr ||
+      w->w_lm == nullptr || w->w_kv_inject == nullptr || w->w_qkv == nullptr || w->w_o == nullptr ||
+      w->w_gu == nullptr || w->w_down == nullptr || w->g_in == nullptr || w->g_post == nullptr)
+    return DFLASH_ERR_INVALID_ARG;
+  for (int l = 0; l < cfg->n_layers; ++l)
+    if (w->w_qkv[l] == nullptr || w->w_o[l] == nullptr || w->w_gu[l] == nullptr || w->w_down[l] == nullptr ||
+        w->g_in[l] == nullptr || w->g_post[l] == nullptr)
+      return DFLASH_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0 || reinterpret_cast<uintptr_t>(kv_pool) % 16 != 0)
+    return DFLASH_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (workspace_bytes < layout(*cfg, sms, nullptr, nullptr) || kv_pool_bytes < dflash_kv_pool_size(cfg))
+    return DFLASH_ERR_WORKSPACE;
+
+  dflash_ctx* c = new (std::nothrow) dflash_ctx();
+  if (c == nullptr) return DFLASH_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  c->elem = elem_bytes(*cfg);
+  c->num_sms = sms;
+  c->w_fc = w->w_fc;
+  c->g_fc = w->g_fc;
+  c->embed = w->embed;
+  c->g_final = w->g_final;
+  c->w_lm = w->w_lm;
+  c->w_kv_inj = w->w_kv_inject;
+  c->key_offset = w->key_offset;
+  c->w_qkv.assign(w->w_qkv, w->w_qkv + cfg->n_layers);
+  c->w_o.assign(w->w_o, w->w_o + cfg->n_layers);
+  c->w_gu.assign(w->w_gu, w->w_gu + cfg->n_layers);
+  c->w_down.assign(w->w_down, w->w_down + cfg->n_layers);
+  c->g_in.assign(w->g_in, w->g_in + cfg->n_layers);
+  c->g_post.assign(w->g_post, w->g_post + cfg->n_layers);
+  const size_t half_pool = dflash_kv_pool_size(cfg) / 2;
+  c->pool_k = kv_pool;
+  c->pool_v = static_cast<char*>(kv_pool) + half_pool;
+  c->page_table = page_table;
+  c->seq_len = seq_len;
+  layout(*cfg, sms, c, static_cast<char*>(workspace));
+  if (launch_rope_table(c, nullptr) != cudaSuccess || launch_reset(c, nullptr) != cudaSuccess ||
+      cudaStreamSynchronize(nullptr) != cudaSuccess) {
+    delete c;
+    return DFLASH_ERR_CUDA;
+  }
+  *out = c;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_destroy(dflash_ctx* ctx) {
+  if (ctx == nullptr) return DFLASH_ERR_INVALID_ARG;
+  for (auto& r : ctx->prof_live) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : ctx->prof_pool) cudaEventDestroy(e);
+  delete ctx;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_reset(dflash_ctx* ctx, dflash_stream stream) {
+  if (ctx == nullptr) return DFLASH_ERR_INVALID_ARG;
+  DF_CHECK(launch_reset(ctx, stream));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_release(dflash_ctx* ctx, int b, dflash_stream stream) {
+  if (ctx == nullptr || b < 0 || b >= ctx->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  DF_CHECK(launch_release(ctx, b, stream));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_truncate(dflash_ctx* ctx, int b, int new_len, dflash_stream stream) {
+  if (ctx == nullptr || b < 0 || b >= ctx->cfg.max_batch || new_len < 0) return DFLASH_ERR_INVALID_ARG;
+  DF_CHECK(launch_truncate(ctx, b, new_len, stream));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t* n_rows, int first_seq, int B,
+                               int max_rows, dflash_stream stream) {
+  if (ctx == nullptr || feats == nullptr || n_rows == nullptr) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& g = ctx->cfg;
+  if (B < 1 || first_seq < 0 || first_seq + B > g.max_batch || max_rows < 1) return DFLASH_ERR_INVALID_ARG;
+  if (max_rows > g.max_rows || static_cast<long long>(B) * max_rows > g.max_inject_rows)
+    return DFLASH_ERR_UNSUPPORTED_SHAPE;
+  if (reinterpret_cast<uintptr_t>(feats) % 16 != 0) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t s = stream;
+  const int rows = B * max_rows;
+  const int d = g.hidden, Fin = g.n_taps * g.tap_width, kvd = g.n_kv_heads * g.head_dim;
+  const int Nkv = 2 * g.n_layers * kvd;
+  {
+    ProfScope p(ctx, DFLASH_PROF_ROWWISE, 2, s);
+    DF_CHECK(launch_alloc(ctx, n_rows, first_seq, B, max_rows, s));
+    DF_CHECK(launch_gather_rows(ctx, feats, rows, max_rows, first_seq, s));
+  }
+  const int s_fc = inject_splits(g, d, Fin);
+  {
+    ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
+    dflash_status st =
+        run_gemm(ctx, ctx->w_fc, d, Fin, ctx->fc_in, nullptr, rows, g.max_inject_rows, s_fc, ctx->scal, s);
+    if (st != DFLASH_OK) return st;
+  }
+  {
+    ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
+    DF_CHECK(launch_fc_norm(ctx, rows, s_fc, s));
+  }
+  const int s_kv = inject_splits(g, Nkv, d);
+  {
+    ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
+    dflash_status st =
+        run_gemm(ctx, ctx->w_kv_inj, Nkv, d, ctx->h_fused, ctx->h_lo, rows, g.max_inject_rows, s_kv, ctx->scal, s);
+    if (st != DFLASH_OK) return st;
+  }
+  {
+    ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
+    DF_CHECK(launch_inject_kv(ctx, rows, s_kv, s));
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_tokens, float* conf, float* logits,
+                                 int32_t* committed, dflash_stream stream) {
+  if (ctx == nullptr || draft_tokens == nullptr) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& g = ctx->cfg;
+  if (B < 1 || B > g.max_batch || (S != 1 && S != 2)) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t s = stream;
+  const int M = B * kBlockK, Mmax = g.max_batch * kBlockK;
+  const int d = g.hidden, F = g.ffn, qd = g.n_q_heads * g.head_dim, kvd = g.n_kv_heads * g.head_dim;
+  const int s_qkv = draft_splits(g, M, qd + 2 * kvd, d);
+  const int s_o = draft_splits(g, M, d, qd);
+  const int s_gu = draft_splits(g, M, 2 * F, d);
+  const int s_dn = draft_splits(g, M, d, F);
+  const int a_sp = attn_splits(ctx, B);
+#define DF_RUN(call)                        \
+  do {                                      \
+    const dflash_status st_ = (call);       \
+    if (st_ != DFLASH_OK) return st_;       \
+  } while (0)
+  for (int pass = 0; pass < S; ++pass) {
+    {
+      ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
+      DF_CHECK(launch_embed_norm(ctx, M, pass == 1, s));
+    }
+    for (int l = 0; l < g.n_layers; ++l) {
+      {
+        ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
+        DF_RUN(run_gemm(ctx, ctx->w_qkv[l], qd + 2 * kvd, d, ctx->a, ctx->a_lo, M, Mmax, s_qkv, nullptr, s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
+        DF_CHECK(launch_qkv_rope(ctx, M, s_qkv, s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_ATTN, 2, s);
+        DF_CHECK(launch_attention(ctx, l, B, a_sp, s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
+        DF_RUN(run_gemm(ctx, ctx->w_o[l], d, qd, ctx->o, ctx->o_lo, M, Mmax, s_o, nullptr, s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
+        DF_CHECK(launch_residual_norm(ctx, M, s_o, ctx->g_post[l], s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
+        DF_RUN(run_gemm(ctx, ctx->w_gu[l], 2 * F, d, ctx->a, ctx->a_lo, M, Mmax, s_gu, nullptr, s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
+        DF_CHECK(launch_swiglu(ctx, M, s_gu, s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
+        DF_RUN(run_gemm(ctx, ctx->w_down[l], d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, s));
+      }
+      {
+        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
+        DF_CHECK(launch_residual_norm(ctx, M, s_dn, l + 1 < g.n_layers ? ctx->g_in[l + 1] : ctx->g_final, s));
+      }
+    }
+    const int32_t* skip = pass == 1 ? ctx->commit : nullptr;
+    ProfScope plm(ctx, DFLASH_PROF_LMHEAD, g.dtype == DFLASH_BF16 ? 1 : 2, s);
+    if (g.dtype == DFLASH_BF16) {
+      GemmLaunch lm{};
+      lm.W = ctx->w_lm;
+      lm.X = ctx->a;
+      lm.X_lo = ctx->a_lo;
+      lm.N = g.vocab;
+      lm.K = d;
+      lm.M = M;
+      lm.M_alloc = Mmax;
+      lm.splits = 1;
+      lm.lm = ctx->lm;
+      lm.logits = logits;
+      lm.ld_logits = g.vocab;
+      lm.skip_rows = skip;
+      DF_CHECK(gemm_launch(ctx, lm, s));
+    } else {
+      GemmLaunch lm{};
+      lm.W = ctx->w_lm;
+      lm.X = ctx->a;
+      lm.N = g.vocab;
+      lm.K = d;
+      lm.M = M;
+      lm.M_alloc = Mmax;
+      lm.splits = 1;
+      lm.out = ctx->logits_ws;
+      lm.ldo = g.vocab;
+      DF_CHECK(gemm_launch(ctx, lm, s));
+      DF_CHECK(launch_logits_tiles(ctx, M, logits, skip, s));
+    }
+    plm.close();
+    ProfScope pm(ctx, DFLASH_PROF_ROWWISE, S == 2 && pass == 0 ? 2 : 1, s);
+    if (S == 1) {
+      DF_CHECK(launch_lm_merge(ctx, M, nullptr, draft_tokens, conf, s));
+    } else if (pass == 0) {
+      DF_CHECK(launch_lm_merge(ctx, M, nullptr, ctx->tok1, ctx->conf1, s));
+      DF_CHECK(launch_commit(ctx, B, s));
+    } else {
+      DF_CHECK(launch_lm_merge(ctx, M, ctx->commit, draft_tokens, conf, s));
+    }
+  }
+  if (committed != nullptr) {
+    if (S == 2)
+      DF_CHECK(cudaMemcpyAsync(committed, ctx->commit, sizeof(int32_t) * M, cudaMemcpyDeviceToDevice, s));
+    else
+      DF_CHECK(cudaMemsetAsync(committed, 0, sizeof(int32_t) * M, s));
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* draft_tokens,
+                            const int32_t* target_tokens, const float* target_logits, const float* draft_probs,
+                            float temperature, uint64_t seed, uint64_t round, int32_t* accept_len, int32_t* emitted,
+                            int32_t* n_emit, dflash_stream stream) {
+  if (ctx == nullptr || draft_tokens == nullptr || accept_len == nullptr || emitted == nullptr || n_emit == nullptr)
+    return DFLASH_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t s = stream;
+  if (mode == 0) {
+    if (target_tokens == nullptr) return DFLASH_ERR_INVALID_ARG;
+    ProfScope p(ctx, DFLASH_PROF_ACCEPT, 1, s);
+    DF_CHECK(launch_accept_greedy(B, kBlockK, draft_tokens, target_tokens, accept_len, emitted, n_emit, s));
+    return DFLASH_OK;
+  }
+  if (mode != 1 || target_logits == nullptr || !(temperature > 0.f)) return DFLASH_ERR_INVALID_ARG;
+  ProfScope p(ctx, DFLASH_PROF_ACCEPT, 1, s);
+  DF_CHECK(launch_accept_stochastic(B, kBlockK, ctx->cfg.vocab, draft_tokens, target_logits, draft_probs,
+                                    temperature, seed, round, accept_len, emitted, n_emit, s));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_gemm_bf16(const void* W, int N, int K, const void* X, const void* X_lo, int M, float* out,
+                               int splits, int* splits_used, int* status, dflash_stream stream) {
+  if (W == nullptr || X == nullptr || out == nullptr || status == nullptr || N < 1 || K < 8 || K % 8 || M < 1 ||
+      splits < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(W) % 16 || reinterpret_cast<uintptr_t>(X) % 16 ||
+      reinterpret_cast<uintptr_t>(X_lo) % 16)
+    return DFLASH_ERR_INVALID_ARG;
+  dflash_ctx tmp;
+  tmp.cfg = dflash_config{};
+  tmp.cfg.dtype = DFLASH_BF16;
+  tmp.status = status;
+  const int n_kb = gemm_kb(K);
+  const int want = std::min(splits, n_kb);
+  const int per = (n_kb + want - 1) / want;
+  const int s_used = (n_kb + per - 1) / per;
+  if (splits_used != nullptr) *splits_used = s_used;
+  GemmLaunch g{};
+  g.W = W;
+  g.X = X;
+  g.X_lo = X_lo;
+  g.N = N;
+  g.K = K;
+  g.M = M;
+  g.M_alloc = M;
+  g.splits = s_used;
+  g.out = out;
+  g.split_stride = static_cast<long long>(M) * N;
+  g.ldo = N;
+  DF_CHECK(gemm_launch(&tmp, g, stream));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_profile_enable(dflash_ctx* ctx, int enable) {
+  if (ctx == nullptr) return DFLASH_ERR_INVALID_ARG;
+  ctx->prof_on = enable != 0;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_profile_read(dflash_ctx* ctx, float* ms, int* launches, dflash_stream stream) {
+  if (ctx == nullptr || ms == nullptr || launches == nullptr) return DFLASH_ERR_INVALID_ARG;
+  for (int i = 0; i < DFLASH_PROF_CLASSES; ++i) {
+    ms[i] = 0.f;
+    launches[i] = 0;
+  }
+  DF_CHECK(cudaStreamSynchronize(stream));
+  for (auto& r : ctx->prof_live) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+      ms[r.cls] += t;
+      launches[r.cls] += r.launches;
+    }
+    ctx->prof_pool.push_back(r.a);
+    ctx->prof_pool.push_back(r.b);
+  }
+  ctx->prof_live.clear();
+  return DFLASH_OK;
+}
+
+dflash_status dflash_get_status(dflash_ctx* ctx, int* device_status, dflash_stream stream) {
+  if (ctx == nullptr || device_status == nullptr) return DFLASH_ERR_INVALID_ARG;
+  DF_CHECK(cudaMemcpyAsync(device_status, ctx->status, sizeof(int), cudaMemcpyDeviceToHost, stream));
+  DF_CHECK(cudaStreamSynchronize(stream));
+  return DFLASH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,44 @@
+// Launch interfaces of the non-GEMM kernels (defined in paging.cu,
+// pointwise.cu, attention.cu and accept.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace dflash {
+
+// paging.cu
+cudaError_t launch_reset(dflash_ctx* c, cudaStream_t s);
+cudaError_t launch_release(dflash_ctx* c, int b, cudaStream_t s);
+cudaError_t launch_truncate(dflash_ctx* c, int b, int new_len, cudaStream_t s);
+cudaError_t launch_alloc(dflash_ctx* c, const int32_t* n_rows, int first_seq, int B, int max_rows, cudaStream_t s);
+cudaError_t launch_rope_table(dflash_ctx* c, cudaStream_t s);
+
+// pointwise.cu (T = the config element type, chosen by c->cfg.dtype)
+cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, int max_rows, int first_seq,
+                               cudaStream_t s);
+cudaError_t launch_fc_norm(dflash_ctx* c, int rows, int splits, cudaStream_t s);
+cudaError_t launch_inject_kv(dflash_ctx* c, int rows, int splits, cudaStream_t s);
+cudaError_t launch_embed_norm(dflash_ctx* c, int M, bool second_pass, cudaStream_t s);
+cudaError_t launch_qkv_rope(dflash_ctx* c, int M, int splits, cudaStream_t s);
+cudaError_t launch_residual_norm(dflash_ctx* c, int M, int splits, const void* gain, cudaStream_t s);
+cudaError_t launch_swiglu(dflash_ctx* c, int M, int splits, cudaStream_t s);
+cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, cudaStream_t s);
+cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,
+                            cudaStream_t s);
+cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s);
+
+// attention.cu
+int attn_splits(dflash_ctx* c, int B);
+cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
+
+// accept.cu
+cudaError_t launch_accept_greedy(int B, int K, const int32_t* d, const int32_t* y, int32_t* tau, int32_t* emitted,
+                                 int32_t* n_emit, cudaStream_t s);
+cudaError_t launch_accept_stochastic(int B, int K, int V, const int32_t* d, const float* z, const float* q,
+                                     float temperature, uint64_t seed, uint64_t round, int32_t* tau,
+                                     int32_t* emitted, int32_t* n_emit, cudaStream_t s);
+
+}  // namespace dflash
