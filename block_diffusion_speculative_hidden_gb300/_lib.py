@@ -13,14 +13,15 @@ LIB_PATH = os.path.join(_HERE, "libdflash.so")
 
 DFLASH_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "pool exhausted",
-                4: "CUDA error", 5: "device status set", 6: "workspace too small"}
+                4: "CUDA error", 5: "device status set", 6: "workspace too small",
+                7: "too large for the fixed scratch"}
 DEV_POOL_EXHAUSTED, DEV_SEQ_TOO_LONG, DEV_WAIT_TIMEOUT, DEV_BAD_TOKEN, DEV_BAD_ROWS = 1, 2, 4, 8, 16
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 EXPORTED = ("dflash_workspace_size", "dflash_kv_pool_size", "dflash_create", "dflash_destroy",
             "dflash_reset", "dflash_release", "dflash_inject_kv", "dflash_draft_block",
             "dflash_accept", "dflash_get_status", "dflash_status_string", "dflash_gemm_bf16",
-            "dflash_profile_enable", "dflash_profile_read", "dflash_truncate")
+            "dflash_profile_enable", "dflash_profile_read", "dflash_truncate", "dflash_gemm_bf16_noalloc")
 PROF_CLASSES = ("proj", "lm_head", "inject", "attention", "rowwise", "accept")
 
 
@@ -83,6 +84,9 @@ def lib() -> ctypes.CDLL:
         L.dflash_gemm_bf16.restype = ctypes.c_int
         L.dflash_gemm_bf16.argtypes = [_VP, ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int, _VP, ctypes.c_int,
                                        ctypes.POINTER(ctypes.c_int), _VP, _VP]
+        L.dflash_gemm_bf16_noalloc.restype = ctypes.c_int
+        L.dflash_gemm_bf16_noalloc.argtypes = [_VP, ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int, _VP,
+                                               ctypes.c_int, ctypes.POINTER(ctypes.c_int), _VP, _VP]
         L.dflash_profile_enable.restype = ctypes.c_int
         L.dflash_profile_enable.argtypes = [_VP, ctypes.c_int]
         L.dflash_profile_read.restype = ctypes.c_int

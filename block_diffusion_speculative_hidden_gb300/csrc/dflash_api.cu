@@ -240,6 +240,7 @@ const char* dflash_status_string(dflash_status s) {
     case DFLASH_ERR_CUDA: return "CUDA error";
     case DFLASH_ERR_STATE: return "device status word set";
     case DFLASH_ERR_WORKSPACE: return "workspace or pool buffer too small";
+    case DFLASH_ERR_TOO_LARGE: return "request exceeds the fixed scratch of the no-allocation entry point";
   }
   return "unknown";
 }

@@ -392,4 +392,37 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s) {
   return launch_tc_bn<false>(c, g, bn, tw, tx, tx, s);
 }
 
+// ---------------------------------------------------------------- launch without a map cache
+
+// The same projection launch with both tensor maps encoded on the stack: no
+// map cache and no host heap, for the entry point that must not allocate.
+static bool encode_tmap_bf16(const void* ptr, int rows, int cols, int box_rows, CUtensorMap* out) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estride[2] = {1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t gemm_launch_uncached(int* status, const GemmLaunch& g, cudaStream_t s) {
+  dflash_ctx tmp;  // holds only the status pointer; its containers stay empty
+  tmp.cfg = dflash_config{};
+  tmp.cfg.dtype = DFLASH_BF16;
+  tmp.status = status;
+  const bool split = g.X_lo != nullptr;
+  const int bn = gemm_bn(g.M, split);
+  CUtensorMap tw, tx, txlo;
+  if (!encode_tmap_bf16(g.W, g.N, g.K, kTileN, &tw) || !encode_tmap_bf16(g.X, g.M_alloc, g.K, bn, &tx))
+    return cudaErrorInvalidValue;
+  if (split) {
+    if (!encode_tmap_bf16(g.X_lo, g.M_alloc, g.K, bn, &txlo)) return cudaErrorInvalidValue;
+    return launch_tc_bn<true>(&tmp, g, bn, tw, tx, txlo, s);
+  }
+  return launch_tc_bn<false>(&tmp, g, bn, tw, tx, tx, s);
+}
+
 }  // namespace dflash

@@ -103,5 +103,6 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
 int choose_splits(int n_tiles, int n_kb);
 int gemm_kb(int K);
 int gemm_bn(int M, bool split);
+cudaError_t gemm_launch_uncached(int* status, const GemmLaunch& g, cudaStream_t s);
 
 }  // namespace dflash

@@ -57,7 +57,8 @@ typedef enum {
   DFLASH_ERR_POOL_EXHAUSTED = 3,    /* (status word bit 1) */
   DFLASH_ERR_CUDA = 4,              /* a CUDA runtime call failed */
   DFLASH_ERR_STATE = 5,             /* the device status word is non-zero */
-  DFLASH_ERR_WORKSPACE = 6          /* workspace or pool buffer too small */
+  DFLASH_ERR_WORKSPACE = 6,         /* workspace or pool buffer too small */
+  DFLASH_ERR_TOO_LARGE = 7          /* request exceeds the fixed scratch of dflash_gemm_bf16_noalloc */
 } dflash_status;
 
 /* Bits of the device status word (dflash_get_status). */
@@ -230,6 +231,33 @@ dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* dra
  * three calls above, exposed so it can be checked on its own. */
 dflash_status dflash_gemm_bf16(const void* W, int N, int K, const void* X, const void* X_lo, int M, float* out,
                                int splits, int* splits_used, int* status, dflash_stream stream);
+
+/* dflash_gemm_bf16 for callers that cannot allocate device memory.  Some
+ * callers must not call cudaMalloc or have it called on their behalf: a
+ * process whose HBM is handed in full to another allocator up front (a
+ * framework's caching allocator, a serving engine's KV reserve), where an
+ * extra allocation fails or fragments that memory, or code that cannot take
+ * cudaMalloc's implicit device synchronisation.  No counterpart on the
+ * pages: it is a packaging of the projection kernel, not a step of the
+ * method.
+ *
+ * out (device fp32 [M, N], caller-owned) = (X + X_lo) . W^T summed over all
+ * k-blocks; W, X, X_lo and splits as for dflash_gemm_bf16 (splits_used:
+ * host, nullable).  The split-K partials live in a fixed 8 MiB array inside
+ * the library (a __device__ object that every GPU loading the library holds
+ * until exit): splits_used * M * N must not exceed 2^21 - 64 floats, else
+ * DFLASH_ERR_TOO_LARGE and nothing is enqueued.  status: device int32
+ * (caller-owned) or NULL to use a slot in that array, cleared by each call.
+ * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ * library routine).  Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents, so calls whose work overlaps on the GPU
+ * (different streams, or host threads) race; serialise them.  Asynchronous
+ * on `stream`. */
+dflash_status dflash_gemm_bf16_noalloc(const void* W, int N, int K, const void* X, const void* X_lo, int M,
+                                       float* out, int splits, int* splits_used, int* status,
+                                       dflash_stream stream);
 
 /* Kernel timing classes of dflash_profile_read. */
 #define DFLASH_PROF_PROJ 0      /* draft-layer projections (QKV, O, gate/up, down) */
