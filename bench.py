@@ -47,6 +47,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reset-every", type=int, default=16,
                     help="roll each sequence back to its prompt length every N rounds")
+    ap.add_argument("--kernel", choices=["gemm"], default=None,
+                    help="time one kernel alone on the workload's shapes (small case for profilers)")
     return ap.parse_args(argv)
 
 
@@ -152,7 +154,7 @@ def algorithmic_bytes(cfg):
     """Bytes the hot path must move per round (B sequences), by kernel class.
 
     Projections: bf16 weights once + activations in (hi+lo bf16, 4 B/elem) +
-    fp32 results out.  Attention: the fp32 context K/V of every layer once.
+    fp32 results out.  Attention (kv_bytes): the K/V of every layer once.
     Inject: FC and K/V weights + the new rows; accept: tokens only."""
     B, d, F, V, L = cfg.batch, cfg.hidden, cfg.ffn, cfg.vocab, cfg.n_layers
     qd, kvd = cfg.q_dim, cfg.kv_dim
@@ -161,14 +163,17 @@ def algorithmic_bytes(cfg):
     def proj(N, Kd, m=M):
         return N * Kd * 2 + m * Kd * 4 + m * N * 4
 
-    per_layer = proj(qd + 2 * kvd, d) + proj(d, qd) + proj(2 * F, d) + proj(d, F)
+    Fp = 64 * -(-F // 64)                     # gate/up rows are packed in groups of 64
+    per_layer = proj(qd + 2 * kvd, d) + proj(d, qd) + proj(2 * Fp, d) + proj(d, F)
     return {"proj": L * per_layer * cfg.s_passes,
             "lm_head": (V * d * 2 + M * d * 4) * cfg.s_passes,
             "inject_weights": d * cfg.feat_dim * 2 + 2 * L * kvd * d * 2}
 
 
 def kv_bytes(cfg, ctx_len):
-    return cfg.n_layers * 2 * cfg.kv_dim * 4 * ctx_len * cfg.batch * cfg.s_passes
+    """K and V of every layer read once per pass: fp16 for bf16 workloads, fp32 otherwise."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    return cfg.n_layers * 2 * cfg.kv_dim * e * (ctx_len + K_BLOCK) * cfg.batch * cfg.s_passes
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -413,11 +418,51 @@ def config_block(cfg, lens):
                   f"({(algorithmic_bytes(cfg)['proj'] + algorithmic_bytes(cfg)['lm_head']) / 1e9:.2f} GB) from HBM"}
 
 
+# --------------------------------------------------------------------------- single kernels
+
+def run_kernel_gemm(args, cfg):
+    """The gate/up projection of one draft layer alone: W [2F, d] bf16,
+    16 activation rows as a hi+lo pair, split-K as the library sizes it."""
+    import torch
+    from block_diffusion_speculative_hidden_gb300 import gemm_bf16
+    N, K, M = 2 * cfg.ffn, cfg.hidden, cfg.batch * K_BLOCK
+    g = torch.Generator(device="cuda").manual_seed(0)
+    W = (torch.randn((N, K), device="cuda", generator=g) * 0.02).bfloat16()
+    x = torch.randn((M, K), device="cuda", generator=g)
+    hi = x.bfloat16()
+    lo = (x - hi.float()).bfloat16()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_tiles, n_kb = -(-N // 128), -(-K // 64)
+    splits = max(1, min(2 * sms // n_tiles, max(1, n_kb // 4)))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        gemm_bf16(W, hi, splits=splits, X_lo=lo)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gemm_bf16(W, hi, splits=splits, X_lo=lo)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = float(np.median(times))
+    byts = N * K * 2 + M * K * 4 + M * N * 4
+    hbm, _, kind = load_peaks()
+    print(json.dumps({"kernel": "k_gemm_tc (gate/up, M=16 hi+lo)", "N": N, "K": K, "M": M, "splits": splits,
+                      "us": ms * 1e3, "GB_per_s": byts / (ms / 1e3) / 1e9,
+                      "frac_hbm": byts / (ms / 1e3) / 1e9 / hbm, "peak": f"{kind} {hbm}"}), flush=True)
+
+
 # --------------------------------------------------------------------------- main
 
 def main(argv=None):
     args = parse_args(argv)
     cfg = synth.get_config(args.config)
+    if args.kernel == "gemm":
+        run_kernel_gemm(args, cfg)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, cfg, world, rank)
@@ -435,7 +480,9 @@ def main(argv=None):
     gemm_bytes = (ab["proj"] + ab["lm_head"]) * steps
     achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
     per_class = {k: {"ms_per_step": v[0] / steps, "launches_per_step": v[1] / steps} for k, v in prof.items()}
-    attn_bytes = kv_bytes(cfg, int(lens.mean()) + 8) * steps
+    # the context grows by tau+1 per round and is rolled back every reset_every rounds
+    mean_ctx = float(lens.mean()) + 0.5 * max(args.reset_every, 1) * (res["mean_tau"] + 1)
+    attn_bytes = kv_bytes(cfg, int(mean_ctx)) * steps
     if prof["attention"][0] > 0:
         per_class["attention"]["GB_per_s"] = attn_bytes / (prof["attention"][0] / 1e3) / 1e9
     per_class["proj"]["GB_per_s"] = ab["proj"] * steps / (prof["proj"][0] / 1e3) / 1e9

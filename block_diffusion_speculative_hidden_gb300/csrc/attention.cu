@@ -11,6 +11,7 @@
 // (o, m, l) partial and a second kernel merges the splits.  No CTA waits on
 // another.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -29,13 +30,13 @@ struct AttnCfg {
   static constexpr int SMEM = sizeof(float) * (R * (DH + 1) + 2 * kChunk * (DH + 1) + R * (kChunk + 1) + R);
 };
 
-template <int DH, int G>
+// KT: element type of q and of the KV pool.  The block's own keys sit in
+// page block_page0 + b of the pool, after the T_b context keys.
+template <typename KT, int DH, int G>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_split(
-    const float* __restrict__ q, const float* __restrict__ kblk, const float* __restrict__ vblk,
-    const float* __restrict__ pool_k, const float* __restrict__ pool_v, const int32_t* __restrict__ page_table,
-    int max_pages,
-    const int32_t* __restrict__ seq_len, float* __restrict__ part_o, float* __restrict__ part_ml, int Hkv,
-    int splits, float scale) {
+    const KT* __restrict__ q, const KT* __restrict__ pool_k, const KT* __restrict__ pool_v,
+    const int32_t* __restrict__ page_table, int max_pages, int block_page0, const int32_t* __restrict__ seq_len,
+    float* __restrict__ part_o, float* __restrict__ part_ml, int Hkv, int splits, float scale) {
   using C = AttnCfg<DH, G>;
   constexpr int R = C::R;
   extern __shared__ float sm[];
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(
 
   const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Hq = Hkv * G, qd = Hq * DH, kvd = Hkv * DH;
+  const int Hq = Hkv * G, qd = Hq * DH;
   const int T_ctx = seq_len[b];
   const int n_keys = T_ctx + kBlockK;
   const int n_chunks = (n_keys + kChunk - 1) / kChunk;
@@ -57,7 +58,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(
   // q rows: r = gi * 16 + i  <->  q head kvh*G + gi, block position i; pre-scaled by 1/sqrt(dh)
   for (int e = tid; e < R * DH; e += kAttnThreads) {
     const int r = e / DH, dd = e % DH, gi = r / kBlockK, i = r % kBlockK;
-    sQ[r * (DH + 1) + dd] = q[static_cast<long long>(b * kBlockK + i) * qd + (kvh * G + gi) * DH + dd] * scale;
+    sQ[r * (DH + 1) + dd] =
+        to_f32(q[static_cast<long long>(b * kBlockK + i) * qd + (kvh * G + gi) * DH + dd]) * scale;
   }
   float m_run[C::RPW], l_run[C::RPW];
 #pragma unroll
@@ -76,15 +78,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(
     for (int e = tid; e < kChunk * DH; e += kAttnThreads) {
       const int j = e / DH, dd = e % DH, key = key0 + j;
       float kv = 0.f, vv = 0.f;
-      if (key < T_ctx) {
-        const int page = page_table[b * max_pages + key / kPage];
-        const long long off = (static_cast<long long>(page) * Hkv + kvh) * (kPage * DH) + (key % kPage) * DH + dd;
-        kv = pool_k[off];
-        vv = pool_v[off];
-      } else if (key < n_keys) {
-        const long long off = static_cast<long long>(b * kBlockK + key - T_ctx) * kvd + kvh * DH + dd;
-        kv = kblk[off];
-        vv = vblk[off];
+      if (key < n_keys) {
+        const int page = key < T_ctx ? page_table[b * max_pages + key / kPage] : block_page0 + b;
+        const int slot = key < T_ctx ? key % kPage : key - T_ctx;
+        const long long off = (static_cast<long long>(page) * Hkv + kvh) * (kPage * DH) + slot * DH + dd;
+        kv = to_f32(pool_k[off]);
+        vv = to_f32(pool_v[off]);
       }
       sK[j * (DH + 1) + dd] = kv;
       sV[j * (DH + 1) + dd] = vv;
@@ -154,28 +153,33 @@ __global__ void k_attn_combine(const float* __restrict__ part_o, const float* __
   }
 }
 
+// Key splits per (sequence, kv head): enough CTAs for about two per SM; the
+// tensor-core kernel merges its splits inside one cluster, so at most 8.
 int attn_splits(dflash_ctx* c, int B) {
   const int heads = B * c->cfg.n_kv_heads;
   int s = (2 * c->num_sms + heads - 1) / heads;
+  if (c->cfg.dtype == DFLASH_BF16) s = std::min(s, 8);
   return std::max(1, std::min(s, c->attn_max_splits));
 }
 
 template <typename T, int DH, int G>
 static cudaError_t launch_attn_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
   using C = AttnCfg<DH, G>;
+  using KT = typename std::conditional<std::is_same<T, float>::value, float, __half>::type;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_split<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_attn_split<KT, DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const auto& g = c->cfg;
-  const long long layer_off = static_cast<long long>(layer) * g.n_pages * g.n_kv_heads * kPage * DH;
+  const long long layer_off = static_cast<long long>(layer) * c->pool_pages * g.n_kv_heads * kPage * DH;
   dim3 grid(splits, g.n_kv_heads, B);
-  k_attn_split<DH, G><<<grid, kAttnThreads, C::SMEM, s>>>(
-      c->q, c->kblk, c->vblk, static_cast<const float*>(c->pool_k) + layer_off,
-      static_cast<const float*>(c->pool_v) + layer_off, c->page_table,
-      g.max_pages_per_seq, c->seq_len, c->attn_o, c->attn_ml, g.n_kv_heads, splits, 1.0f / sqrtf(static_cast<float>(DH)));
+  k_attn_split<KT, DH, G><<<grid, kAttnThreads, C::SMEM, s>>>(
+      static_cast<const KT*>(c->q), static_cast<const KT*>(c->pool_k) + layer_off,
+      static_cast<const KT*>(c->pool_v) + layer_off, c->page_table, g.max_pages_per_seq, g.n_pages, c->seq_len,
+      c->attn_o, c->attn_ml, g.n_kv_heads, splits, 1.0f / sqrtf(static_cast<float>(DH)));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_attn_combine<T><<<B * kBlockK, 256, 0, s>>>(c->attn_o, c->attn_ml,
@@ -205,8 +209,10 @@ static cudaError_t launch_attn_ty(dflash_ctx* c, int layer, int B, int splits, c
   }
 }
 
+// fp32 workloads: the fp32 SIMT kernel above; bf16 workloads (fp16 pool):
+// the tensor-core kernel of attention_tc.cu.
 cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
-  if (c->cfg.dtype == DFLASH_BF16) return launch_attn_ty<__nv_bfloat16>(c, layer, B, splits, s);
+  if (c->cfg.dtype == DFLASH_BF16) return launch_attention_tc(c, layer, B, splits, s);
   return launch_attn_ty<float>(c, layer, B, splits, s);
 }
 

@@ -18,19 +18,31 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 int elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 4; }
+// q and the KV pool: fp16 for bf16 workloads, fp32 for fp32 workloads
+int kv_elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 4; }
+
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+// Concurrent CTA slots of the projection kernel: tiles up to 64 rows wide
+// fit two CTAs per SM, wider ones one.
+int gemm_slots(int num_sms, int bn) { return num_sms * (bn <= 64 ? 2 : 1); }
+
 // Split count of one draft-side GEMM for M activation rows (hi/lo inputs).
-int draft_splits(const dflash_config& g, int M, int N, int K) {
+int draft_splits(const dflash_config& g, int num_sms, int M, int N, int K) {
   if (g.dtype != DFLASH_BF16) return 1;
-  const int tiles = ceil_div(N, kTileN) * ceil_div(M, gemm_bn(M, true));
-  return choose_splits(tiles, gemm_kb(K));
+  const int bn = gemm_bn(M, true);
+  const int tiles = ceil_div(N, kTileN) * ceil_div(M, bn);
+  return choose_splits(tiles, gemm_kb(K), gemm_slots(num_sms, bn));
 }
 // Split count of an inject-side GEMM: independent of the row count, so a
 // row's result does not depend on how many rows share the call.
-int inject_splits(const dflash_config& g, int N, int K) {
+int inject_splits(const dflash_config& g, int num_sms, int N, int K) {
   if (g.dtype != DFLASH_BF16) return 1;
-  return choose_splits(ceil_div(N, kTileN), gemm_kb(K));
+  return choose_splits(ceil_div(N, kTileN), gemm_kb(K), gemm_slots(num_sms, 32));
 }
+
+// Rows of the packed gate/up weight: groups of 64 features, 64 gate rows then
+// the 64 matching up rows, the last group zero-padded.
+int gu_rows(int F) { return 128 * ceil_div(F, 64); }
 
 int attn_max_splits_for(const dflash_config& g, int num_sms) {
   const int max_keys = g.max_pages_per_seq * kPage + kBlockK;
@@ -47,6 +59,7 @@ bool config_ok(const dflash_config* g) {
   const int G = g->n_q_heads / g->n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return false;
   if (g->head_dim != 32 && g->head_dim != 64 && g->head_dim != 128) return false;
+  if (g->dtype == DFLASH_BF16 && g->head_dim == 32) return false;  // the fp16 attention tiles 64-wide
   if (g->ffn < 8 || g->vocab < 2 || g->mask_id < 0 || g->mask_id >= g->vocab) return false;
   if (g->n_taps < 1 || g->tap_width < 1) return false;
   if (g->max_batch < 1 || g->max_batch > 4096 || g->max_pages_per_seq < 1 || g->n_pages < 1) return false;
@@ -78,16 +91,12 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   const int Fin = g.n_taps * g.tap_width, V = g.vocab, L = g.n_layers;
   const int n_lm_tiles = ceil_div(V, kTileN);
   const int rope_rows = g.max_pages_per_seq * kPage + kBlockK;
-  // largest split-K partial
-  size_t part = static_cast<size_t>(inject_splits(g, d, Fin)) * R * d;
-  part = std::max(part, static_cast<size_t>(inject_splits(g, 2 * L * kvd, d)) * R * 2 * L * kvd);
-  for (int B = 1; B <= g.max_batch; ++B) {
-    const int Mb = B * kBlockK;
-    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, qd + 2 * kvd, d)) * Mb * (qd + 2 * kvd));
-    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, d, qd)) * Mb * d);
-    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, 2 * F, d)) * Mb * 2 * F);
-    part = std::max(part, static_cast<size_t>(draft_splits(g, Mb, d, F)) * Mb * d);
-  }
+  const int Ngu = gu_rows(F), Nkv = 2 * L * kvd, Nqkv = qd + 2 * kvd;
+  // fp32 projection outputs: the FC output u; for fp32 workloads also the
+  // staging of every projection before its epilogue
+  size_t yf = R * d;
+  if (g.dtype == DFLASH_F32)
+    yf = std::max({yf, R * static_cast<size_t>(Nkv), M * static_cast<size_t>(std::max({Nqkv, Ngu, d}))});
   const int G = g.n_q_heads / g.n_kv_heads;
   const int amax = attn_max_splits_for(g, num_sms);
   const size_t attn_rows = static_cast<size_t>(g.max_batch) * g.n_kv_heads * amax * G * kBlockK;
@@ -103,13 +112,11 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   void* fc_in = w.take(R * Fin * e);
   void* h_fused = w.take(R * d * e);
   void* h_lo = lo ? w.take(R * d * e) : nullptr;
-  auto partp = static_cast<float*>(w.take(sizeof(float) * part));
+  auto y = static_cast<float*>(w.take(sizeof(float) * yf));
   auto x = static_cast<float*>(w.take(sizeof(float) * M * d));
   void* a = w.take(M * d * e);
   void* a_lo = lo ? w.take(M * d * e) : nullptr;
-  auto q = static_cast<float*>(w.take(sizeof(float) * M * qd));
-  auto kb = static_cast<float*>(w.take(sizeof(float) * M * kvd));
-  auto vb = static_cast<float*>(w.take(sizeof(float) * M * kvd));
+  void* q = w.take(M * qd * kv_elem_bytes(g));
   void* o = w.take(M * qd * e);
   void* o_lo = lo ? w.take(M * qd * e) : nullptr;
   void* act = w.take(M * F * e);
@@ -136,14 +143,11 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
     c->fc_in = fc_in;
     c->h_fused = h_fused;
     c->h_lo = h_lo;
-    c->part = partp;
-    c->part_floats = part;
+    c->y = y;
     c->x = x;
     c->a = a;
     c->a_lo = a_lo;
     c->q = q;
-    c->kblk = kb;
-    c->vblk = vb;
     c->o = o;
     c->o_lo = o_lo;
     c->act = act;
@@ -172,8 +176,14 @@ int device_sms() {
     if ((call) != cudaSuccess) return DFLASH_ERR_CUDA; \
   } while (0)
 
+#define DF_RUN(call)                  \
+  do {                                \
+    const dflash_status st_ = (call); \
+    if (st_ != DFLASH_OK) return st_; \
+  } while (0)
+
 dflash_status run_gemm(dflash_ctx* c, const void* W, int N, int K, const void* X, const void* X_lo, int M,
-                       int M_alloc, int splits, const int* m_valid, cudaStream_t s) {
+                       int M_alloc, int splits, const int* m_valid, const EpiArgs& epi, cudaStream_t s) {
   GemmLaunch g{};
   g.W = W;
   g.X = X;
@@ -182,13 +192,32 @@ dflash_status run_gemm(dflash_ctx* c, const void* W, int N, int K, const void* X
   g.K = K;
   g.M = M;
   g.M_alloc = M_alloc;
-  g.splits = splits;
-  g.out = c->part;
+  g.splits = c->cfg.dtype == DFLASH_BF16 ? splits : 1;
+  g.out = c->cfg.dtype == DFLASH_BF16 ? nullptr : c->y;  // fp32 staging (bf16: epilogues write directly)
   g.split_stride = static_cast<long long>(M) * N;
   g.ldo = N;
   g.m_valid = m_valid;
+  g.epi = epi;
   DF_CHECK(gemm_launch(c, g, s));
   return DFLASH_OK;
+}
+
+EpiArgs epi_base(dflash_ctx* c, int kind, int M, int N) {
+  EpiArgs e{};
+  e.kind = kind;
+  e.M = M;
+  e.N = N;
+  e.Hq = c->cfg.n_q_heads;
+  e.Hkv = c->cfg.n_kv_heads;
+  e.dh = c->cfg.head_dim;
+  e.rope_cos = c->rope_cos;
+  e.rope_sin = c->rope_sin;
+  return e;
+}
+
+char* pool_layer(void* pool, const dflash_ctx* c, int layer) {
+  const long long per_layer = static_cast<long long>(c->pool_pages) * c->cfg.n_kv_heads * kPage * c->cfg.head_dim;
+  return static_cast<char*>(pool) + per_layer * layer * c->kv_elem;
 }
 
 // Brackets the launches between its construction and destruction with a
@@ -252,7 +281,8 @@ size_t dflash_workspace_size(const dflash_config* cfg) {
 
 size_t dflash_kv_pool_size(const dflash_config* cfg) {
   if (!config_ok(cfg)) return 0;
-  return 2ull * cfg->n_layers * cfg->n_pages * cfg->n_kv_heads * kPage * cfg->head_dim * sizeof(float);
+  return 2ull * cfg->n_layers * (cfg->n_pages + cfg->max_batch) * cfg->n_kv_heads * kPage * cfg->head_dim *
+         kv_elem_bytes(*cfg);
 }
 
 dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, void* kv_pool, size_t kv_pool_bytes,
@@ -296,13 +326,18 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, v
   c->w_down.assign(w->w_down, w->w_down + cfg->n_layers);
   c->g_in.assign(w->g_in, w->g_in + cfg->n_layers);
   c->g_post.assign(w->g_post, w->g_post + cfg->n_layers);
+  c->pool_pages = cfg->n_pages + cfg->max_batch;
+  c->kv_elem = kv_elem_bytes(*cfg);
   const size_t half_pool = dflash_kv_pool_size(cfg) / 2;
   c->pool_k = kv_pool;
   c->pool_v = static_cast<char*>(kv_pool) + half_pool;
   c->page_table = page_table;
   c->seq_len = seq_len;
   layout(*cfg, sms, c, static_cast<char*>(workspace));
-  if (launch_rope_table(c, nullptr) != cudaSuccess || launch_reset(c, nullptr) != cudaSuccess ||
+  // zero the pool once: attention multiplies masked (zero-probability) slots
+  // by their values, which must therefore be finite
+  if (cudaMemsetAsync(kv_pool, 0, dflash_kv_pool_size(cfg), nullptr) != cudaSuccess ||
+      launch_rope_table(c, nullptr) != cudaSuccess || launch_reset(c, nullptr) != cudaSuccess ||
       cudaStreamSynchronize(nullptr) != cudaSuccess) {
     delete c;
     return DFLASH_ERR_CUDA;
@@ -357,27 +392,33 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t
     DF_CHECK(launch_alloc(ctx, n_rows, first_seq, B, max_rows, s));
     DF_CHECK(launch_gather_rows(ctx, feats, rows, max_rows, first_seq, s));
   }
-  const int s_fc = inject_splits(g, d, Fin);
+  const int s_fc = inject_splits(g, ctx->num_sms, d, Fin);
   {
     ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
-    dflash_status st =
-        run_gemm(ctx, ctx->w_fc, d, Fin, ctx->fc_in, nullptr, rows, g.max_inject_rows, s_fc, ctx->scal, s);
-    if (st != DFLASH_OK) return st;
+    EpiArgs e = epi_base(ctx, EPI_STORE, rows, d);
+    e.m_valid = ctx->scal;
+    e.out = ctx->y;
+    DF_RUN(run_gemm(ctx, ctx->w_fc, d, Fin, ctx->fc_in, nullptr, rows, g.max_inject_rows, s_fc, ctx->scal, e, s));
   }
   {
     ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-    DF_CHECK(launch_fc_norm(ctx, rows, s_fc, s));
+    DF_CHECK(launch_fc_norm(ctx, rows, s));
   }
-  const int s_kv = inject_splits(g, Nkv, d);
+  const int s_kv = inject_splits(g, ctx->num_sms, Nkv, d);
   {
     ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
-    dflash_status st =
-        run_gemm(ctx, ctx->w_kv_inj, Nkv, d, ctx->h_fused, ctx->h_lo, rows, g.max_inject_rows, s_kv, ctx->scal, s);
-    if (st != DFLASH_OK) return st;
-  }
-  {
-    ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-    DF_CHECK(launch_inject_kv(ctx, rows, s_kv, s));
+    EpiArgs e = epi_base(ctx, EPI_KV_INJECT, rows, Nkv);
+    e.m_valid = ctx->scal;
+    e.pool_k = ctx->pool_k;
+    e.pool_v = ctx->pool_v;
+    e.layer_stride = static_cast<long long>(ctx->pool_pages) * g.n_kv_heads * kPage * g.head_dim;
+    e.row_seq = ctx->row_seq;
+    e.row_pos = ctx->row_pos;
+    e.page_table = ctx->page_table;
+    e.max_pages = g.max_pages_per_seq;
+    e.key_offset = ctx->key_offset;
+    DF_RUN(run_gemm(ctx, ctx->w_kv_inj, Nkv, d, ctx->h_fused, ctx->h_lo, rows, g.max_inject_rows, s_kv, ctx->scal,
+                    e, s));
   }
   return DFLASH_OK;
 }
@@ -390,16 +431,13 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
   cudaStream_t s = stream;
   const int M = B * kBlockK, Mmax = g.max_batch * kBlockK;
   const int d = g.hidden, F = g.ffn, qd = g.n_q_heads * g.head_dim, kvd = g.n_kv_heads * g.head_dim;
-  const int s_qkv = draft_splits(g, M, qd + 2 * kvd, d);
-  const int s_o = draft_splits(g, M, d, qd);
-  const int s_gu = draft_splits(g, M, 2 * F, d);
-  const int s_dn = draft_splits(g, M, d, F);
+  const int sms = ctx->num_sms;
+  const int Nqkv = qd + 2 * kvd, Ngu = gu_rows(F);
+  const int s_qkv = draft_splits(g, sms, M, Nqkv, d);
+  const int s_o = draft_splits(g, sms, M, d, qd);
+  const int s_gu = draft_splits(g, sms, M, Ngu, d);
+  const int s_dn = draft_splits(g, sms, M, d, F);
   const int a_sp = attn_splits(ctx, B);
-#define DF_RUN(call)                        \
-  do {                                      \
-    const dflash_status st_ = (call);       \
-    if (st_ != DFLASH_OK) return st_;       \
-  } while (0)
   for (int pass = 0; pass < S; ++pass) {
     {
       ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
@@ -408,39 +446,45 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
     for (int l = 0; l < g.n_layers; ++l) {
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
-        DF_RUN(run_gemm(ctx, ctx->w_qkv[l], qd + 2 * kvd, d, ctx->a, ctx->a_lo, M, Mmax, s_qkv, nullptr, s));
+        EpiArgs e = epi_base(ctx, EPI_QKV, M, Nqkv);
+        e.q = ctx->q;
+        e.pool_k = pool_layer(ctx->pool_k, ctx, l);
+        e.pool_v = pool_layer(ctx->pool_v, ctx, l);
+        e.block_page0 = g.n_pages;
+        e.seq_len = ctx->seq_len;
+        DF_RUN(run_gemm(ctx, ctx->w_qkv[l], Nqkv, d, ctx->a, ctx->a_lo, M, Mmax, s_qkv, nullptr, e, s));
       }
       {
-        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-        DF_CHECK(launch_qkv_rope(ctx, M, s_qkv, s));
-      }
-      {
-        ProfScope p(ctx, DFLASH_PROF_ATTN, 2, s);
+        ProfScope p(ctx, DFLASH_PROF_ATTN, g.dtype == DFLASH_BF16 ? 1 : 2, s);
         DF_CHECK(launch_attention(ctx, l, B, a_sp, s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
-        DF_RUN(run_gemm(ctx, ctx->w_o[l], d, qd, ctx->o, ctx->o_lo, M, Mmax, s_o, nullptr, s));
+        EpiArgs e = epi_base(ctx, EPI_RESIDUAL, M, d);
+        e.out = ctx->x;
+        DF_RUN(run_gemm(ctx, ctx->w_o[l], d, qd, ctx->o, ctx->o_lo, M, Mmax, s_o, nullptr, e, s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-        DF_CHECK(launch_residual_norm(ctx, M, s_o, ctx->g_post[l], s));
+        DF_CHECK(launch_rmsnorm_rows(ctx, M, ctx->g_post[l], s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
-        DF_RUN(run_gemm(ctx, ctx->w_gu[l], 2 * F, d, ctx->a, ctx->a_lo, M, Mmax, s_gu, nullptr, s));
-      }
-      {
-        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-        DF_CHECK(launch_swiglu(ctx, M, s_gu, s));
+        EpiArgs e = epi_base(ctx, EPI_SWIGLU, M, Ngu);
+        e.act_hi = ctx->act;
+        e.act_lo = ctx->act_lo;
+        e.F = F;
+        DF_RUN(run_gemm(ctx, ctx->w_gu[l], Ngu, d, ctx->a, ctx->a_lo, M, Mmax, s_gu, nullptr, e, s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
-        DF_RUN(run_gemm(ctx, ctx->w_down[l], d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, s));
+        EpiArgs e = epi_base(ctx, EPI_RESIDUAL, M, d);
+        e.out = ctx->x;
+        DF_RUN(run_gemm(ctx, ctx->w_down[l], d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, e, s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-        DF_CHECK(launch_residual_norm(ctx, M, s_dn, l + 1 < g.n_layers ? ctx->g_in[l + 1] : ctx->g_final, s));
+        DF_CHECK(launch_rmsnorm_rows(ctx, M, l + 1 < g.n_layers ? ctx->g_in[l + 1] : ctx->g_final, s));
       }
     }
     const int32_t* skip = pass == 1 ? ctx->commit : nullptr;

@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace dflash {
@@ -39,16 +40,19 @@ struct TcCfg {
   static constexpr int SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/ +
                               3 * 4 * BN * 4 /*LM-head reduction*/;
   static_assert(STAGES >= 2, "pipeline too shallow");
+  // the own tile plus the reduced slice (at most half the rows, splits >= 2) fit in the stage ring
+  static_assert(BN * 128 * 4 * 3 / 2 <= STAGES * STAGE_BYTES, "epilogue tiles must fit in the stage ring");
 };
 
 struct TcParams {
   int M, N;
-  int n_kb, kb_per_split;
-  float* out;
+  int n_kb, kb_per_split, splits;
+  float* out;  // split-K partial planes [splits][M][ldo]
   long long split_stride;
   int ldo;
   const int* m_valid;
   int* status;
+  EpiArgs epi;
   LmPartials lm;
   float* logits;
   long long ld_logits;
@@ -69,6 +73,7 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
   uint64_t* empty = full + C::STAGES;
   uint64_t* accb = empty + C::STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  int* s_prog = reinterpret_cast<int*>(tmem_slot + 1);  // [0] stages issued, [1] stages consumed
   float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -87,6 +92,8 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
       mbar_init(&empty[s], 1);
     }
     mbar_init(accb, 1);
+    s_prog[0] = 0;
+    s_prog[1] = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -111,6 +118,7 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
         tma_load_2d_hint(sW + s * C::W_BYTES, &tmW, &full[s], kx, n0, pol);
         tma_load_2d(sX + s * XS, &tmX, &full[s], kx, m0);
         if (SPLIT) tma_load_2d(sX + s * XS + C::X_BYTES, &tmXlo, &full[s], kx, m0);
+        s_prog[0] = it + 1;
       }
     }
     __syncwarp();
@@ -131,6 +139,7 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
           if (SPLIT) tc_mma_bf16(tmem, dW, sw128_kmajor_desc(aX + C::X_BYTES + 32 * k), idesc, 1u);
         }
         tc_commit(&empty[s]);
+        s_prog[1] = it + 1;
       }
       tc_commit(accb);
     }
@@ -141,21 +150,68 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
   mbar_wait(accb, 0, p.status);
   __syncwarp();  // lanes may leave the poll loop at different times; tcgen05.ld is warp-aligned
   tc_fence_after();
+  __syncthreads();
+  if (threadIdx.x == 0 && s_prog[1] < s_prog[0]) {
+    // a wait gave up: let every copy still in flight land before the ring is reused
+    for (int it = s_prog[1]; it < s_prog[0]; ++it) mbar_wait(&full[it % C::STAGES], (it / C::STAGES) & 1, p.status);
+  }
   const int n = n0 + warp * 32 + lane;
   const bool nv = n < p.N;
   const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  if constexpr (!LMHEAD) {
+    // the accumulator goes to a [BN][128] fp32 tile in the (now idle) stage ring
+    float* tile = reinterpret_cast<float*>(smem);
+    __syncthreads();
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 16) {
-    float v[16];
-    tc_ld_32x32b_x16(tbase + c, v);
-    if constexpr (!LMHEAD) {
-      float* o = p.out + split * p.split_stride;
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tc_ld_32x32b_x16(tbase + c, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int m = m0 + c + j;
-        if (nv && m < p.M) o[static_cast<long long>(m) * p.ldo + n] = v[j];
+      for (int j = 0; j < 16; ++j) tile[(c + j) * 128 + warp * 32 + lane] = v[j];
+    }
+    tc_fence_before();
+    __syncthreads();
+    const int t = threadIdx.x;
+    if (p.epi.kind == EPI_NONE) {
+      float* o = p.out + split * p.split_stride;
+      for (int j = 0; j < BN && m0 + j < p.M; ++j)
+        if (nv) o[static_cast<long long>(m0 + j) * p.ldo + n] = tile[j * 128 + t];
+    }
+    if (p.epi.kind != EPI_NONE) {
+      if (p.splits == 1) {
+        apply_epilogue<__nv_bfloat16, __half>(p.epi, tile, m0, BN, n0);
+      } else {
+        // split-K reduction inside the cluster of this tile's `splits` CTAs:
+        // each CTA sums a contiguous slice of the rows over every CTA's tile
+        // (distributed shared memory, split order) and finishes those rows
+        cluster_sync_all();
+        const int S = p.splits, cr = static_cast<int>(cluster_ctarank());
+        const int rpr = (BN + S - 1) / S;
+        const int r_begin = min(BN, cr * rpr), r_end = min(BN, r_begin + rpr);
+        float* sub = tile + BN * 128;
+        const uint32_t tile_s = smem_u32(tile);
+        for (int e = t; e < (r_end - r_begin) * 32; e += 128) {
+          const int j = r_begin + e / 32, c4 = (e % 32) * 4;
+          const uint32_t off = static_cast<uint32_t>((j * 128 + c4) * 4);
+          float4 acc = ld_dsmem_f4(dsmem_map(tile_s + off, 0));
+          for (int r = 1; r < S; ++r) {
+            const float4 v = ld_dsmem_f4(dsmem_map(tile_s + off, r));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
+          *reinterpret_cast<float4*>(sub + (j - r_begin) * 128 + c4) = acc;
+        }
+        cluster_sync_all();  // no CTA's tile is read after this point
+        if (r_end > r_begin) apply_epilogue<__nv_bfloat16, __half>(p.epi, sub, m0 + r_begin, r_end - r_begin, n0);
       }
-    } else {
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tc_ld_32x32b_x16(tbase + c, v);
 #pragma unroll 1
       for (int j = 0; j < 16; ++j) {
         const int m = m0 + c + j;
@@ -182,8 +238,6 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
         }
       }
     }
-  }
-  if constexpr (LMHEAD) {
     __syncthreads();
     for (int j = threadIdx.x; j < BN; j += blockDim.x) {
       const int m = m0 + j;
@@ -207,13 +261,26 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
       p.lm.se[o] = se;
       p.lm.idx[o] = ix;
     }
+    tc_fence_before();
   }
-  tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// Finishes an fp32 projection written by the SIMT kernel: one CTA per
+// (128-column, 16-row) tile runs the same epilogue as the tensor-core path.
+__global__ void __launch_bounds__(128) k_epilogue_apply_f32(const float* __restrict__ y, int M, int N, EpiArgs e) {
+  __shared__ float tile[16 * 128];
+  const int n0 = blockIdx.x * 128, m0 = blockIdx.y * 16, t = threadIdx.x;
+  for (int j = 0; j < 16; ++j) {
+    const int m = m0 + j, n = n0 + t;
+    tile[j * 128 + t] = (m < M && n < N) ? y[static_cast<long long>(m) * N + n] : 0.f;
+  }
+  __syncthreads();
+  apply_epilogue<float, float>(e, tile, m0, 16, n0);
 }
 
 // --------------------------------------------------------------- fp32 SIMT kernel
@@ -302,11 +369,13 @@ static bool get_tmap(dflash_ctx* c, const void* ptr, int rows, int cols, int box
 
 int gemm_kb(int K) { return (K + kTileK - 1) / kTileK; }
 
-// Split-K count for a GEMM with n_tiles output tiles and n_kb k-blocks:
-// about kSplitTargetCtas CTAs in total, at least 4 k-blocks per split, and
-// normalised so that every split owns at least one k-block.
-int choose_splits(int n_tiles, int n_kb) {
-  int s = (kSplitTargetCtas + n_tiles / 2) / std::max(1, n_tiles);
+// Split-K count for a GEMM with n_tiles output tiles and n_kb k-blocks: at
+// most `slots` CTAs in total (one wave), at most 8 (one portable cluster), at
+// least 4 k-blocks per split, and normalised so that every split owns at
+// least one k-block.
+int choose_splits(int n_tiles, int n_kb, int slots) {
+  // as many splits as keep the whole grid inside one wave of `slots` CTAs
+  int s = std::min(8, slots / std::max(1, n_tiles));
   s = std::max(1, std::min(s, std::max(1, n_kb / 4)));
   const int per = (n_kb + s - 1) / s;
   return (n_kb + per - 1) / per;
@@ -329,6 +398,8 @@ static cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorM
   p.N = g.N;
   p.n_kb = n_kb;
   p.kb_per_split = (n_kb + g.splits - 1) / g.splits;
+  p.splits = g.splits;
+  p.epi = g.epi;
   p.out = g.out;
   p.split_stride = g.split_stride;
   p.ldo = g.ldo;
@@ -340,8 +411,24 @@ static cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorM
   p.skip_rows = g.skip_rows;
   // splits come from choose_splits: every split owns at least one k-block
   dim3 grid((g.N + kTileN - 1) / kTileN, (g.M + BN - 1) / BN, g.splits);
-  k_gemm_tc<BN, LM, SPLIT><<<grid, 128, C::SMEM, s>>>(tw, tx, txlo, p);
-  return cudaGetLastError();
+  if (LM || g.epi.kind == EPI_NONE || g.splits == 1) {
+    k_gemm_tc<BN, LM, SPLIT><<<grid, 128, C::SMEM, s>>>(tw, tx, txlo, p);
+    return cudaGetLastError();
+  }
+  // the splits of one output tile form a thread-block cluster (reduced over DSMEM)
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = dim3(128);
+  lc.dynamicSmemBytes = C::SMEM;
+  lc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = g.splits;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, k_gemm_tc<BN, LM, SPLIT>, tw, tx, txlo, p);
 }
 
 template <bool SPLIT>
@@ -378,6 +465,10 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s) {
     dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
     k_gemm_f32<<<grid, 256, 0, s>>>(static_cast<const float*>(g.W), static_cast<const float*>(g.X), g.out, g.M,
                                     g.N, g.K, g.ldo, g.m_valid);
+    if (g.epi.kind != EPI_NONE) {
+      dim3 eg((g.N + 127) / 128, (g.M + 15) / 16);
+      k_epilogue_apply_f32<<<eg, 128, 0, s>>>(g.out, g.M, g.N, g.epi);
+    }
     return cudaGetLastError();
   }
   const bool split = g.X_lo != nullptr;

@@ -8,14 +8,12 @@
 #include <vector>
 
 #include "../../include/dflash.h"
+#include "epilogue.cuh"
 
 namespace dflash {
 
-constexpr int kBlockK = 16;
-constexpr int kPage = 16;
 constexpr int kTileN = 128;   // weight rows per GEMM tile (MMA M)
 constexpr int kTileK = 64;    // reduction depth per pipeline stage (one 128-byte swizzle row)
-constexpr int kSplitTargetCtas = 304;  // split-K aims at about 2 CTAs per SM of a 152-SM part
 
 // Per-row, per-128-column-tile reduction of logits: running max, its
 // (lowest) column, and sum of exp(logit - max).
@@ -39,6 +37,7 @@ struct GemmLaunch {
   long long split_stride;
   int ldo;
   const int* m_valid;  // nullable device row count; tiles at or past it exit
+  EpiArgs epi;         // fused epilogue; EPI_NONE writes raw partial planes (no cluster)
   // LM-head epilogue (bf16 only): when lm.mx != nullptr the kernel reduces
   // each tile to LmPartials instead of writing `out`.
   LmPartials lm;
@@ -72,14 +71,17 @@ struct dflash_ctx {
   int32_t *free_ring, *row_seq, *row_pos, *row_src;
   float *rope_cos, *rope_sin;
   int rope_rows;
+  int pool_pages;  // pages per layer in the pool: n_pages context pages + max_batch block pages
+  int kv_elem;     // bytes per KV-pool / q element: 2 (fp16) for bf16 workloads, 4 for fp32
   void *fc_in, *h_fused, *h_lo;
-  float* part;
-  size_t part_floats;
-  float* x;
+  float* y;        // fp32 projection output (FC output u; fp32-path staging)
+  float* x;        // residual stream [M][d]
   void *a, *a_lo, *o, *o_lo, *act, *act_lo;  // GEMM inputs (lo: second bf16 term, bf16 only)
-  float *q, *kblk, *vblk;
+  void* q;         // block queries [M][Hq*dh] (KV element type)
   float *attn_o, *attn_ml;
   int attn_max_splits;
+  bool attn_maps_ready = false;
+  CUtensorMap attn_map_k, attn_map_v;  // 4-D maps over the fp16 pool
   dflash::LmPartials lm;
   float* logits_ws;  // fp32 mode: full logits [M][V]
   int32_t* tok1;
@@ -100,7 +102,7 @@ namespace dflash {
 
 // gemm.cu
 cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
-int choose_splits(int n_tiles, int n_kb);
+int choose_splits(int n_tiles, int n_kb, int slots);
 int gemm_kb(int K);
 int gemm_bn(int M, bool split);
 cudaError_t gemm_launch_uncached(int* status, const GemmLaunch& g, cudaStream_t s);

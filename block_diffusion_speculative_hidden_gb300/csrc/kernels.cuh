@@ -19,12 +19,9 @@ cudaError_t launch_rope_table(dflash_ctx* c, cudaStream_t s);
 // pointwise.cu (T = the config element type, chosen by c->cfg.dtype)
 cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, int max_rows, int first_seq,
                                cudaStream_t s);
-cudaError_t launch_fc_norm(dflash_ctx* c, int rows, int splits, cudaStream_t s);
-cudaError_t launch_inject_kv(dflash_ctx* c, int rows, int splits, cudaStream_t s);
+cudaError_t launch_fc_norm(dflash_ctx* c, int rows, cudaStream_t s);
 cudaError_t launch_embed_norm(dflash_ctx* c, int M, bool second_pass, cudaStream_t s);
-cudaError_t launch_qkv_rope(dflash_ctx* c, int M, int splits, cudaStream_t s);
-cudaError_t launch_residual_norm(dflash_ctx* c, int M, int splits, const void* gain, cudaStream_t s);
-cudaError_t launch_swiglu(dflash_ctx* c, int M, int splits, cudaStream_t s);
+cudaError_t launch_rmsnorm_rows(dflash_ctx* c, int M, const void* gain, cudaStream_t s);
 cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, cudaStream_t s);
 cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,
                             cudaStream_t s);
@@ -33,6 +30,8 @@ cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s);
 // attention.cu
 int attn_splits(dflash_ctx* c, int B);
 cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
+// attention_tc.cu (fp16 pool)
+cudaError_t launch_attention_tc(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
 
 // accept.cu
 cudaError_t launch_accept_greedy(int B, int K, const int32_t* d, const int32_t* y, int32_t* tau, int32_t* emitted,

@@ -1,7 +1,7 @@
-// Row-wise kernels around the GEMMs: split-K reduction fused with the
-// operation that follows each projection (RMSNorm, RoPE + paged KV write,
-// residual add, SwiGLU), the block input embedding, and the LM-head argmax
-// merge and S = 2 commit.
+// Row-wise kernels around the projections: the feature-fusion RMSNorm, the
+// pre-norms of the draft layers, the block input embedding, the LM-head
+// argmax merge and the S = 2 commit.  (Residual adds, SwiGLU, RoPE and the
+// paged K/V stores run inside the projection epilogues, epilogue.cuh.)
 //
 // Passages: the DFlash Guide, "2. Target Hidden-State Conditioning" (fused
 // features) and "3. Cross-Layer KV Injection" (K, V of every draft layer
@@ -13,13 +13,6 @@
 #include "kernels.cuh"
 
 namespace dflash {
-
-// Sum of `splits` fp32 partial planes at element e.
-__device__ __forceinline__ float sum_splits(const float* __restrict__ part, long long plane, int splits, long long e) {
-  float v = part[e];
-  for (int s = 1; s < splits; ++s) v += part[s * plane + e];
-  return v;
-}
 
 // ------------------------------------------------------------ inject side
 
@@ -37,61 +30,20 @@ __global__ void k_gather_rows(const T* __restrict__ feats, T* __restrict__ out, 
   for (int i = threadIdx.x; i < n16; i += blockDim.x) d[i] = s[i];
 }
 
-// h[r] = RMSNorm(sum of FC partials)[r] * g_fc
+// h[r] = RMSNorm(u[r]) * g_fc, u = the fused-feature FC output (fp32)
 template <typename T>
-__global__ void k_fc_norm(const float* __restrict__ part, long long plane, int splits, const T* __restrict__ gain,
-                          ActOut<T> h, const int* scal, int d, float eps) {
-  extern __shared__ float sbuf[];  // [d] + 32
+__global__ void k_fc_norm(const float* __restrict__ u, const T* __restrict__ gain, ActOut<T> h, const int* scal,
+                          int d, float eps) {
+  __shared__ float red[32];
   const int r = blockIdx.x;
   if (r >= scal[0]) return;
+  const float* row = u + static_cast<long long>(r) * d;
   float ss = 0.f;
-  for (int n = threadIdx.x; n < d; n += blockDim.x) {
-    const float u = sum_splits(part, plane, splits, static_cast<long long>(r) * d + n);
-    sbuf[n] = u;
-    ss += u * u;
-  }
-  ss = block_sum(ss, sbuf + d);
+  for (int n = threadIdx.x; n < d; n += blockDim.x) ss += row[n] * row[n];
+  ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / d + eps);
   for (int n = threadIdx.x; n < d; n += blockDim.x)
-    h.put(static_cast<long long>(r) * d + n, sbuf[n] * inv * to_f32(gain[n]));
-}
-
-// Injected K (RoPE at the row's absolute position, optional pre-RoPE offset)
-// and V of every layer, written into the row's page slot (fp32 pool).
-// GEMM output columns: layer l -> [l*2*kvd, +kvd) keys, [+kvd, +2kvd) values.
-__global__ void k_inject_kv(const float* __restrict__ part, long long plane, int splits, const int* scal,
-                            const int32_t* __restrict__ row_seq, const int32_t* __restrict__ row_pos,
-                            const int32_t* __restrict__ page_table, int max_pages, const float* __restrict__ rcos,
-                            const float* __restrict__ rsin, const float* __restrict__ key_offset, float* pool_k,
-                            float* pool_v, int L, int P, int Hkv, int dh) {
-  const int r = blockIdx.x;
-  if (r >= scal[0]) return;
-  const int b = row_seq[r], pos = row_pos[r];
-  const int page = page_table[b * max_pages + pos / kPage], slot = pos % kPage;
-  const int kvd = Hkv * dh, half = dh / 2, ncol = 2 * L * kvd;
-  const long long rowbase = static_cast<long long>(r) * ncol;
-  // keys: one thread per rotated pair (l, head, i)
-  for (int t = threadIdx.x; t < L * Hkv * half; t += blockDim.x) {
-    const int i = t % half, hl = t / half, hh = hl % Hkv, l = hl / Hkv;
-    const int c0 = l * 2 * kvd + hh * dh + i;
-    float x1 = sum_splits(part, plane, splits, rowbase + c0);
-    float x2 = sum_splits(part, plane, splits, rowbase + c0 + half);
-    if (key_offset != nullptr) {
-      x1 += key_offset[(l * Hkv + hh) * dh + i];
-      x2 += key_offset[(l * Hkv + hh) * dh + i + half];
-    }
-    const float cs = rcos[pos * half + i], sn = rsin[pos * half + i];
-    const long long o = ((static_cast<long long>(l) * P + page) * Hkv + hh) * (kPage * dh) + slot * dh + i;
-    pool_k[o] = x1 * cs - x2 * sn;
-    pool_k[o + half] = x2 * cs + x1 * sn;
-  }
-  // values
-  for (int t = threadIdx.x; t < L * kvd; t += blockDim.x) {
-    const int dd = t % dh, hl = t / dh, hh = hl % Hkv, l = hl / Hkv;
-    const float v = sum_splits(part, plane, splits, rowbase + l * 2 * kvd + kvd + hh * dh + dd);
-    const long long o = ((static_cast<long long>(l) * P + page) * Hkv + hh) * (kPage * dh) + slot * dh + dd;
-    pool_v[o] = v;
-  }
+    h.put(static_cast<long long>(r) * d + n, row[n] * inv * to_f32(gain[n]));
 }
 
 // ------------------------------------------------------------ draft side
@@ -124,67 +76,28 @@ __global__ void k_embed_norm(const T* __restrict__ embed, const T* __restrict__ 
   }
 }
 
-// Reduce the QKV partials, rotate q and k at the block position
-// seq_len[b] + i, and store q, k_blk, v_blk (fp32).
-__global__ void k_qkv_rope(const float* __restrict__ part, long long plane, int splits, const int32_t* seq_len,
-                           const float* __restrict__ rcos, const float* __restrict__ rsin, float* q, float* kb,
-                           float* vb, int Hq, int Hkv, int dh) {
-  const int m = blockIdx.x;
-  const int b = m / kBlockK, i = m % kBlockK;
-  const int pos = seq_len[b] + i;
-  const int half = dh / 2, qd = Hq * dh, kvd = Hkv * dh, ncol = qd + 2 * kvd;
-  const long long rowbase = static_cast<long long>(m) * ncol;
-  for (int t = threadIdx.x; t < (Hq + Hkv) * half; t += blockDim.x) {
-    const int j = t % half, h = t / half;
-    const int c0 = h * dh + j;  // q heads, then k heads, contiguous
-    const float x1 = sum_splits(part, plane, splits, rowbase + c0);
-    const float x2 = sum_splits(part, plane, splits, rowbase + c0 + half);
-    const float cs = rcos[pos * half + j], sn = rsin[pos * half + j];
-    const float y1 = x1 * cs - x2 * sn, y2 = x2 * cs + x1 * sn;
-    if (h < Hq) {
-      q[static_cast<long long>(m) * qd + c0] = y1;
-      q[static_cast<long long>(m) * qd + c0 + half] = y2;
-    } else {
-      const int kc = c0 - qd;
-      kb[static_cast<long long>(m) * kvd + kc] = y1;
-      kb[static_cast<long long>(m) * kvd + kc + half] = y2;
-    }
-  }
-  for (int t = threadIdx.x; t < kvd; t += blockDim.x)
-    vb[static_cast<long long>(m) * kvd + t] = sum_splits(part, plane, splits, rowbase + qd + kvd + t);
-}
-
-// x[m] += sum of partials; a[m] = RMSNorm(x[m]) * gain
+// a[m] = RMSNorm(x[m]) * gain (the pre-norm of the next projection)
 template <typename T>
-__global__ void k_residual_norm(const float* __restrict__ part, long long plane, int splits, float* __restrict__ x,
-                                ActOut<T> a, const T* __restrict__ gain, int d, float eps) {
+__global__ void k_rmsnorm_rows(const float* __restrict__ x, ActOut<T> a, const T* __restrict__ gain, int d,
+                               float eps) {
   __shared__ float red[32];
   const int m = blockIdx.x;
+  const float4* row = reinterpret_cast<const float4*>(x + static_cast<long long>(m) * d);
   float ss = 0.f;
-  for (int n = threadIdx.x; n < d; n += blockDim.x) {
-    const long long e = static_cast<long long>(m) * d + n;
-    const float v = x[e] + sum_splits(part, plane, splits, e);
-    x[e] = v;
-    ss += v * v;
+  for (int n = threadIdx.x; n < d / 4; n += blockDim.x) {
+    const float4 v = row[n];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / d + eps);
-  for (int n = threadIdx.x; n < d; n += blockDim.x) {
-    const long long e = static_cast<long long>(m) * d + n;
-    a.put(e, x[e] * inv * to_f32(gain[n]));
+  for (int n = threadIdx.x; n < d / 4; n += blockDim.x) {
+    const float4 v = row[n];
+    const long long e = static_cast<long long>(m) * d + 4 * n;
+    a.put(e + 0, v.x * inv * to_f32(gain[4 * n + 0]));
+    a.put(e + 1, v.y * inv * to_f32(gain[4 * n + 1]));
+    a.put(e + 2, v.z * inv * to_f32(gain[4 * n + 2]));
+    a.put(e + 3, v.w * inv * to_f32(gain[4 * n + 3]));
   }
-}
-
-// act[m][f] = silu(gate) * up, gate = columns [0, F), up = [F, 2F)
-template <typename T>
-__global__ void k_swiglu(const float* __restrict__ part, long long plane, int splits, ActOut<T> act, int F,
-                         int M) {
-  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= static_cast<long long>(M) * F) return;
-  const long long m = t / F, f = t % F;
-  const float g = sum_splits(part, plane, splits, m * 2 * F + f);
-  const float u = sum_splits(part, plane, splits, m * 2 * F + F + f);
-  act.put(t, g / (1.f + expf(-g)) * u);
 }
 
 // fp32 path: per (row, 128-column tile) max / argmax / sum-exp of the logits,
@@ -307,8 +220,6 @@ __global__ void k_commit(const float* __restrict__ conf1, int32_t* commit, int B
     }                                                 \
   } while (0)
 
-static long long part_plane(int rows, int cols) { return static_cast<long long>(rows) * cols; }
-
 template <typename T>
 static ActOut<T> act_out(void* hi, void* lo) {
   return ActOut<T>{static_cast<T*>(hi), static_cast<T*>(lo)};
@@ -324,23 +235,11 @@ cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, int m
   return cudaGetLastError();
 }
 
-cudaError_t launch_fc_norm(dflash_ctx* c, int rows, int splits, cudaStream_t s) {
+cudaError_t launch_fc_norm(dflash_ctx* c, int rows, cudaStream_t s) {
   const int d = c->cfg.hidden;
-  const size_t smem = sizeof(float) * (d + 32);
-  DFLASH_DISPATCH(c, (k_fc_norm<T><<<rows, 256, smem, s>>>(c->part, part_plane(rows, d), splits,
-                                                           static_cast<const T*>(c->g_fc),
-                                                           act_out<T>(c->h_fused, c->h_lo), c->scal, d,
-                                                           c->cfg.rms_eps)));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_inject_kv(dflash_ctx* c, int rows, int splits, cudaStream_t s) {
-  const auto& g = c->cfg;
-  const int ncol = 2 * g.n_layers * g.n_kv_heads * g.head_dim;
-  k_inject_kv<<<rows, 256, 0, s>>>(c->part, part_plane(rows, ncol), splits, c->scal, c->row_seq, c->row_pos,
-                                   c->page_table, g.max_pages_per_seq, c->rope_cos, c->rope_sin, c->key_offset,
-                                   static_cast<float*>(c->pool_k), static_cast<float*>(c->pool_v), g.n_layers,
-                                   g.n_pages, g.n_kv_heads, g.head_dim);
+  DFLASH_DISPATCH(c, (k_fc_norm<T><<<rows, 256, 0, s>>>(c->y, static_cast<const T*>(c->g_fc),
+                                                        act_out<T>(c->h_fused, c->h_lo), c->scal, d,
+                                                        c->cfg.rms_eps)));
   return cudaGetLastError();
 }
 
@@ -354,28 +253,10 @@ cudaError_t launch_embed_norm(dflash_ctx* c, int M, bool second_pass, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_qkv_rope(dflash_ctx* c, int M, int splits, cudaStream_t s) {
-  const auto& g = c->cfg;
-  const int ncol = (g.n_q_heads + 2 * g.n_kv_heads) * g.head_dim;
-  k_qkv_rope<<<M, 256, 0, s>>>(c->part, part_plane(M, ncol), splits, c->seq_len, c->rope_cos, c->rope_sin, c->q,
-                               c->kblk, c->vblk, g.n_q_heads, g.n_kv_heads, g.head_dim);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_residual_norm(dflash_ctx* c, int M, int splits, const void* gain, cudaStream_t s) {
+cudaError_t launch_rmsnorm_rows(dflash_ctx* c, int M, const void* gain, cudaStream_t s) {
   const int d = c->cfg.hidden;
-  DFLASH_DISPATCH(c, (k_residual_norm<T><<<M, 256, 0, s>>>(c->part, part_plane(M, d), splits, c->x,
-                                                           act_out<T>(c->a, c->a_lo), static_cast<const T*>(gain),
-                                                           d, c->cfg.rms_eps)));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_swiglu(dflash_ctx* c, int M, int splits, cudaStream_t s) {
-  const int F = c->cfg.ffn;
-  const long long n = static_cast<long long>(M) * F;
-  const int blocks = static_cast<int>((n + 255) / 256);
-  DFLASH_DISPATCH(c, (k_swiglu<T><<<blocks, 256, 0, s>>>(c->part, part_plane(M, 2 * F), splits,
-                                                         act_out<T>(c->act, c->act_lo), F, M)));
+  DFLASH_DISPATCH(c, (k_rmsnorm_rows<T><<<M, 256, 0, s>>>(c->x, act_out<T>(c->a, c->a_lo),
+                                                          static_cast<const T*>(gain), d, c->cfg.rms_eps)));
   return cudaGetLastError();
 }
 

@@ -60,6 +60,18 @@ def gemm_bf16(W: torch.Tensor, X: torch.Tensor, splits: int = 1, status: Optiona
     return out
 
 
+def pack_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor) -> torch.Tensor:
+    """[128 * ceil(F/64), d]: per group of 64 features, the 64 gate rows then
+    the 64 matching up rows (the last group zero-padded), so that one 128-row
+    projection tile holds both halves of its SwiGLU."""
+    F, d = w_gate.shape
+    G = -(-F // 64)
+    pad = G * 64 - F
+    g = torch.cat([w_gate, w_gate.new_zeros(pad, d)]) if pad else w_gate
+    u = torch.cat([w_up, w_up.new_zeros(pad, d)]) if pad else w_up
+    return torch.stack([g.reshape(G, 64, d), u.reshape(G, 64, d)], 1).reshape(G * 128, d)
+
+
 class Drafter:
     """One libdflash context plus the device buffers it borrows.
 
@@ -113,7 +125,7 @@ class Drafter:
             return t
 
         w_qkv = [keep(torch.cat([w[f"w_q.{l}"], w[f"w_k.{l}"], w[f"w_v.{l}"]], 0)) for l in range(nl)]
-        w_gu = [keep(torch.cat([w[f"w_gate.{l}"], w[f"w_up.{l}"]], 0)) for l in range(nl)]
+        w_gu = [keep(pack_gate_up(w[f"w_gate.{l}"], w[f"w_up.{l}"])) for l in range(nl)]
         w_kv = keep(torch.cat([torch.cat([w[f"w_k.{l}"], w[f"w_v.{l}"]], 0) for l in range(nl)], 0))
         singles = {k: keep(w[k]) for k in ("w_fc", "g_fc", "embed", "g_final", "w_lm")}
         w_o = [keep(w[f"w_o.{l}"]) for l in range(nl)]
@@ -148,11 +160,14 @@ class Drafter:
 
     # ------------------------------------------------------------------ cache views
     def pool_kv(self):
-        """(K, V) fp32 views of the pool: [L, n_pages, Hkv, 16, head_dim]."""
+        """(K, V) views of the pool: [L, n_pages + max_batch, Hkv, 16, head_dim],
+        fp16 for bf16 workloads and fp32 for fp32 ones.  Pages n_pages + b hold
+        sequence b's draft-block keys and values of the latest pass."""
         s, c = self.shape, self.cfg
-        n = s.n_layers * c.n_pages * s.n_kv_heads * 16 * s.head_dim
-        flat = self.kv_pool.view(torch.float32)
-        shp = (s.n_layers, c.n_pages, s.n_kv_heads, 16, s.head_dim)
+        pages = c.n_pages + c.max_batch
+        n = s.n_layers * pages * s.n_kv_heads * 16 * s.head_dim
+        flat = self.kv_pool.view(torch.float16 if s.dtype == "bf16" else torch.float32)
+        shp = (s.n_layers, pages, s.n_kv_heads, 16, s.head_dim)
         return flat[:n].view(shp), flat[n:2 * n].view(shp)
 
     # ------------------------------------------------------------------ the ABI calls

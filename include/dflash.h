@@ -34,8 +34,9 @@
  *     is a bf16 x bf16 tensor-core product with fp32 accumulation.  An
  *     activation that enters a projection is carried as an exact pair of
  *     bf16 terms (hi + lo, two MMAs), so it keeps about 16 significant bits;
- *     the residual stream, block q/k/v, the KV pool, logits and confidences
- *     are fp32.  dtype DFLASH_F32: everything fp32 (SIMT kernels).
+ *     block queries and the KV pool are fp16; the residual stream, logits
+ *     and confidences are fp32.  dtype DFLASH_F32: everything fp32 (SIMT
+ *     kernels).
  */
 #ifndef DFLASH_H_
 #define DFLASH_H_
@@ -75,7 +76,7 @@ typedef struct {
   int hidden;            /* draft hidden size d */
   int n_q_heads;         /* Hq */
   int n_kv_heads;        /* Hkv; Hq % Hkv == 0, G = Hq / Hkv in {1, 2, 4, 8} */
-  int head_dim;          /* dh in {32, 64, 128} */
+  int head_dim;          /* dh in {64, 128} (DFLASH_BF16) or {32, 64, 128} (DFLASH_F32) */
   int ffn;               /* SwiGLU width F */
   int vocab;             /* V */
   int mask_id;           /* the [MASK] token id */
@@ -109,7 +110,9 @@ typedef struct {
                               injected keys before RoPE (a workload knob; NULL = none) */
   const void* const* w_qkv;  /* per layer [Hq*dh + 2*kvd, hidden]: q rows, then k, then v */
   const void* const* w_o;    /* per layer [hidden, Hq*dh] */
-  const void* const* w_gu;   /* per layer [2*ffn, hidden]: gate rows, then up rows */
+  const void* const* w_gu;   /* per layer [128*ceil(ffn/64), hidden]: for each group of 64
+                                features, its 64 gate rows then its 64 up rows; rows of
+                                features past ffn are zero */
   const void* const* w_down; /* per layer [hidden, ffn] */
   const void* const* g_in;   /* per layer [hidden]  pre-attention RMSNorm gain */
   const void* const* g_post; /* per layer [hidden]  pre-MLP RMSNorm gain */
@@ -118,8 +121,10 @@ typedef struct {
 /* Bytes of caller-provided scratch the context needs; 0 on a bad config. */
 size_t dflash_workspace_size(const dflash_config* cfg);
 
-/* Bytes of the paged KV pool: K then V, each [n_layers][n_pages][n_kv_heads]
- * [page_size][head_dim] fp32.  [Guide] "3. Cross-Layer KV
+/* Bytes of the paged KV pool: K then V, each [n_layers][n_pages + max_batch]
+ * [n_kv_heads][page_size][head_dim], fp16 (DFLASH_BF16) or fp32 (DFLASH_F32).
+ * Pages n_pages + b hold sequence b's draft-block keys and values of the
+ * current pass; pages 0..n_pages-1 the injected context.  [Guide] "3. Cross-Layer KV
  * Injection" ("Zero Redundant KV Caching"): the draft cache holds only the
  * injected target context, never the block's own keys. */
 size_t dflash_kv_pool_size(const dflash_config* cfg);

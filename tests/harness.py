@@ -20,9 +20,9 @@ from oracle import dflash_oracle as O
 # argmax agreement except where the oracle's top-2 gap is below 1e-2).
 LOGIT_TOL = {"bf16": 2e-2, "f32": 1e-4}
 TOP2_EXEMPT = 1e-2
-# KV pool (fp32 storage): the bf16 path's fused features enter the K/V
-# projection as a hi+lo bf16 pair (~2^-17 relative), plus fp32 accumulation.
-KV_TOL = {"bf16": (1e-3, 1e-3), "f32": (1e-5, 1e-5)}   # (atol, rtol)
+# KV pool: fp16 storage for bf16 workloads (rounding 2^-11 relative), fp32
+# for fp32 workloads.
+KV_TOL = {"bf16": (2e-3, 2e-3), "f32": (1e-5, 1e-5)}   # (atol, rtol)
 
 
 def cache_dims(cfg, rounds: int, lens: np.ndarray):

@@ -48,7 +48,7 @@ def _cfg(**kw):
 def test_sizes_and_config_validation(L):
     c = _cfg()
     pool = L.dflash_kv_pool_size(ctypes.byref(c))
-    assert pool == 2 * 2 * 80 * 2 * 16 * 128 * 4     # K and V, fp32
+    assert pool == 2 * 2 * (80 + 3) * 2 * 16 * 128 * 2     # K and V, fp16, 3 block pages
     assert L.dflash_workspace_size(ctypes.byref(c)) > 0
     for bad in (dict(block_k=8), dict(page_size=32), dict(head_dim=96), dict(n_q_heads=6),
                 dict(hidden=500), dict(dtype=7), dict(mask_id=5000), dict(max_inject_rows=10)):
@@ -56,7 +56,7 @@ def test_sizes_and_config_validation(L):
         assert L.dflash_workspace_size(ctypes.byref(cb)) == 0, bad
         assert L.dflash_kv_pool_size(ctypes.byref(cb)) == 0, bad
     f32 = _cfg(dtype=0, hidden=500)
-    assert L.dflash_kv_pool_size(ctypes.byref(f32)) == 2 * 2 * 80 * 2 * 16 * 128 * 4
+    assert L.dflash_kv_pool_size(ctypes.byref(f32)) == 2 * 2 * (80 + 3) * 2 * 16 * 128 * 4
 
 
 def test_null_arguments_rejected_before_device_work(L):
