@@ -49,6 +49,8 @@ def parse_args(argv=None):
                     help="roll each sequence back to its prompt length every N rounds")
     ap.add_argument("--kernel", choices=["gemm"], default=None,
                     help="time one kernel alone on the workload's shapes (small case for profilers)")
+    ap.add_argument("--small", action="store_true",
+                    help="profiler case: the workload's layer shapes with 1 draft layer and a 16384 vocab")
     return ap.parse_args(argv)
 
 
@@ -460,6 +462,8 @@ def run_kernel_gemm(args, cfg):
 def main(argv=None):
     args = parse_args(argv)
     cfg = synth.get_config(args.config)
+    if args.small:
+        cfg = cfg.replace(n_layers=1, vocab=16384, name=cfg.name + "_1layer_v16k")
     if args.kernel == "gemm":
         run_kernel_gemm(args, cfg)
         return

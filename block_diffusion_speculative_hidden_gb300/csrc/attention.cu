@@ -154,11 +154,11 @@ __global__ void k_attn_combine(const float* __restrict__ part_o, const float* __
 }
 
 // Key splits per (sequence, kv head): enough CTAs for about two per SM; the
-// tensor-core kernel merges its splits inside one cluster, so at most 8.
+// tensor-core kernel merges its splits inside one cluster (at most 16).
 int attn_splits(dflash_ctx* c, int B) {
   const int heads = B * c->cfg.n_kv_heads;
   int s = (2 * c->num_sms + heads - 1) / heads;
-  if (c->cfg.dtype == DFLASH_BF16) s = std::min(s, 8);
+  if (c->cfg.dtype == DFLASH_BF16) s = std::min(s, attention_tc_max_splits(c));
   return std::max(1, std::min(s, c->attn_max_splits));
 }
 

@@ -30,8 +30,9 @@ namespace dflash {
 
 namespace {
 
-constexpr int kPPS = 2;      // pages per pipeline stage (32 keys)
+constexpr int kPPS = 2;        // pages per pipeline stage (32 keys)
 constexpr int kStages = 4;
+constexpr int kMaxSplits = 16;  // splits merged in one cluster (16 needs the non-portable size)
 
 template <int DH, int G>
 struct TcAttnCfg {
@@ -42,7 +43,7 @@ struct TcAttnCfg {
   static constexpr int Q_BYTES = G * 16 * QROW * 2;
   static constexpr int THREADS = (G + 1) * 32;
   static constexpr int ML_BYTES = G * 16 * 2 * 4;                // per-row (m, l) for the split merge
-  static constexpr int SMEM = 1024 + kStages * STAGE_BYTES + Q_BYTES + ML_BYTES + 256;
+  static constexpr int SMEM_FIXED = 1024 + kStages * STAGE_BYTES + Q_BYTES + ML_BYTES + 256;  // + page ids
   static_assert(G * 16 * DH * 4 <= kStages * STAGE_BYTES, "the split partial must fit in the ring");
 };
 
@@ -90,6 +91,7 @@ struct TcAttnParams {
   const int32_t* seq_len;
   int max_pages, block_page0, pool_pages, layer;
   int Hkv, splits;
+  int page_slots;             // capacity of the shared-memory page-id list
   float scale_log2;           // log2(e) / sqrt(dh)
   void* o_hi;                 // ActOut<bf16> of the attention output [B*16][Hq*DH]
   void* o_lo;
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__((G + 1) * 32) k_attn_tc(const __grid_constant_
   float* sML = reinterpret_cast<float*>(smem + kStages * C::STAGE_BYTES + C::Q_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::STAGE_BYTES + C::Q_BYTES + C::ML_BYTES);
   uint64_t* empty = full + kStages;
+  int* s_pages = reinterpret_cast<int*>(empty + kStages);  // this split's page ids, staged once
 
   const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -127,17 +130,25 @@ __global__ void __launch_bounds__((G + 1) * 32) k_attn_tc(const __grid_constant_
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  // block queries of this kv group: warp gi's 16 rows = query head kvh*G + gi
-  {
+  __syncthreads();  // barriers initialised; from here each warp stages only what it uses itself
+  if (warp == G) {
+    // page id of every virtual page of this split (context pages, then the block
+    // page; 0 past the end), so that issuing a stage never waits on a global load
+    for (int j = lane; j < n_st * kPPS && j < p.page_slots; j += 32) {
+      const int vp = vp_begin + j;
+      s_pages[j] = vp >= vp_end ? 0 : vp < n_ctx_pages ? p.page_table[b * p.max_pages + vp] : p.block_page0 + b;
+    }
+  } else {
+    // this warp's 16 block queries: query head kvh*G + warp, block positions 0..15
     const int qd = p.Hkv * G * DH;
-    for (int e = threadIdx.x; e < R * (DH / 8); e += blockDim.x) {
-      const int row = e / (DH / 8), c8 = e % (DH / 8), gi = row >> 4, i = row & 15;
+    for (int e = lane; e < 16 * (DH / 8); e += 32) {
+      const int i = e / (DH / 8), c8 = e % (DH / 8);
       const int4 v = *reinterpret_cast<const int4*>(p.q + static_cast<long long>(b * kBlockK + i) * qd +
-                                                    (kvh * G + gi) * DH + c8 * 8);
-      *reinterpret_cast<int4*>(sQ + row * C::QROW + c8 * 8) = v;
+                                                    (kvh * G + warp) * DH + c8 * 8);
+      *reinterpret_cast<int4*>(sQ + (warp * 16 + i) * C::QROW + c8 * 8) = v;
     }
   }
-  __syncthreads();
+  __syncwarp();
 
   float o[DH / 8][4];
 #pragma unroll
@@ -157,11 +168,8 @@ __global__ void __launch_bounds__((G + 1) * 32) k_attn_tc(const __grid_constant_
         uint8_t* kdst = ring + s * C::STAGE_BYTES;
         uint8_t* vdst = kdst + kPPS * C::PAGE_BYTES;
         for (int j = 0; j < kPPS; ++j) {
-          const int vp = vp_begin + st * kPPS + j;
           // past this split's end: page 0 (finite data, fully masked)
-          const int page = vp >= vp_end ? 0
-                           : vp < n_ctx_pages ? p.page_table[b * p.max_pages + vp]
-                                              : p.block_page0 + b;
+          const int page = s_pages[st * kPPS + j];
           for (int bx = 0; bx < C::NBOX; ++bx) {
             tma_load_4d(kdst + j * C::PAGE_BYTES + bx * 2048, &tmK, &full[s], bx * 64, 0, kvh, l_off + page);
             tma_load_4d(vdst + j * C::PAGE_BYTES + bx * 2048, &tmV, &full[s], bx * 64, 0, kvh, l_off + page);
@@ -320,21 +328,32 @@ __global__ void __launch_bounds__((G + 1) * 32) k_attn_tc(const __grid_constant_
     const uint32_t sO_s = smem_u32(sO), sML_s = smem_u32(sML);
     for (int e = threadIdx.x; e < (r1 - r0) * (DH / 4); e += blockDim.x) {
       const int r = r0 + e / (DH / 4), d4 = (e % (DH / 4)) * 4;
+      // every split's (m, l, o) of this row and 4 columns, loads issued back to back
+      float ms[kMaxSplits], ls[kMaxSplits];
+      float4 os[kMaxSplits];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplits; ++s2)
+        if (s2 < S) {
+          ms[s2] = ld_dsmem_f32(dsmem_map(sML_s + 8 * r, s2));
+          ls[s2] = ld_dsmem_f32(dsmem_map(sML_s + 8 * r + 4, s2));
+          os[s2] = ld_dsmem_f4(dsmem_map(sO_s + 4 * (r * DH + d4), s2));
+        }
       float M = -INFINITY;
-      for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, ld_dsmem_f32(dsmem_map(sML_s + 8 * r, s2)));
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplits; ++s2)
+        if (s2 < S) M = fmaxf(M, ms[s2]);
       float den = 0.f;
       float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float ms = ld_dsmem_f32(dsmem_map(sML_s + 8 * r, s2));
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - M);
-        den += w * ld_dsmem_f32(dsmem_map(sML_s + 8 * r + 4, s2));
-        const float4 v = ld_dsmem_f4(dsmem_map(sO_s + 4 * (r * DH + d4), s2));
-        num.x += w * v.x;
-        num.y += w * v.y;
-        num.z += w * v.z;
-        num.w += w * v.w;
-      }
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplits; ++s2)
+        if (s2 < S && ms[s2] > -INFINITY) {
+          const float w = exp2f(ms[s2] - M);
+          den += w * ls[s2];
+          num.x += w * os[s2].x;
+          num.y += w * os[s2].y;
+          num.z += w * os[s2].z;
+          num.w += w * os[s2].w;
+        }
       const float inv = den > 0.f ? 1.f / den : 0.f;
       const int gi = r >> 4, i = r & 15;
       const long long base = static_cast<long long>(b * kBlockK + i) * qd + (kvh * G + gi) * DH + d4;
@@ -378,13 +397,21 @@ bool pool_map(const void* base, int dh, int Hkv, long long pages_total, CUtensor
 template <int DH, int G>
 cudaError_t launch_tc_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
   using C = TcAttnCfg<DH, G>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_tc<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static int attr_smem = 0;
+  static bool attr_np = false;
+  if (!attr_np) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tc<DH, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr_np = true;
   }
   const auto& g = c->cfg;
+  const int page_slots = g.max_pages_per_seq + 1 + kPPS;  // a split holds at most every page + the block page
+  const int smem = C::SMEM_FIXED + 4 * page_slots;
+  if (smem > attr_smem) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tc<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_smem = smem;
+  }
   const long long pages_total = static_cast<long long>(g.n_layers) * c->pool_pages;
   if (!c->attn_maps_ready) {
     if (!pool_map(c->pool_k, DH, g.n_kv_heads, pages_total, &c->attn_map_k) ||
@@ -402,20 +429,21 @@ cudaError_t launch_tc_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_
   p.layer = layer;
   p.Hkv = g.n_kv_heads;
   p.splits = splits;
+  p.page_slots = page_slots;
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
   p.o_hi = c->o;
   p.o_lo = c->o_lo;
   p.status = c->status;
   dim3 grid(splits, g.n_kv_heads, B);
   if (splits == 1) {
-    k_attn_tc<DH, G><<<grid, C::THREADS, C::SMEM, s>>>(c->attn_map_k, c->attn_map_v, p);
+    k_attn_tc<DH, G><<<grid, C::THREADS, smem, s>>>(c->attn_map_k, c->attn_map_v, p);
     return cudaGetLastError();
   }
   // the splits of one (sequence, kv head) form a cluster (at most 8: portable)
   cudaLaunchConfig_t lc = {};
   lc.gridDim = grid;
   lc.blockDim = dim3(C::THREADS);
-  lc.dynamicSmemBytes = C::SMEM;
+  lc.dynamicSmemBytes = smem;
   lc.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -439,6 +467,53 @@ cudaError_t launch_tc_dh(dflash_ctx* c, int layer, int B, int splits, cudaStream
 }
 
 }  // namespace
+
+// Largest cluster (= split count) the tensor-core attention may use here:
+// 16 when the device can hold such clusters of this kernel, else the
+// portable 8.  Queried once per context.
+template <int DH, int G>
+static int max_splits_t(dflash_ctx* c) {
+  using C = TcAttnCfg<DH, G>;
+  const int smem = C::SMEM_FIXED + 4 * (c->cfg.max_pages_per_seq + 1 + kPPS);
+  if (cudaFuncSetAttribute(k_attn_tc<DH, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+      cudaFuncSetAttribute(k_attn_tc<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 8;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(16, 1, 1);
+  lc.blockDim = dim3(C::THREADS);
+  lc.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 16;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<DH, G>, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    return 8;
+  }
+  return n > 0 ? 16 : 8;
+}
+
+template <int DH>
+static int max_splits_dh(dflash_ctx* c) {
+  switch (c->cfg.n_q_heads / c->cfg.n_kv_heads) {
+    case 1: return max_splits_t<DH, 1>(c);
+    case 2: return max_splits_t<DH, 2>(c);
+    case 4: return max_splits_t<DH, 4>(c);
+    default: return max_splits_t<DH, 8>(c);
+  }
+}
+
+int attention_tc_max_splits(dflash_ctx* c) {
+  if (c->attn_tc_max_splits == 0)
+    c->attn_tc_max_splits = c->cfg.head_dim == 128 ? max_splits_dh<128>(c) : max_splits_dh<64>(c);
+  return c->attn_tc_max_splits;
+}
 
 cudaError_t launch_attention_tc(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
   switch (c->cfg.head_dim) {

@@ -22,22 +22,18 @@ int elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 4; 
 int kv_elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 4; }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
-// Concurrent CTA slots of the projection kernel: tiles up to 64 rows wide
-// fit two CTAs per SM, wider ones one.
-int gemm_slots(int num_sms, int bn) { return num_sms * (bn <= 64 ? 2 : 1); }
-
 // Split count of one draft-side GEMM for M activation rows (hi/lo inputs).
-int draft_splits(const dflash_config& g, int num_sms, int M, int N, int K) {
+int draft_splits(const dflash_config& g, int M, int N, int K) {
   if (g.dtype != DFLASH_BF16) return 1;
   const int bn = gemm_bn(M, true);
-  const int tiles = ceil_div(N, kTileN) * ceil_div(M, bn);
-  return choose_splits(tiles, gemm_kb(K), gemm_slots(num_sms, bn));
+  return gemm_splits(ceil_div(N, kTileN) * ceil_div(M, bn), gemm_kb(K), bn, true);
 }
-// Split count of an inject-side GEMM: independent of the row count, so a
-// row's result does not depend on how many rows share the call.
-int inject_splits(const dflash_config& g, int num_sms, int N, int K) {
+// Split count of an inject-side GEMM: independent of the row count (sized
+// for a 32-row tile), so a row's result does not depend on how many rows
+// share the call.
+int inject_splits(const dflash_config& g, int N, int K, bool split) {
   if (g.dtype != DFLASH_BF16) return 1;
-  return choose_splits(ceil_div(N, kTileN), gemm_kb(K), gemm_slots(num_sms, 32));
+  return gemm_splits(ceil_div(N, kTileN), gemm_kb(K), 32, split);
 }
 
 // Rows of the packed gate/up weight: groups of 64 features, 64 gate rows then
@@ -392,7 +388,7 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t
     DF_CHECK(launch_alloc(ctx, n_rows, first_seq, B, max_rows, s));
     DF_CHECK(launch_gather_rows(ctx, feats, rows, max_rows, first_seq, s));
   }
-  const int s_fc = inject_splits(g, ctx->num_sms, d, Fin);
+  const int s_fc = inject_splits(g, d, Fin, false);
   {
     ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
     EpiArgs e = epi_base(ctx, EPI_STORE, rows, d);
@@ -404,7 +400,7 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t
     ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
     DF_CHECK(launch_fc_norm(ctx, rows, s));
   }
-  const int s_kv = inject_splits(g, ctx->num_sms, Nkv, d);
+  const int s_kv = inject_splits(g, Nkv, d, true);
   {
     ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
     EpiArgs e = epi_base(ctx, EPI_KV_INJECT, rows, Nkv);
@@ -431,12 +427,11 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
   cudaStream_t s = stream;
   const int M = B * kBlockK, Mmax = g.max_batch * kBlockK;
   const int d = g.hidden, F = g.ffn, qd = g.n_q_heads * g.head_dim, kvd = g.n_kv_heads * g.head_dim;
-  const int sms = ctx->num_sms;
   const int Nqkv = qd + 2 * kvd, Ngu = gu_rows(F);
-  const int s_qkv = draft_splits(g, sms, M, Nqkv, d);
-  const int s_o = draft_splits(g, sms, M, d, qd);
-  const int s_gu = draft_splits(g, sms, M, Ngu, d);
-  const int s_dn = draft_splits(g, sms, M, d, F);
+  const int s_qkv = draft_splits(g, M, Nqkv, d);
+  const int s_o = draft_splits(g, M, d, qd);
+  const int s_gu = draft_splits(g, M, Ngu, d);
+  const int s_dn = draft_splits(g, M, d, F);
   const int a_sp = attn_splits(ctx, B);
   for (int pass = 0; pass < S; ++pass) {
     {

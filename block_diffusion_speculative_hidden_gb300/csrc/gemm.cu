@@ -369,18 +369,6 @@ static bool get_tmap(dflash_ctx* c, const void* ptr, int rows, int cols, int box
 
 int gemm_kb(int K) { return (K + kTileK - 1) / kTileK; }
 
-// Split-K count for a GEMM with n_tiles output tiles and n_kb k-blocks: at
-// most `slots` CTAs in total (one wave), at most 8 (one portable cluster), at
-// least 4 k-blocks per split, and normalised so that every split owns at
-// least one k-block.
-int choose_splits(int n_tiles, int n_kb, int slots) {
-  // as many splits as keep the whole grid inside one wave of `slots` CTAs
-  int s = std::min(8, slots / std::max(1, n_tiles));
-  s = std::max(1, std::min(s, std::max(1, n_kb / 4)));
-  const int per = (n_kb + s - 1) / s;
-  return (n_kb + per - 1) / per;
-}
-
 template <int BN, bool LM, bool SPLIT>
 static cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& tw, const CUtensorMap& tx,
                              const CUtensorMap& txlo, cudaStream_t s) {
@@ -409,7 +397,7 @@ static cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorM
   p.logits = g.logits;
   p.ld_logits = g.ld_logits;
   p.skip_rows = g.skip_rows;
-  // splits come from choose_splits: every split owns at least one k-block
+  // splits come from gemm_splits: every split owns at least one k-block
   dim3 grid((g.N + kTileN - 1) / kTileN, (g.M + BN - 1) / BN, g.splits);
   if (LM || g.epi.kind == EPI_NONE || g.splits == 1) {
     k_gemm_tc<BN, LM, SPLIT><<<grid, 128, C::SMEM, s>>>(tw, tx, txlo, p);
@@ -451,6 +439,62 @@ static cudaError_t launch_tc_bn(dflash_ctx* c, const GemmLaunch& g, int bn, cons
         return lm ? launch_tc<256, true, false>(c, g, tw, tx, txlo, s)
                   : launch_tc<256, false, false>(c, g, tw, tx, txlo, s);
   }
+}
+
+// How many clusters of `cluster` CTAs of the projection kernel (tile width
+// bn, hi+lo operands or not) can be resident at once on this device.  GPCs
+// have uneven SM counts, so this is not simply SMs x CTAs-per-SM / cluster.
+template <int BN, bool SPLIT>
+static int max_clusters_t(int cluster) {
+  using C = TcCfg<BN, SPLIT>;
+  if (cudaFuncSetAttribute(k_gemm_tc<BN, false, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(1, 1, cluster);
+  lc.blockDim = dim3(128);
+  lc.dynamicSmemBytes = C::SMEM;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = cluster;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<BN, false, SPLIT>, &lc) != cudaSuccess) return 0;
+  return n;
+}
+
+int gemm_max_clusters(int bn, bool split, int cluster) {
+  static int cache[2][5][9] = {};  // [split][log2(bn/16)][cluster]
+  int bi = 0;
+  while ((16 << bi) < bn && bi < 4) ++bi;
+  if (cluster < 1 || cluster > 8) return 0;
+  int& c = cache[split ? 1 : 0][bi][cluster];
+  if (c == 0) {
+    switch (bi) {
+      case 0: c = split ? max_clusters_t<16, true>(cluster) : max_clusters_t<16, false>(cluster); break;
+      case 1: c = split ? max_clusters_t<32, true>(cluster) : max_clusters_t<32, false>(cluster); break;
+      case 2: c = split ? max_clusters_t<64, true>(cluster) : max_clusters_t<64, false>(cluster); break;
+      case 3: c = split ? max_clusters_t<128, true>(cluster) : max_clusters_t<128, false>(cluster); break;
+      default: c = split ? 0 : max_clusters_t<256, false>(cluster); break;
+    }
+    if (c <= 0) c = -1;
+  }
+  return c;
+}
+
+// Split-K count for `n_tiles` output tiles of width bn: the largest split
+// count S <= 8 (a portable cluster) such that all n_tiles clusters of S CTAs
+// are resident at once, with at least 4 k-blocks per split; normalised so that
+// every split owns at least one k-block.
+int gemm_splits(int n_tiles, int n_kb, int bn, bool split) {
+  int s = std::min(8, std::max(1, n_kb / 4));
+  for (; s > 1; --s)
+    if (n_tiles <= gemm_max_clusters(bn, split, s)) break;
+  const int per = (n_kb + s - 1) / s;
+  return (n_kb + per - 1) / per;
 }
 
 int gemm_bn(int M, bool split) {

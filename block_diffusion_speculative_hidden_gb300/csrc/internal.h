@@ -81,6 +81,7 @@ struct dflash_ctx {
   float *attn_o, *attn_ml;
   int attn_max_splits;
   bool attn_maps_ready = false;
+  int attn_tc_max_splits = 0;  // 8 or 16, queried on first use
   CUtensorMap attn_map_k, attn_map_v;  // 4-D maps over the fp16 pool
   dflash::LmPartials lm;
   float* logits_ws;  // fp32 mode: full logits [M][V]
@@ -102,9 +103,10 @@ namespace dflash {
 
 // gemm.cu
 cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
-int choose_splits(int n_tiles, int n_kb, int slots);
 int gemm_kb(int K);
 int gemm_bn(int M, bool split);
+int gemm_max_clusters(int bn, bool split, int cluster);
+int gemm_splits(int n_tiles, int n_kb, int bn, bool split);
 cudaError_t gemm_launch_uncached(int* status, const GemmLaunch& g, cudaStream_t s);
 
 }  // namespace dflash

@@ -32,6 +32,7 @@ int attn_splits(dflash_ctx* c, int B);
 cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
 // attention_tc.cu (fp16 pool)
 cudaError_t launch_attention_tc(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
+int attention_tc_max_splits(dflash_ctx* c);
 
 // accept.cu
 cudaError_t launch_accept_greedy(int B, int K, const int32_t* d, const int32_t* y, int32_t* tau, int32_t* emitted,

@@ -147,16 +147,27 @@ __global__ void k_logits_tiles(const float* __restrict__ z, int V, LmPartials lm
   }
 }
 
-// One warp per row: merge the tile partials into (argmax, confidence).
+// One CTA per row: merge the tile partials into (argmax, confidence).
 // Confidence = max softmax probability = exp(max - LSE) = 1 / sum exp(z - max).
 // With `commit`, committed rows keep tok1/conf1 and only the others are merged.
-__global__ void k_lm_merge(LmPartials lm, int M, const int32_t* commit, const int32_t* tok1, const float* conf1,
-                           int32_t* tok_out, float* conf_out) {
-  const int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (m >= M) return;
+// Each thread folds a strided set of tiles (increasing column order), then the
+// CTA combines the per-thread states in a fixed tree, ties to the lower id.
+__device__ __forceinline__ void lm_fold(float& mx, float& se, int& ix, float om, float os, int oi) {
+  const float nm = fmaxf(mx, om);
+  const float ns = (mx > -INFINITY ? se * expf(mx - nm) : 0.f) + (om > -INFINITY ? os * expf(om - nm) : 0.f);
+  if (om > mx || (om == mx && oi < ix)) ix = oi;
+  mx = nm;
+  se = ns;
+}
+
+__global__ void __launch_bounds__(256) k_lm_merge(LmPartials lm, int M, const int32_t* commit, const int32_t* tok1,
+                                                  const float* conf1, int32_t* tok_out, float* conf_out) {
+  __shared__ float s_mx[8], s_se[8];
+  __shared__ int s_ix[8];
+  const int m = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (commit != nullptr && commit[m] != 0) {
-    if (lane == 0) {
+    if (threadIdx.x == 0) {
       tok_out[m] = tok1[m];
       if (conf_out != nullptr) conf_out[m] = conf1[m];
     }
@@ -165,28 +176,20 @@ __global__ void k_lm_merge(LmPartials lm, int M, const int32_t* commit, const in
   const long long base = static_cast<long long>(m) * lm.n_tiles;
   float mx = -INFINITY, se = 0.f;
   int ix = 0x7fffffff;
-  for (int t = lane; t < lm.n_tiles; t += 32) {  // tiles in increasing column order
-    const float tm = lm.mx[base + t], ts = lm.se[base + t];
-    const int ti = lm.idx[base + t];
-    if (tm > mx) {
-      se = se * expf(mx - tm) + ts;
-      mx = tm;
-      ix = ti;
-    } else {
-      se += ts * expf(tm - mx);
-    }
-  }
+  for (int t = threadIdx.x; t < lm.n_tiles; t += blockDim.x) lm_fold(mx, se, ix, lm.mx[base + t], lm.se[base + t], lm.idx[base + t]);
   for (int o = 16; o > 0; o >>= 1) {
-    const float om = __shfl_xor_sync(0xffffffffu, mx, o);
-    const float os = __shfl_xor_sync(0xffffffffu, se, o);
+    const float om = __shfl_xor_sync(0xffffffffu, mx, o), os = __shfl_xor_sync(0xffffffffu, se, o);
     const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
-    const float nm = fmaxf(mx, om);
-    const float ns = (mx > -INFINITY ? se * expf(mx - nm) : 0.f) + (om > -INFINITY ? os * expf(om - nm) : 0.f);
-    if (om > mx || (om == mx && oi < ix)) ix = oi;
-    mx = nm;
-    se = ns;
+    lm_fold(mx, se, ix, om, os, oi);
   }
   if (lane == 0) {
+    s_mx[warp] = mx;
+    s_se[warp] = se;
+    s_ix[warp] = ix;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) lm_fold(mx, se, ix, s_mx[w], s_se[w], s_ix[w]);
     tok_out[m] = ix;
     if (conf_out != nullptr) conf_out[m] = 1.f / se;
   }
@@ -268,7 +271,7 @@ cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const 
 
 cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,
                             cudaStream_t s) {
-  k_lm_merge<<<(M + 3) / 4, 128, 0, s>>>(c->lm, M, commit, c->tok1, c->conf1, tok_out, conf_out);
+  k_lm_merge<<<M, 256, 0, s>>>(c->lm, M, commit, c->tok1, c->conf1, tok_out, conf_out);
   return cudaGetLastError();
 }
 
