@@ -18,6 +18,8 @@ namespace dflash {
 
 __global__ void k_accept_greedy(int B, int K, const int32_t* __restrict__ d, const int32_t* __restrict__ y,
                                 int32_t* tau_out, int32_t* emitted, int32_t* n_emit) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(kAccThreads) k_accept_stochastic(int K, int V,
                                                                    int32_t* emitted, int32_t* n_emit) {
   __shared__ float s_a[32], s_b[32], s_c[32];
   __shared__ int s_i[32], s_j[32];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int tau = K;
   for (int i = 0; i <= K; ++i) {
@@ -180,18 +184,17 @@ __global__ void __launch_bounds__(kAccThreads) k_accept_stochastic(int K, int V,
 }
 
 cudaError_t launch_accept_greedy(int B, int K, const int32_t* d, const int32_t* y, int32_t* tau, int32_t* emitted,
-                                 int32_t* n_emit, cudaStream_t s) {
-  k_accept_greedy<<<(B + 3) / 4, 128, 0, s>>>(B, K, d, y, tau, emitted, n_emit);
-  return cudaGetLastError();
+                                 int32_t* n_emit, bool pdl, cudaStream_t s) {
+  return launch_k(k_accept_greedy, dim3((B + 3) / 4), dim3(128), 0, s, dim3(1), pdl, B, K, d, y, tau, emitted,
+                  n_emit);
 }
 
 cudaError_t launch_accept_stochastic(int B, int K, int V, const int32_t* d, const float* z, const float* q,
                                      float temperature, uint64_t seed, uint64_t round, int32_t* tau,
-                                     int32_t* emitted, int32_t* n_emit, cudaStream_t s) {
+                                     int32_t* emitted, int32_t* n_emit, bool pdl, cudaStream_t s) {
   const uint2 key = make_uint2(static_cast<uint32_t>(seed & 0xffffffffu), static_cast<uint32_t>(seed >> 32));
-  k_accept_stochastic<<<B, kAccThreads, 0, s>>>(K, V, d, z, q, 1.0f / temperature, key,
-                                                static_cast<uint32_t>(round & 0xffffffffu), tau, emitted, n_emit);
-  return cudaGetLastError();
+  return launch_k(k_accept_stochastic, dim3(B), dim3(kAccThreads), 0, s, dim3(1), pdl, K, V, d, z, q,
+                  1.0f / temperature, key, static_cast<uint32_t>(round & 0xffffffffu), tau, emitted, n_emit);
 }
 
 }  // namespace dflash

@@ -1,0 +1,768 @@
+// Block attention on the fifth-generation tensor cores (tcgen05) for the fp16
+// KV pool of bf16 workloads.
+//
+// The contraction is the one attention.cu computes in fp32: the K block
+// queries of one sequence attend, unmasked, to every injected context key
+// and to all K keys of the block itself (DFlash Guide, "1. Single-Pass
+// Block-Diffusion Drafting": bidirectional attention inside the masked
+// block; "3. Cross-Layer KV Injection": the context keys come from the
+// target's fused features).  Layout and schedule:
+//
+//   - one CTA per (sequence, kv head, key split), 10 warps: warps 0-7 run
+//     the softmax (two per TMEM lane quadrant, splitting the pages of a
+//     block), warp 8 drives TMA, one thread of warp 9 issues the MMAs;
+//   - the split's pages are taken KBP pages (16*KBP keys) at a time through
+//     an NST-deep ring of K / V tiles (4-D TMA, 128-byte swizzle);
+//   - S = Q K^T is one MMA chain per key block (query rows on M = 64 or
+//     128, keys on N, accumulated in TMEM); the softmax threads read S, form
+//     the block's row max, P = 2^(S*scale - max) in fp16 (written over the
+//     block's K tile, the A operand of the next MMA) and the running sums;
+//     O_blk = P V reuses the same TMEM columns (V enters as an MN-major
+//     operand); the threads fold O_blk into fp32 registers with the
+//     online-softmax rescale;
+//   - only the real query rows of Q and P are stored: the MMA's padding rows
+//     (G*16 .. 127) read whatever follows in shared memory, and the results
+//     in those rows are never used;
+//   - everything that does not depend on the QKV projection (barriers, TMEM,
+//     page ids, the context pages) is set up before the programmatic-launch
+//     wait; q and the block page come after it;
+//   - with several splits, the splits of one (sequence, kv head) form a
+//     cluster and merge (o, m, l) with bulk copies between the CTAs' shared
+//     memories.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace dflash {
+
+namespace {
+
+constexpr int kMergeMax = 16;  // splits merged in one cluster (16 needs the non-portable size)
+constexpr int kAttnThreads = 320;  // 8 softmax warps, the TMA warp, the MMA warp
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+
+// TMEM layout of the accumulators (rows = query rows, columns = keys or head
+// dims): with M = 64, row r sits in lane 32*(r/16) + r%16; with M = 128, row
+// r in lane r.  The softmax reads 16-lane blocks with the 16x256b shape:
+// thread t of the warp gets rows t/4 and t/4 + 8 of the block, columns
+// 2*(t%4) and 2*(t%4) + 1 of every 8-column group.
+template <int DH, int G, int KBP, int NST>
+struct MmaAttnCfg {
+  static constexpr int R = G * 16;                 // real query rows
+  static constexpr int M = R <= 64 ? 64 : 128;     // MMA rows
+  static constexpr int SUB = M / 64;               // 16-lane row blocks per TMEM quadrant
+  static constexpr int QUADS = R <= 64 ? R / 16 : 4;  // quadrants holding real rows
+  static constexpr int RPT = 2 * SUB;              // rows per softmax thread
+  static constexpr int RPT_MAX = 4;
+  static constexpr int NCH = DH / 64;              // 128-byte column chunks of a head
+  static constexpr int Q_CH = R * 128;             // stride of the Q chunks (real rows only)
+  static constexpr int Q_BYTES = NCH * Q_CH;
+  static constexpr int P_CHUNKS = (KBP * 16 + 63) / 64;
+  static constexpr int P_CH = R * 128;
+  static constexpr int P_BYTES = P_CHUNKS * P_CH;
+  static constexpr int KV_CH = KBP * 16 * 128;     // one 64-column chunk of the K (or V) tile
+  static constexpr int KV_BYTES = NCH * KV_CH;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K then V
+  // P overwrites the block's K tile (dead once S is computed) when it fits
+  static constexpr bool P_IN_K = P_BYTES <= KV_BYTES;
+  static constexpr int OFF_P = Q_BYTES;
+  static constexpr int OFF_KV = OFF_P + (P_IN_K ? 0 : P_BYTES);
+  static constexpr int OFF_BAR = OFF_KV + NST * STAGE_BYTES;
+  static constexpr int BAR_BYTES = 128 + 8 * 32 * RPT_MAX * 4;  // barriers, then the pair-exchange slots
+  static constexpr int SMEM_FIXED = 1024 + OFF_BAR + BAR_BYTES;  // + 4 bytes per page id
+  static constexpr int TMEM_COLS = 256;
+  static_assert(KBP * 16 <= 256 && DH <= 256, "S and O share 256 TMEM columns");
+  // the padding rows (R .. M-1) of the last Q / P chunk read into the
+  // following buffers, never past the allocation
+  static_assert((NCH - 1) * Q_CH + M * 128 <= OFF_BAR + BAR_BYTES, "Q padding rows stay inside");
+  static_assert((P_IN_K ? OFF_KV + (NST - 1) * STAGE_BYTES : OFF_P) + (P_CHUNKS - 1) * P_CH + M * 128 <=
+                    OFF_BAR + BAR_BYTES,
+                "P padding rows stay inside");
+  // the staged rows [R][DH + 4] and the received split partials [splits][rows
+  // per split][DH + 4] (at most R + kMergeMax rows) reuse Q, P and the ring
+  static_assert((2 * R + kMergeMax) * (DH + 4) * 4 <= OFF_BAR, "split partials must fit");
+};
+
+struct MmaAttnParams {
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  int max_pages, block_page0, pool_pages, layer;
+  int Hkv, splits;
+  int page_slots;     // capacity of the shared-memory page-id list
+  float scale_log2;   // log2(e) / sqrt(dh)
+  void* o_hi;         // ActOut<bf16> of the attention output [B*16][Hq*DH]
+  void* o_lo;
+  int* status;
+};
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 16 TMEM lanes x 16 (x2) or 32 (x4) columns in the 16x256b fragment layout.
+__device__ __forceinline__ void tc_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tc_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to the
+// shared memory of cluster CTA `rank` (same offsets), completing as
+// transaction bytes on that CTA's mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy_to_rank(uint32_t dst_local, uint32_t src_local, uint32_t bytes,
+                                                  uint64_t* bar, uint32_t rank) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dsmem_map(dst_local, rank)),
+      "r"(src_local), "r"(bytes), "r"(dsmem_map(smem_u32(bar), rank))
+      : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+template <int DH, int G, int KBP, int NST>
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_constant__ CUtensorMap tmQ,
+                                                              const __grid_constant__ CUtensorMap tmK,
+                                                              const __grid_constant__ CUtensorMap tmV,
+                                                              const __grid_constant__ MmaAttnParams p) {
+  using C = MmaAttnCfg<DH, G, KBP, NST>;
+  constexpr int R = C::R;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sP = smem + C::OFF_P;
+  uint8_t* sKV = smem + C::OFF_KV;
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_empty = kv_full + NST;
+  uint64_t* q_full = kv_empty + NST;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* p_full = q_full + 2;
+  uint64_t* o_full = q_full + 3;
+  uint64_t* o_free = q_full + 4;
+  uint64_t* recv_bar = q_full + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 6);
+  float* s_red = reinterpret_cast<float*>(smem + C::OFF_BAR + 128);  // [8 warps][32 lanes][2] pair exchange
+  int* s_pages = reinterpret_cast<int*>(smem + C::OFF_BAR + C::BAR_BYTES);
+
+  const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.seq_len[b];
+  const int n_ctx_pages = (T + kPage - 1) / kPage;
+  const int n_pages = n_ctx_pages + 1;  // + the block page
+  const int per_split = (n_pages + p.splits - 1) / p.splits;
+  const int vp_begin = min(n_pages, sp * per_split), vp_end = min(n_pages, vp_begin + per_split);
+  const int np = min(vp_end - vp_begin, p.page_slots);
+  const int nblk = (np + KBP - 1) / KBP;
+  constexpr int SOFT = 2 * C::QUADS * 32;  // softmax threads: two warps per TMEM quadrant holding real rows
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, SOFT);
+    mbar_init(o_full, 1);
+    mbar_init(o_free, SOFT);
+    mbar_init(recv_bar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kProducerWarp) {
+    // page ids of this split (context pages, then the block page), so that
+    // issuing a block never waits on a global load
+    for (int j = lane; j < np; j += 32) {
+      const int vp = vp_begin + j;
+      s_pages[j] = vp < n_ctx_pages ? p.page_table[b * p.max_pages + vp] : p.block_page0 + b;
+    }
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Softmax warps: warp w serves TMEM quadrant qd = w % 4 (rows of that
+  // quadrant) and half hf = w / 4 of each block's pages (and of the head
+  // dims of O).  Thread state: RPT rows x (2 of every 8 of its head dims).
+  // With a single stage the split is one key block (np <= page_slots <= KBP)
+  // and O stays in TMEM until the output; otherwise it is folded into
+  // registers with the online-softmax rescale.
+  constexpr int RPT = C::RPT, OG = DH / 16;  // 8-column groups per half of the head dims
+  constexpr bool ONE = NST == 1;
+  const int qd = warp & 3, hf = warp >> 2;
+  const bool soft = warp < 8 && qd < C::QUADS;
+  float o_acc[ONE ? 1 : RPT][ONE ? 1 : 2 * OG];
+  float m_run[RPT], l_run[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
+#pragma unroll
+    for (int d = 0; d < (ONE ? 1 : 2 * OG); ++d) o_acc[ONE ? 0 : i][d] = 0.f;
+  }
+  const int c4 = lane & 3, rq = lane >> 2;
+  // query row of state row i (i = 2*sb + h: 16-lane block sb, half h) and its TMEM lane block
+  auto row_of = [&](int i) { return (C::M == 64 ? 16 * qd : 32 * qd + 16 * (i >> 1)) + rq + 8 * (i & 1); };
+  auto lanes_of = [&](int sb) { return static_cast<uint32_t>(C::M == 64 ? 32 * qd : 32 * qd + 16 * sb) << 16; };
+  // pair exchange of per-row values between the two warps of a quadrant
+  auto pair_combine = [&](float (&v)[RPT], bool is_max) {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) s_red[(warp * 32 + lane) * RPT + i] = v[i];
+    named_sync(1 + qd, 64);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float o = s_red[(((warp + 4) & 7) * 32 + lane) * RPT + i];
+      v[i] = is_max ? fmaxf(v[i], o) : v[i] + o;
+    }
+    named_sync(1 + qd, 64);  // the slots may be reused
+  };
+
+  if (warp == kProducerWarp) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      const int l_off = p.layer * p.pool_pages;
+      bool waited = false;
+      auto issue = [&](int blk, bool may_wait) {
+        const int s = blk % NST;
+        const int pg0 = blk * KBP, npb = min(KBP, np - pg0);
+        mbar_arrive_expect_tx(&kv_full[s], 2 * npb * C::NCH * 2048);
+        uint8_t* kd = sKV + s * C::STAGE_BYTES;
+        uint8_t* vd = kd + C::KV_BYTES;
+        for (int j = 0; j < npb; ++j) {
+          if (vp_begin + pg0 + j == n_ctx_pages && !waited) {
+            // the block page is written by the QKV projection
+            if (!may_wait) return false;
+            pdl_wait();
+            waited = true;
+          }
+          const int page = s_pages[pg0 + j];
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_load_4d(kd + c * C::KV_CH + j * 2048, &tmK, &kv_full[s], c * 64, 0, kvh, l_off + page);
+            tma_load_4d(vd + c * C::KV_CH + j * 2048, &tmV, &kv_full[s], c * 64, 0, kvh, l_off + page);
+          }
+        }
+        return true;
+      };
+      int blk = 0;
+      // context-only blocks stream while the QKV projection is still running
+      for (; blk < nblk && blk < NST; ++blk) {
+        const int last_vp = vp_begin + min(np, (blk + 1) * KBP) - 1;
+        if (last_vp >= n_ctx_pages) break;
+        issue(blk, false);
+      }
+      pdl_wait();
+      waited = true;
+      mbar_arrive_expect_tx(q_full, G * C::NCH * 2048);
+      for (int g = 0; g < G; ++g)
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_2d(sQ + c * C::Q_CH + g * 2048, &tmQ, q_full, (kvh * G + g) * DH + c * 64, b * kBlockK);
+      pdl_trigger();
+      int issued = blk;
+      for (; blk < nblk; ++blk) {
+        if (blk >= NST && !mbar_wait(&kv_empty[blk % NST], ((blk / NST) & 1) ^ 1, p.status)) break;
+        issue(blk, true);
+        issued = blk + 1;
+      }
+      // every copy this CTA issued must have landed before it exits (bounded)
+      for (int i = max(0, issued - NST); i < issued; ++i) mbar_wait(&kv_full[i % NST], (i / NST) & 1, p.status);
+      mbar_wait(q_full, 0, p.status);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      bool ok = nblk == 0 || mbar_wait(q_full, 0, p.status);
+      for (int blk = 0; ok && blk < nblk; ++blk) {
+        const int s = blk % NST;
+        const int npb = min(KBP, np - blk * KBP);
+        if (!mbar_wait(&kv_full[s], (blk / NST) & 1, p.status)) break;
+        if (blk > 0 && !mbar_wait(o_free, (blk - 1) & 1, p.status)) break;
+        tc_fence_after();
+        const uint32_t aq = smem_u32(sQ), ak = smem_u32(sKV + s * C::STAGE_BYTES);
+        const uint32_t av = ak + C::KV_BYTES, ap = C::P_IN_K ? ak : smem_u32(sP);
+        const uint32_t id_s = mma_idesc_f16_f32(C::M, 16 * npb, false);
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;
+          tc_mma_bf16(tmem, sw128_desc(aq + (ks >> 2) * C::Q_CH + off, 16, 1024),
+                      sw128_desc(ak + (ks >> 2) * C::KV_CH + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full);
+        if (!mbar_wait(p_full, blk & 1, p.status)) break;
+        tc_fence_after();
+        const uint32_t id_o = mma_idesc_f16_f32(C::M, DH, true);
+        for (int k16 = 0; k16 < npb; ++k16)
+          tc_mma_bf16(tmem, sw128_desc(ap + (k16 >> 2) * C::P_CH + (k16 & 3) * 32, 16, 1024),
+                      sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, k16 > 0 ? 1u : 0u);
+        tc_commit(o_full);
+        tc_commit(&kv_empty[s]);
+      }
+    }
+    __syncwarp();
+  } else if (soft) {
+    // ---------------- softmax.  The two warps of a quadrant meet at named
+    // barriers, so both always run every block: a wait that gives up only
+    // marks the work as failed (status word) and later waits are skipped.
+    bool live = true;
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int npb = min(KBP, np - blk * KBP);
+      const int vp0 = vp_begin + blk * KBP;
+      // this warp's pages of the block: [pg_lo, pg_hi)
+      const int pg_split = (npb + 1) >> 1;
+      const int pg_lo = hf == 0 ? 0 : pg_split, pg_hi = hf == 0 ? pg_split : npb;
+      live = live && mbar_wait(s_full, blk & 1, p.status);
+      __syncwarp();
+      tc_fence_after();
+      constexpr int HP = (KBP + 1) / 2;  // pages per warp at most
+      float alpha[RPT], lsum[RPT], mx[RPT];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) mx[i] = -INFINITY;
+      uint32_t sv[C::SUB][HP][8];
+      // S columns of this warp's pages in registers (one wait)
+#pragma unroll
+      for (int sb = 0; sb < C::SUB; ++sb)
+#pragma unroll
+        for (int j = 0; j < HP; ++j)
+          if (pg_lo + j < pg_hi) tc_ld_16x256b_x2(tmem + lanes_of(sb) + (pg_lo + j) * 16, sv[sb][j]);
+      tc_wait_ld();
+      // pass 1: row max over the valid keys
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        const int pg = pg_lo + j;
+        if (pg >= pg_hi) break;
+        const int vp = vp0 + pg;
+        const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // keys 2c4, 2c4+1, 8+2c4, 9+2c4
+          const int key = (q >> 1) * 8 + 2 * c4 + (q & 1);
+          if (key < nvalid)
+#pragma unroll
+            for (int sb = 0; sb < C::SUB; ++sb) {
+              mx[2 * sb] = fmaxf(mx[2 * sb], __uint_as_float(sv[sb][j][(q >> 1) * 4 + (q & 1)]));
+              mx[2 * sb + 1] = fmaxf(mx[2 * sb + 1], __uint_as_float(sv[sb][j][(q >> 1) * 4 + 2 + (q & 1)]));
+            }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+      }
+      pair_combine(mx, true);
+      float m_new[RPT];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        m_new[i] = fmaxf(m_run[i], mx[i] * p.scale_log2);
+        alpha[i] = m_run[i] == -INFINITY ? 0.f : exp2f(m_run[i] - m_new[i]);
+        m_run[i] = m_new[i];
+        lsum[i] = 0.f;
+      }
+      // pass 2: P = 2^(S scale - m) in fp16 into the swizzled A operand
+      uint8_t* pbase = C::P_IN_K ? sKV + (blk % NST) * C::STAGE_BYTES : sP;
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        const int pg = pg_lo + j;
+        if (pg >= pg_hi) break;
+        const int vp = vp0 + pg;
+        const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
+        uint8_t* pch = pbase + (pg >> 2) * C::P_CH;
+        const int u0 = 2 * (pg & 3);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+          const int sb = i >> 1, h = i & 1;
+          float e[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int key = (q >> 1) * 8 + 2 * c4 + (q & 1);
+            e[q] = key < nvalid ? exp2f(__uint_as_float(sv[sb][j][(q >> 1) * 4 + 2 * h + (q & 1)]) * p.scale_log2 -
+                                        m_new[i])
+                                : 0.f;
+          }
+          lsum[i] += (e[0] + e[1]) + (e[2] + e[3]);
+          const int r = row_of(i);
+          if (r < R) {
+            // keys 2*c4, 2*c4+1 of the page's first / second 8-key unit
+            uint8_t* prow = pch + r * 128 + 4 * c4;
+            *reinterpret_cast<uint32_t*>(prow + ((u0 ^ (r & 7)) << 4)) = pack_half2(e[0], e[1]);
+            *reinterpret_cast<uint32_t*>(prow + (((u0 + 1) ^ (r & 7)) << 4)) = pack_half2(e[2], e[3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) l_run[i] = l_run[i] * alpha[i] + lsum[i];
+      fence_proxy_async_smem();  // P is read by the tensor cores
+      tc_fence_before();
+      mbarrier_arrive_one(p_full);
+      live = live && mbar_wait(o_full, blk & 1, p.status);
+      __syncwarp();
+      tc_fence_after();
+      if constexpr (ONE) break;  // O stays in TMEM (a single block: both warps leave here)
+      // O_blk = P V: this warp's half of the head dims, folded with the rescale
+#pragma unroll
+      for (int sb = 0; sb < C::SUB; ++sb) {
+#pragma unroll
+        for (int d0 = 0; d0 < DH / 2; d0 += 32) {
+          uint32_t v[16];
+          tc_ld_16x256b_x4(tmem + lanes_of(sb) + hf * (DH / 2) + d0, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int i = 2 * sb + h, d = 2 * (d0 / 8 + gq) + e;
+                if constexpr (!ONE) o_acc[i][d] = o_acc[i][d] * alpha[i] + __uint_as_float(v[4 * gq + 2 * h + e]);
+              }
+        }
+      }
+      tc_fence_before();
+      mbarrier_arrive_one(o_free);
+    }
+    // full row sums: over the 4 threads of each row, then the warp pair
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 1);
+      l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
+    }
+    pair_combine(l_run, false);
+  }
+
+  // ---------------- output
+  const int Hq = p.Hkv * G, q_dim = Hq * DH;
+  ActOut<__nv_bfloat16> out{static_cast<__nv_bfloat16*>(p.o_hi), static_cast<__nv_bfloat16*>(p.o_lo)};
+  // visits this thread's unnormalised O values: f(state row i, head dim d, o[d], o[d + 1])
+  auto for_each_o = [&](auto&& f) {
+    if constexpr (ONE) {
+      const bool have = nblk > 0;  // with no keys O was never written (its l is 0)
+#pragma unroll
+      for (int sb = 0; sb < C::SUB; ++sb)
+#pragma unroll
+        for (int d0 = 0; d0 < DH / 2; d0 += 32) {
+          uint32_t v[16];
+          tc_ld_16x256b_x4(tmem + lanes_of(sb) + hf * (DH / 2) + d0, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              f(2 * sb + h, hf * (DH / 2) + d0 + 8 * gq + 2 * c4, have ? __uint_as_float(v[4 * gq + 2 * h]) : 0.f,
+                have ? __uint_as_float(v[4 * gq + 2 * h + 1]) : 0.f);
+        }
+    } else {
+#pragma unroll
+      for (int i = 0; i < RPT; ++i)
+#pragma unroll
+        for (int j = 0; j < OG; ++j) f(i, hf * (DH / 2) + 8 * j + 2 * c4, o_acc[i][2 * j], o_acc[i][2 * j + 1]);
+    }
+  };
+  if (p.splits == 1) {
+    if (soft) {
+      for_each_o([&](int i, int d, float o0, float o1) {
+        const int r = row_of(i);
+        if (r >= R) return;
+        const float inv = l_run[i] > 0.f ? 1.f / l_run[i] : 0.f;
+        const long long at = static_cast<long long>(b * kBlockK + (r & 15)) * q_dim + (kvh * G + (r >> 4)) * DH + d;
+        const float v0 = o0 * inv, v1 = o1 * inv;
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
+        const __nv_bfloat162 lv = __floats2bfloat162_rn(v0 - __low2float(hv), v1 - __high2float(hv));
+        *reinterpret_cast<__nv_bfloat162*>(out.hi + at) = hv;
+        *reinterpret_cast<__nv_bfloat162*>(out.lo + at) = lv;
+      });
+    }
+  } else {
+    // Split merge inside the cluster.  Each split stages its unnormalised
+    // rows (o, m, l) in row order; once every CTA is past its main loop
+    // (cluster barrier), one thread copies the rows owned by cluster rank k
+    // (rows k*rpr ..) into slot [split] of k's receive area with a bulk
+    // shared-memory copy that completes on k's mbarrier; each CTA then
+    // merges its rows from local memory in split order.  A final cluster
+    // barrier keeps every CTA (and so every copy source) alive until all
+    // copies have landed.
+    const int S = p.splits, cr = static_cast<int>(cluster_ctarank());
+    const int rpr = (R + S - 1) / S;
+    constexpr int LD = DH + 4;  // floats per row: o, m, l, pad (16-byte multiple)
+    float* stage = reinterpret_cast<float*>(smem);          // [R][LD] (Q, P and the ring are idle now)
+    float* recv = stage + R * LD;                           // [S][rpr][LD]
+    const int r0 = min(R, cr * rpr), r1 = min(R, r0 + rpr);
+    __syncthreads();
+    if (soft) {
+      for_each_o([&](int i, int d, float o0, float o1) {
+        const int r = row_of(i);
+        if (r < R) *reinterpret_cast<float2*>(stage + r * LD + d) = make_float2(o0, o1);
+      });
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int r = row_of(i);
+        if (r < R && c4 == 0 && hf == 0) *reinterpret_cast<float2*>(stage + r * LD + DH) = make_float2(m_run[i], l_run[i]);
+      }
+    }
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(S * (r1 - r0) * LD * 4));
+    fence_proxy_async_smem();
+    __syncthreads();
+    cluster_sync_all();  // every receive area is idle and armed
+    if (threadIdx.x == 0) {
+      for (int k = 0; k < S; ++k) {
+        const int k0 = min(R, k * rpr), k1 = min(R, k0 + rpr);
+        if (k1 > k0)
+          bulk_copy_to_rank(smem_u32(recv + cr * rpr * LD), smem_u32(stage + k0 * LD),
+                            static_cast<uint32_t>((k1 - k0) * LD * 4), recv_bar, static_cast<uint32_t>(k));
+      }
+    }
+    mbar_wait(recv_bar, 0, p.status);
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    for (int e = threadIdx.x; e < (r1 - r0) * (DH / 4); e += blockDim.x) {
+      const int j = e / (DH / 4), d4 = (e % (DH / 4)) * 4, r = r0 + j;
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, recv[(s2 * rpr + j) * LD + DH]);
+      float den = 0.f;
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float* row = recv + (s2 * rpr + j) * LD;
+        const float ms = row[DH];
+        if (ms == -INFINITY) continue;
+        const float w = exp2f(ms - M);
+        const float4 o4 = *reinterpret_cast<const float4*>(row + d4);
+        den += w * row[DH + 1];
+        num.x += w * o4.x;
+        num.y += w * o4.y;
+        num.z += w * o4.z;
+        num.w += w * o4.w;
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const long long base = static_cast<long long>(b * kBlockK + (r & 15)) * q_dim + (kvh * G + (r >> 4)) * DH + d4;
+      out.put(base + 0, num.x * inv);
+      out.put(base + 1, num.y * inv);
+      out.put(base + 2, num.z * inv);
+      out.put(base + 3, num.w * inv);
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_mma() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// The fp16 pool [L*pool_pages][Hkv][16][dh] as a 4-D map with 16 x 64 boxes.
+bool pool_map4(const void* base, int dh, int Hkv, long long pages_total, CUtensorMap* out) {
+  auto fn = encode_fn_mma();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(dh), 16, static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(pages_total)};
+  cuuint64_t gstride[3] = {static_cast<cuuint64_t>(dh) * 2, static_cast<cuuint64_t>(dh) * 2 * 16,
+                           static_cast<cuuint64_t>(dh) * 2 * 16 * Hkv};
+  cuuint32_t box[4] = {64, 16, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), gdim, gstride, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The block queries q [rows][Hq*dh] (fp16) as a 2-D map with 16-row x 64-column boxes.
+bool q_map(const void* base, int rows, int cols, CUtensorMap* out) {
+  auto fn = encode_fn_mma();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t es[2] = {1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DH, int G, int KBP, int NST>
+int smem_bytes(int page_slots) {
+  return MmaAttnCfg<DH, G, KBP, NST>::SMEM_FIXED + 4 * page_slots;
+}
+
+template <int DH, int G, int KBP, int NST>
+cudaError_t set_attrs(int smem) {
+  static int attr_smem = 0;
+  static bool np = false;
+  if (!np) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<DH, G, KBP, NST>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    np = true;
+  }
+  if (smem > attr_smem) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<DH, G, KBP, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_smem = smem;
+  }
+  return cudaSuccess;
+}
+
+// Pages one split can hold at most (the split's share of the longest
+// sequence plus its block page).
+int split_pages_bound(const dflash_ctx* c, int splits) {
+  return (c->cfg.max_pages_per_seq + 1 + splits - 1) / splits;
+}
+
+template <int DH, int G, int KBP, int NST>
+cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
+  const auto& g = c->cfg;
+  const int page_slots = split_pages_bound(c, splits);
+  const int smem = smem_bytes<DH, G, KBP, NST>(page_slots);
+  cudaError_t e = set_attrs<DH, G, KBP, NST>(smem);
+  if (e != cudaSuccess) return e;
+  if (!c->attn_maps_ready) {
+    const long long pages_total = static_cast<long long>(g.n_layers) * c->pool_pages;
+    if (!pool_map4(c->pool_k, DH, g.n_kv_heads, pages_total, &c->attn_map_k) ||
+        !pool_map4(c->pool_v, DH, g.n_kv_heads, pages_total, &c->attn_map_v) ||
+        !q_map(c->q, g.max_batch * kBlockK, g.n_q_heads * DH, &c->attn_map_q))
+      return cudaErrorInvalidValue;
+    c->attn_maps_ready = true;
+  }
+  MmaAttnParams p;
+  p.page_table = c->page_table;
+  p.seq_len = c->seq_len;
+  p.max_pages = g.max_pages_per_seq;
+  p.block_page0 = g.n_pages;
+  p.pool_pages = c->pool_pages;
+  p.layer = layer;
+  p.Hkv = g.n_kv_heads;
+  p.splits = splits;
+  p.page_slots = page_slots;
+  p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
+  p.o_hi = c->o;
+  p.o_lo = c->o_lo;
+  p.status = c->status;
+  return launch_k(k_attn_mma<DH, G, KBP, NST>, dim3(splits, g.n_kv_heads, B), dim3(kAttnThreads), smem, s,
+                  dim3(splits, 1, 1), c->pdl, c->attn_map_q, c->attn_map_k, c->attn_map_v, p);
+}
+
+// How many clusters of `splits` CTAs of this kernel instance can be
+// resident at once (0 if unknown).
+template <int DH, int G, int KBP, int NST>
+int max_clusters_t(dflash_ctx* c, int splits) {
+  const int smem = smem_bytes<DH, G, KBP, NST>(split_pages_bound(c, splits));
+  if (set_attrs<DH, G, KBP, NST>(smem) != cudaSuccess ||
+      !prefer_max_smem(reinterpret_cast<const void*>(k_attn_mma<DH, G, KBP, NST>))) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(splits, 1, 1);
+  lc.blockDim = dim3(kAttnThreads);
+  lc.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = splits;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_attn_mma<DH, G, KBP, NST>, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Short splits (at most 13 pages): all keys in one block, no ring, and a CTA
+// small enough to share an SM with a projection CTA (so the context streams
+// in while the QKV projection runs); longer splits stream 8-page blocks
+// through a 2-deep ring.
+constexpr int kShortPages = 13;
+
+// Runs F<DH, G, KBP, NST>(args) for the kernel instance serving `splits`.
+template <template <int, int, int, int> class F, typename... A>
+auto dispatch(dflash_ctx* c, int splits, A... args) {
+  const bool short_split = split_pages_bound(c, splits) <= kShortPages;
+  const int G = c->cfg.n_q_heads / c->cfg.n_kv_heads;
+  const bool d64 = c->cfg.head_dim == 64;
+#define DFLASH_ATTN_CASE(DH_, G_)                                                              \
+  if (c->cfg.head_dim == DH_ && G == G_)                                                       \
+    return short_split ? F<DH_, G_, kShortPages, 1>::run(c, splits, args...)                   \
+                       : F<DH_, G_, 8, 2>::run(c, splits, args...);
+  DFLASH_ATTN_CASE(64, 1) DFLASH_ATTN_CASE(64, 2) DFLASH_ATTN_CASE(64, 4) DFLASH_ATTN_CASE(64, 8)
+  DFLASH_ATTN_CASE(128, 1) DFLASH_ATTN_CASE(128, 2) DFLASH_ATTN_CASE(128, 4) DFLASH_ATTN_CASE(128, 8)
+#undef DFLASH_ATTN_CASE
+  (void)d64;
+  return F<64, 1, 8, 2>::invalid();
+}
+
+template <int DH, int G, int KBP, int NST>
+struct LaunchF {
+  static cudaError_t run(dflash_ctx* c, int splits, int layer, int B, cudaStream_t s) {
+    return launch_t<DH, G, KBP, NST>(c, layer, B, splits, s);
+  }
+  static cudaError_t invalid() { return cudaErrorInvalidValue; }
+};
+
+template <int DH, int G, int KBP, int NST>
+struct ClustersF {
+  static int run(dflash_ctx* c, int splits) { return max_clusters_t<DH, G, KBP, NST>(c, splits); }
+  static int invalid() { return 0; }
+};
+
+}  // namespace
+
+// Key splits per (sequence, kv head): the largest count up to 16 (and about
+// two CTAs per SM overall) whose clusters all fit on the device at once;
+// when none does, the plain share of the SMs.  GPCs bound how many clusters
+// of a given size can be resident (on a GB300, 7 of 16 CTAs but 8 of 12), so
+// the largest split is not always the fastest.
+int attention_mma_splits(dflash_ctx* c, int B) {
+  const int heads = B * c->cfg.n_kv_heads;
+  const int s0 = std::max(1, std::min({kMergeMax, (2 * c->num_sms + heads - 1) / heads, c->attn_max_splits}));
+  for (int S = s0; S > 1; --S) {
+    int& n = c->attn_fit[S];
+    if (n == 0) n = std::max(-1, dispatch<ClustersF>(c, S));
+    if (n >= heads) return S;
+  }
+  return s0;
+}
+
+cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
+  return dispatch<LaunchF>(c, splits, layer, B, s);
+}
+
+}  // namespace dflash

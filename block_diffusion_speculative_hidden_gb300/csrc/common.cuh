@@ -81,6 +81,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the inject / draft chain is launched so that it may start
+// while its stream predecessor is still running.  The rule that keeps this
+// race-free everywhere in the library:
+//   - before pdl_wait() a kernel touches only data that its immediate
+//     predecessor neither writes nor reads back (weights, tensor maps, the
+//     context pages of the KV pool, its own shared memory);
+//   - pdl_trigger() (which lets the successor start) comes after pdl_wait()
+//     in every CTA, so when a kernel starts, every kernel before its
+//     predecessor has completed.
+// pdl_wait() returns once the predecessor grid has completed and its memory
+// is visible; without a programmatic dependency both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- clusters / DSMEM
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -105,6 +120,9 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+__device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   float v;
@@ -208,6 +226,41 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
+
+// Shared-memory matrix descriptor with 128-byte swizzling and explicit
+// leading / stride byte offsets.  K-major operands: rows of 128 bytes, 8-row
+// groups `sbo` apart (lbo unused).  MN-major operands: 64 MN-elements per
+// 128-byte row, K rows 128 bytes apart, 8-row K groups `sbo` apart and the
+// next 64 MN-elements `lbo` bytes away.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with fp16 A and B (format
+// 0) and an fp32 accumulator; b_mn: B is MN-major (bit 16).
+__host__ __device__ constexpr uint32_t mma_idesc_f16_f32(int m, int n, bool b_mn) {
+  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// tcgen05.ld without the trailing wait: several loads may be in flight; call
+// tc_wait_ld() before using any of the registers.
+__device__ __forceinline__ void tc_ld_32x32b_x16_nw(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
 // 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 =

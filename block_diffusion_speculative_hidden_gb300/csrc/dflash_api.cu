@@ -2,7 +2,9 @@
 // and the sequence of kernels behind dflash_inject_kv, dflash_draft_block and
 // dflash_accept.  All device memory is the caller's; nothing here allocates.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "common.cuh"
@@ -10,6 +12,25 @@
 #include "kernels.cuh"
 
 using namespace dflash;
+
+namespace dflash {
+
+bool prefer_max_smem(const void* kernel) {
+  // a fixed table (no host heap): the library has a few dozen kernel instances
+  static std::mutex mu;
+  static const void* done[256];
+  static int n_done = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i] == kernel) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+      cudaSuccess)
+    return false;
+  if (n_done < 256) done[n_done++] = kernel;
+  return true;
+}
+
+}  // namespace dflash
 
 namespace {
 
@@ -23,17 +44,17 @@ int kv_elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Split count of one draft-side GEMM for M activation rows (hi/lo inputs).
-int draft_splits(const dflash_config& g, int M, int N, int K) {
+int draft_splits(const dflash_config& g, int M, int N, int K, int num_sms, int max_ctas = 0) {
   if (g.dtype != DFLASH_BF16) return 1;
   const int bn = gemm_bn(M, true);
-  return gemm_splits(ceil_div(N, kTileN) * ceil_div(M, bn), gemm_kb(K), bn, true);
+  return gemm_splits(ceil_div(N, kTileN) * ceil_div(M, bn), gemm_kb(K), bn, true, num_sms, max_ctas);
 }
 // Split count of an inject-side GEMM: independent of the row count (sized
 // for a 32-row tile), so a row's result does not depend on how many rows
 // share the call.
-int inject_splits(const dflash_config& g, int N, int K, bool split) {
+int inject_splits(const dflash_config& g, int N, int K, bool split, int num_sms) {
   if (g.dtype != DFLASH_BF16) return 1;
-  return gemm_splits(ceil_div(N, kTileN), gemm_kb(K), 32, split);
+  return gemm_splits(ceil_div(N, kTileN), gemm_kb(K), 32, split, num_sms);
 }
 
 // Rows of the packed gate/up weight: groups of 64 features, 64 gate rows then
@@ -126,6 +147,9 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   auto tok1 = static_cast<int32_t*>(w.take(sizeof(int32_t) * M));
   auto conf1 = static_cast<float*>(w.take(sizeof(float) * M));
   auto commit = static_cast<int32_t*>(w.take(sizeof(int32_t) * M));
+  const size_t d_tiles = ceil_div(d, kTileN);
+  auto ss_x = static_cast<float*>(w.take(sizeof(float) * d_tiles * M));
+  auto ss_h = static_cast<float*>(w.take(sizeof(float) * d_tiles * R));
   if (c != nullptr) {
     c->status = status;
     c->scal = status + 4;
@@ -156,6 +180,8 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
     c->tok1 = tok1;
     c->conf1 = conf1;
     c->commit = commit;
+    c->ss_x = ss_x;
+    c->ss_h = ss_h;
   }
   return w.off;
 }
@@ -209,6 +235,25 @@ EpiArgs epi_base(dflash_ctx* c, int kind, int M, int N) {
   e.rope_cos = c->rope_cos;
   e.rope_sin = c->rope_sin;
   return e;
+}
+
+// Folded RMSNorm over the hidden size (epilogue.cuh), consumer side: the
+// projection's input is g . z and its output rows are scaled by 1 / RMS(z).
+void norm_in(dflash_ctx* c, EpiArgs& e, const float* ss, int ss_ld) {
+  e.ss_in = ss;
+  e.ss_tiles = ceil_div(c->cfg.hidden, kTileN);
+  e.norm_dim_inv = 1.f / static_cast<float>(c->cfg.hidden);
+  e.eps = c->cfg.rms_eps;
+  e.ss_ld = ss_ld;
+}
+// Producer side: the stored rows z also become the next input g . z (hi, lo)
+// with their partial sums of squares.
+void norm_out(EpiArgs& e, void* hi, void* lo, const void* gain, float* ss, int ss_ld) {
+  e.nx_hi = hi;
+  e.nx_lo = lo;
+  e.nx_gain = gain;
+  e.ss_out = ss;
+  e.ss_ld = ss_ld;
 }
 
 char* pool_layer(void* pool, const dflash_ctx* c, int layer) {
@@ -322,6 +367,10 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, v
   c->w_down.assign(w->w_down, w->w_down + cfg->n_layers);
   c->g_in.assign(w->g_in, w->g_in + cfg->n_layers);
   c->g_post.assign(w->g_post, w->g_post + cfg->n_layers);
+  {
+    const char* env = std::getenv("DFLASH_PDL");
+    c->pdl = env == nullptr || std::strcmp(env, "0") != 0;
+  }
   c->pool_pages = cfg->n_pages + cfg->max_batch;
   c->kv_elem = kv_elem_bytes(*cfg);
   const size_t half_pool = dflash_kv_pool_size(cfg) / 2;
@@ -386,24 +435,24 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t
   {
     ProfScope p(ctx, DFLASH_PROF_ROWWISE, 2, s);
     DF_CHECK(launch_alloc(ctx, n_rows, first_seq, B, max_rows, s));
-    DF_CHECK(launch_gather_rows(ctx, feats, rows, max_rows, first_seq, s));
+    DF_CHECK(launch_gather_rows(ctx, feats, rows, s));
   }
-  const int s_fc = inject_splits(g, d, Fin, false);
+  const int R = g.max_inject_rows;
+  const int s_fc = inject_splits(g, d, Fin, false, ctx->num_sms);
   {
+    // u = W_fc f; the fused hidden state RMSNorm(u) * g_fc is folded into the
+    // K/V projection below
     ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
     EpiArgs e = epi_base(ctx, EPI_STORE, rows, d);
     e.m_valid = ctx->scal;
-    e.out = ctx->y;
-    DF_RUN(run_gemm(ctx, ctx->w_fc, d, Fin, ctx->fc_in, nullptr, rows, g.max_inject_rows, s_fc, ctx->scal, e, s));
+    norm_out(e, ctx->h_fused, ctx->h_lo, ctx->g_fc, ctx->ss_h, R);
+    DF_RUN(run_gemm(ctx, ctx->w_fc, d, Fin, ctx->fc_in, nullptr, rows, R, s_fc, ctx->scal, e, s));
   }
-  {
-    ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-    DF_CHECK(launch_fc_norm(ctx, rows, s));
-  }
-  const int s_kv = inject_splits(g, Nkv, d, true);
+  const int s_kv = inject_splits(g, Nkv, d, true, ctx->num_sms);
   {
     ProfScope p(ctx, DFLASH_PROF_INJECT, 1, s);
     EpiArgs e = epi_base(ctx, EPI_KV_INJECT, rows, Nkv);
+    norm_in(ctx, e, ctx->ss_h, R);
     e.m_valid = ctx->scal;
     e.pool_k = ctx->pool_k;
     e.pool_v = ctx->pool_v;
@@ -413,8 +462,7 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t
     e.page_table = ctx->page_table;
     e.max_pages = g.max_pages_per_seq;
     e.key_offset = ctx->key_offset;
-    DF_RUN(run_gemm(ctx, ctx->w_kv_inj, Nkv, d, ctx->h_fused, ctx->h_lo, rows, g.max_inject_rows, s_kv, ctx->scal,
-                    e, s));
+    DF_RUN(run_gemm(ctx, ctx->w_kv_inj, Nkv, d, ctx->h_fused, ctx->h_lo, rows, R, s_kv, ctx->scal, e, s));
   }
   return DFLASH_OK;
 }
@@ -428,20 +476,26 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
   const int M = B * kBlockK, Mmax = g.max_batch * kBlockK;
   const int d = g.hidden, F = g.ffn, qd = g.n_q_heads * g.head_dim, kvd = g.n_kv_heads * g.head_dim;
   const int Nqkv = qd + 2 * kvd, Ngu = gu_rows(F);
-  const int s_qkv = draft_splits(g, M, Nqkv, d);
-  const int s_o = draft_splits(g, M, d, qd);
-  const int s_gu = draft_splits(g, M, Ngu, d);
-  const int s_dn = draft_splits(g, M, d, F);
+  const int sms = ctx->num_sms;
+  // at most one QKV CTA per SM, so that the attention CTAs (launched early)
+  // find room beside them and stream the context while QKV runs
+  const int s_qkv = draft_splits(g, M, Nqkv, d, sms, sms);
+  const int s_o = draft_splits(g, M, d, qd, sms);
+  const int s_gu = draft_splits(g, M, Ngu, d, sms);
+  const int s_dn = draft_splits(g, M, d, F, sms);
   const int a_sp = attn_splits(ctx, B);
   for (int pass = 0; pass < S; ++pass) {
     {
       ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-      DF_CHECK(launch_embed_norm(ctx, M, pass == 1, s));
+      DF_CHECK(launch_embed(ctx, M, pass == 1, s));
     }
+    // every pre-norm runs folded: the producing epilogue writes g . x and the
+    // sums of squares of x (ss_x), the consuming projection scales its rows
     for (int l = 0; l < g.n_layers; ++l) {
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
         EpiArgs e = epi_base(ctx, EPI_QKV, M, Nqkv);
+        norm_in(ctx, e, ctx->ss_x, Mmax);
         e.q = ctx->q;
         e.pool_k = pool_layer(ctx->pool_k, ctx, l);
         e.pool_v = pool_layer(ctx->pool_v, ctx, l);
@@ -457,15 +511,13 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
         EpiArgs e = epi_base(ctx, EPI_RESIDUAL, M, d);
         e.out = ctx->x;
+        norm_out(e, ctx->a, ctx->a_lo, ctx->g_post[l], ctx->ss_x, Mmax);
         DF_RUN(run_gemm(ctx, ctx->w_o[l], d, qd, ctx->o, ctx->o_lo, M, Mmax, s_o, nullptr, e, s));
-      }
-      {
-        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-        DF_CHECK(launch_rmsnorm_rows(ctx, M, ctx->g_post[l], s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
         EpiArgs e = epi_base(ctx, EPI_SWIGLU, M, Ngu);
+        norm_in(ctx, e, ctx->ss_x, Mmax);
         e.act_hi = ctx->act;
         e.act_lo = ctx->act_lo;
         e.F = F;
@@ -475,13 +527,12 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
         EpiArgs e = epi_base(ctx, EPI_RESIDUAL, M, d);
         e.out = ctx->x;
+        norm_out(e, ctx->a, ctx->a_lo, l + 1 < g.n_layers ? ctx->g_in[l + 1] : ctx->g_final, ctx->ss_x, Mmax);
         DF_RUN(run_gemm(ctx, ctx->w_down[l], d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, e, s));
       }
-      {
-        ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-        DF_CHECK(launch_rmsnorm_rows(ctx, M, l + 1 < g.n_layers ? ctx->g_in[l + 1] : ctx->g_final, s));
-      }
     }
+    EpiArgs fin = epi_base(ctx, EPI_NONE, M, g.vocab);  // the final norm, folded into the LM head
+    norm_in(ctx, fin, ctx->ss_x, Mmax);
     const int32_t* skip = pass == 1 ? ctx->commit : nullptr;
     ProfScope plm(ctx, DFLASH_PROF_LMHEAD, g.dtype == DFLASH_BF16 ? 1 : 2, s);
     if (g.dtype == DFLASH_BF16) {
@@ -498,6 +549,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
       lm.logits = logits;
       lm.ld_logits = g.vocab;
       lm.skip_rows = skip;
+      lm.epi = fin;
       DF_CHECK(gemm_launch(ctx, lm, s));
     } else {
       GemmLaunch lm{};
@@ -511,7 +563,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
       lm.out = ctx->logits_ws;
       lm.ldo = g.vocab;
       DF_CHECK(gemm_launch(ctx, lm, s));
-      DF_CHECK(launch_logits_tiles(ctx, M, logits, skip, s));
+      DF_CHECK(launch_logits_tiles(ctx, M, logits, skip, fin, s));
     }
     plm.close();
     ProfScope pm(ctx, DFLASH_PROF_ROWWISE, S == 2 && pass == 0 ? 2 : 1, s);
@@ -544,13 +596,13 @@ dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* dra
   if (mode == 0) {
     if (target_tokens == nullptr) return DFLASH_ERR_INVALID_ARG;
     ProfScope p(ctx, DFLASH_PROF_ACCEPT, 1, s);
-    DF_CHECK(launch_accept_greedy(B, kBlockK, draft_tokens, target_tokens, accept_len, emitted, n_emit, s));
+    DF_CHECK(launch_accept_greedy(B, kBlockK, draft_tokens, target_tokens, accept_len, emitted, n_emit, ctx->pdl, s));
     return DFLASH_OK;
   }
   if (mode != 1 || target_logits == nullptr || !(temperature > 0.f)) return DFLASH_ERR_INVALID_ARG;
   ProfScope p(ctx, DFLASH_PROF_ACCEPT, 1, s);
   DF_CHECK(launch_accept_stochastic(B, kBlockK, ctx->cfg.vocab, draft_tokens, target_logits, draft_probs,
-                                    temperature, seed, round, accept_len, emitted, n_emit, s));
+                                    temperature, seed, round, accept_len, emitted, n_emit, ctx->pdl, s));
   return DFLASH_OK;
 }
 

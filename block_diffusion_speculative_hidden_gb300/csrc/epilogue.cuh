@@ -2,13 +2,24 @@
 //
 // A projection's output tile (16..256 activation rows x 128 weight rows,
 // fp32) is finished here, straight from shared memory, by the CTA that owns
-// the complete sum (the only CTA, or the last split-K CTA of the tile):
+// the complete sum (the only CTA, or one CTA per row slice of a split-K
+// cluster):
 //
-//   EPI_STORE     out[m][n] = v                     (feature-fusion FC)
-//   EPI_RESIDUAL  x[m][n] += v                      (O-proj, down-proj)
+//   EPI_STORE     z = v                             (feature-fusion FC)
+//   EPI_RESIDUAL  z = x + v, x = z                  (O-proj, down-proj)
 //   EPI_SWIGLU    act[m][f] = silu(g) * u           (gate/up interleaved per 64 features)
 //   EPI_QKV       q (RoPE) ; block k (RoPE) and v into the sequence's block page
 //   EPI_KV_INJECT K (offset + RoPE) and V of every layer into the row's page slot
+//
+// RMSNorm is folded into the projections instead of running as a kernel of
+// its own.  RMSNorm(z) * g feeds the next projection W; since
+// W (RMSNorm(z) * g) = r * W (g . z) with r = 1 / sqrt(mean(z^2) + eps) a
+// per-row scalar, the producer of z (STORE or RESIDUAL) writes g . z as the
+// next GEMM input together with per-(128-column tile, row) partial sums of
+// z^2, and the consumer multiplies each output row by r, computed from those
+// partials in a fixed order.  The result is the same function; only the
+// point where the rounding to the GEMM input happens moves (g . z instead of
+// r g . z, both carried as an exact two-term bf16 split).
 //
 // KT is the element type of q and of the KV pool: fp16 for the bf16
 // workloads, fp32 for the fp32 ones.  The tile layout in shared memory is
@@ -30,7 +41,7 @@ struct EpiArgs {
   int kind;
   int M, N;               // rows and columns of the projection
   const int* m_valid;     // nullable device row count (rows at or past it are left alone)
-  float* out;             // STORE: [M][N]; RESIDUAL: x [M][N]
+  float* out;             // STORE: nullable fp32 copy of z [M][N]; RESIDUAL: x [M][N]
   void* act_hi;           // SWIGLU: activation (ActOut of the config type) [M][F]
   void* act_lo;
   int F;
@@ -49,22 +60,32 @@ struct EpiArgs {
   const float* rope_sin;
   const float* key_offset;  // KV_INJECT: optional [L][Hkv][dh]
   int Hq, Hkv, dh;
+  // folded RMSNorm, consumer side: nullable partial sums of squares of the
+  // normalised rows, ss_in[t * ss_ld + m] for t < ss_tiles; row m of the
+  // output is scaled by 1 / sqrt(sum_t ss_in / norm_dim + eps)
+  const float* ss_in;
+  int ss_tiles;
+  float norm_dim_inv;
+  float eps;
+  int ss_ld;              // row stride of ss_in / ss_out
+  // folded RMSNorm, producer side (STORE, RESIDUAL): nullable next input
+  // (ActOut of the config type) nx[m][n] = nx_gain[n] * z[m][n], and
+  // ss_out[(n0 / 128) * ss_ld + m] = sum over the tile's columns of z^2
+  void* nx_hi;
+  void* nx_lo;
+  const void* nx_gain;
+  float* ss_out;
 };
 
 __device__ __forceinline__ long long pool_index(int page, int head, int slot, int i, int Hkv, int dh) {
   return ((static_cast<long long>(page) * Hkv + head) * kPage + slot) * dh + i;
 }
 
-// RoPE (rotate-half) of element i of the head whose element 0 sits at tile
-// column t - i, at position pos; add_lo/add_hi are added to the pair first.
-__device__ __forceinline__ float rope_col(const float* row, int t, int i, int dh, int pos, const float* rc,
-                                          const float* rs, float add_lo = 0.f, float add_hi = 0.f) {
-  const int half = dh / 2;
-  const int base = t - i;
-  const int j = i < half ? i : i - half;
-  const float x1 = row[base + j] + add_lo, x2 = row[base + j + half] + add_hi;
-  const float cs = rc[pos * half + j], sn = rs[pos * half + j];
-  return i < half ? x1 * cs - x2 * sn : x2 * cs + x1 * sn;
+// 1 / RMS of row m from the partial sums of squares (fixed summation order).
+__device__ __forceinline__ float norm_row_scale(const EpiArgs& e, int m) {
+  float s = 0.f;
+  for (int t = 0; t < e.ss_tiles; ++t) s += e.ss_in[static_cast<long long>(t) * e.ss_ld + m];
+  return rsqrtf(s * e.norm_dim_inv + e.eps);
 }
 
 template <typename KT>
@@ -74,82 +95,167 @@ __device__ __forceinline__ float kv_store<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __half kv_store<__half>(float v) { return __float2half_rn(v); }
 
-// Finishes one tile.  All threads of the block call it; thread t handles
-// output column n0 + t (blockDim.x == 128).
+// Per-row facts an epilogue needs from global memory, gathered ahead of it
+// (by otherwise idle warps while the main loop runs): x = position, y = page
+// of the row's K/V slot, z = slot in the page (QKV: the block page).
+__device__ __forceinline__ int4 epi_row_info(const EpiArgs& e, int m) {
+  if (e.kind == EPI_QKV) {
+    const int b = m / kBlockK, slot = m % kBlockK;
+    return make_int4(e.seq_len[b] + slot, e.block_page0 + b, slot, 0);
+  }
+  if (e.kind == EPI_KV_INJECT) {
+    const int b = e.row_seq[m], pos = e.row_pos[m];
+    return make_int4(pos, e.page_table[b * e.max_pages + pos / kPage], pos % kPage, 0);
+  }
+  return make_int4(0, 0, 0, 0);
+}
+
+constexpr int kEpiBatch = 8;  // rows finished together (their loads in flight at once)
+
+// Finishes one tile.  All threads of the block call it (blockDim.x == 128);
+// thread t handles output column n0 + t.  `rs` (nullable) holds the row
+// scales of rows m0 .. m0 + rows - 1 and `ri` (nullable) their epi_row_info;
+// `scratch` holds 4 * rows floats and is used when e.ss_out is set.  Rows
+// are processed kEpiBatch at a time with every global load of a batch
+// issued before any of its results is used.
 template <typename T, typename KT>
-__device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int rows, int n0) {
+__device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int rows, int n0, const float* rs,
+                               const int4* ri, float* scratch) {
   const int t = threadIdx.x;
   const int n = n0 + t;
   if (e.m_valid != nullptr) rows = min(rows, *e.m_valid - m0);
+  rows = min(rows, e.M - m0);
+  if (rows <= 0) return;
   KT* q = static_cast<KT*>(e.q);
   KT* pk = static_cast<KT*>(e.pool_k);
   KT* pv = static_cast<KT*>(e.pool_v);
   switch (e.kind) {
     case EPI_STORE:
-      if (n < e.N)
-        for (int j = 0; j < rows && m0 + j < e.M; ++j)
-          e.out[static_cast<long long>(m0 + j) * e.N + n] = tile[j * 128 + t];
+    case EPI_RESIDUAL: {
+      const bool nv = n < e.N;
+      const ActOut<T> nx{static_cast<T*>(e.nx_hi), static_cast<T*>(e.nx_lo)};
+      const float gn = (e.nx_hi != nullptr && nv) ? to_f32(static_cast<const T*>(e.nx_gain)[n]) : 0.f;
+      const int warp = t >> 5, lane = t & 31;
+      for (int j0 = 0; j0 < rows; j0 += kEpiBatch) {
+        float z[kEpiBatch];
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          const int j = j0 + u;
+          z[u] = 0.f;
+          if (nv && j < rows) {
+            z[u] = tile[j * 128 + t] * (rs != nullptr ? rs[j] : 1.f);
+            if (e.kind == EPI_RESIDUAL) z[u] += e.out[static_cast<long long>(m0 + j) * e.N + n];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          const int j = j0 + u;
+          if (nv && j < rows) {
+            const long long o = static_cast<long long>(m0 + j) * e.N + n;
+            if (e.out != nullptr) e.out[o] = z[u];
+            if (e.nx_hi != nullptr) nx.put(o, gn * z[u]);
+          }
+        }
+        if (e.ss_out != nullptr) {
+#pragma unroll
+          for (int u = 0; u < kEpiBatch; ++u) z[u] = warp_sum(z[u] * z[u]);
+          if (lane == 0)
+#pragma unroll
+            for (int u = 0; u < kEpiBatch; ++u)
+              if (j0 + u < rows) scratch[(j0 + u) * 4 + warp] = z[u];
+        }
+      }
+      if (e.ss_out != nullptr) {
+        __syncthreads();
+        for (int j = t; j < rows; j += 128)
+          e.ss_out[static_cast<long long>(n0 >> 7) * e.ss_ld + m0 + j] =
+              (scratch[j * 4 + 0] + scratch[j * 4 + 1]) + (scratch[j * 4 + 2] + scratch[j * 4 + 3]);
+      }
       break;
-    case EPI_RESIDUAL:
-      if (n < e.N)
-        for (int j = 0; j < rows && m0 + j < e.M; ++j)
-          e.out[static_cast<long long>(m0 + j) * e.N + n] += tile[j * 128 + t];
-      break;
+    }
     case EPI_SWIGLU: {
       const int f = (n0 >> 7) * 64 + t;  // tile = 64 gate rows then the 64 matching up rows
       if (t < 64 && f < e.F) {
         ActOut<T> a{static_cast<T*>(e.act_hi), static_cast<T*>(e.act_lo)};
-        for (int j = 0; j < rows && m0 + j < e.M; ++j) {
-          const float g = tile[j * 128 + t], u = tile[j * 128 + t + 64];
-          a.put(static_cast<long long>(m0 + j) * e.F + f, g / (1.f + expf(-g)) * u);
+        for (int j0 = 0; j0 < rows; j0 += kEpiBatch) {
+#pragma unroll
+          for (int u = 0; u < kEpiBatch; ++u) {
+            const int j = j0 + u;
+            if (j < rows) {
+              const float sc = rs != nullptr ? rs[j] : 1.f;
+              const float g = tile[j * 128 + t] * sc, up = tile[j * 128 + t + 64] * sc;
+              a.put(static_cast<long long>(m0 + j) * e.F + f, g / (1.f + expf(-g)) * up);
+            }
+          }
         }
       }
       break;
     }
-    case EPI_QKV: {
-      if (n >= e.N) break;
-      const int qd = e.Hq * e.dh, kvd = e.Hkv * e.dh;
-      const int i = n % e.dh;
-      for (int j = 0; j < rows && m0 + j < e.M; ++j) {
-        const int m = m0 + j, b = m / kBlockK, slot = m % kBlockK;
-        const float* row = tile + j * 128;
-        if (n < qd) {
-          const int pos = e.seq_len[b] + slot;
-          q[static_cast<long long>(m) * qd + n] = kv_store<KT>(rope_col(row, t, i, e.dh, pos, e.rope_cos, e.rope_sin));
-        } else if (n < qd + kvd) {
-          const int pos = e.seq_len[b] + slot, g = (n - qd) / e.dh;
-          pk[pool_index(e.block_page0 + b, g, slot, i, e.Hkv, e.dh)] =
-              kv_store<KT>(rope_col(row, t, i, e.dh, pos, e.rope_cos, e.rope_sin));
-        } else {
-          const int g = (n - qd - kvd) / e.dh;
-          pv[pool_index(e.block_page0 + b, g, slot, i, e.Hkv, e.dh)] = kv_store<KT>(row[t]);
-        }
-      }
-      break;
-    }
+    case EPI_QKV:
     case EPI_KV_INJECT: {
       if (n >= e.N) break;
-      const int kvd = e.Hkv * e.dh;
-      const int l = n / (2 * kvd), w = n % (2 * kvd);
-      const bool is_k = w < kvd;
-      const int g = (is_k ? w : w - kvd) / e.dh, i = w % e.dh, half = e.dh / 2;
+      const int half = e.dh / 2;
+      int kind;    // 0: q, 1: k, 2: v
+      int head;    // q head (kind 0) or kv head
+      int i;       // element within the head
+      int l = 0;   // layer (KV_INJECT)
       float off_lo = 0.f, off_hi = 0.f;
-      if (is_k && e.key_offset != nullptr) {
-        const float* ko = e.key_offset + (static_cast<long long>(l) * e.Hkv + g) * e.dh;
-        const int jj = i < half ? i : i - half;
-        off_lo = ko[jj];
-        off_hi = ko[jj + half];
+      if (e.kind == EPI_QKV) {
+        const int qd = e.Hq * e.dh, kvd = e.Hkv * e.dh;
+        kind = n < qd ? 0 : n < qd + kvd ? 1 : 2;
+        const int w = kind == 0 ? n : kind == 1 ? n - qd : n - qd - kvd;
+        head = w / e.dh;
+        i = w % e.dh;
+      } else {
+        const int kvd = e.Hkv * e.dh;
+        l = n / (2 * kvd);
+        const int w = n % (2 * kvd);
+        kind = w < kvd ? 1 : 2;
+        head = (kind == 1 ? w : w - kvd) / e.dh;
+        i = w % e.dh;
+        if (kind == 1 && e.key_offset != nullptr) {
+          const float* ko = e.key_offset + (static_cast<long long>(l) * e.Hkv + head) * e.dh;
+          const int jj = i < half ? i : i - half;
+          off_lo = ko[jj];
+          off_hi = ko[jj + half];
+        }
       }
-      for (int j = 0; j < rows && m0 + j < e.M; ++j) {
-        const int r = m0 + j;
-        const int b = e.row_seq[r], pos = e.row_pos[r];
-        const int page = e.page_table[b * e.max_pages + pos / kPage], slot = pos % kPage;
-        const float* row = tile + j * 128;
-        const long long idx = l * e.layer_stride + pool_index(page, g, slot, i, e.Hkv, e.dh);
-        if (is_k)
-          pk[idx] = kv_store<KT>(rope_col(row, t, i, e.dh, pos, e.rope_cos, e.rope_sin, off_lo, off_hi));
-        else
-          pv[idx] = kv_store<KT>(row[t]);
+      const int jr = i < half ? i : i - half;  // RoPE frequency index
+      const int base = t - i;                   // tile column of the head's element 0
+      const long long lbase = static_cast<long long>(l) * e.layer_stride;
+      for (int j0 = 0; j0 < rows; j0 += kEpiBatch) {
+        int4 info[kEpiBatch];
+        float cs[kEpiBatch], sn[kEpiBatch];
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          const int j = min(j0 + u, rows - 1);
+          info[u] = ri != nullptr ? ri[j] : epi_row_info(e, m0 + j);
+          cs[u] = sn[u] = 0.f;
+          if (kind != 2) {
+            cs[u] = e.rope_cos[info[u].x * half + jr];
+            sn[u] = e.rope_sin[info[u].x * half + jr];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          const int j = j0 + u;
+          if (j >= rows) continue;
+          const float* row = tile + j * 128;
+          const float sc = rs != nullptr ? rs[j] : 1.f;
+          float v;
+          if (kind == 2) {
+            v = row[t] * sc;
+          } else {
+            const float x1 = row[base + jr] * sc + off_lo, x2 = row[base + jr + half] * sc + off_hi;
+            v = i < half ? x1 * cs[u] - x2 * sn[u] : x2 * cs[u] + x1 * sn[u];
+          }
+          if (kind == 0) {
+            q[static_cast<long long>(m0 + j) * (e.Hq * e.dh) + n] = kv_store<KT>(v);
+          } else {
+            const long long idx = lbase + pool_index(info[u].y, head, info[u].z, i, e.Hkv, e.dh);
+            (kind == 1 ? pk : pv)[idx] = kv_store<KT>(v);
+          }
+        }
       }
       break;
     }

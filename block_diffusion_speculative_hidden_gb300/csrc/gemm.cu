@@ -28,6 +28,10 @@ namespace dflash {
 
 // --------------------------------------------------------------- tcgen05 kernel
 
+// Row stride (floats) of the LM head's logits tile in shared memory: 128
+// columns + 8 keeps the per-row segment reads free of bank conflicts.
+constexpr int kLmLd = 136;
+
 template <int BN, bool SPLIT>
 struct TcCfg {
   static constexpr int W_BYTES = kTileN * kTileK * 2;  // 16 KB
@@ -38,10 +42,12 @@ struct TcCfg {
   static constexpr int STAGES = (BUDGET / STAGE_BYTES) < 8 ? (BUDGET / STAGE_BYTES) : 8;
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
   static constexpr int SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/ +
-                              3 * 4 * BN * 4 /*LM-head reduction*/;
+                              4 * BN * 4 /*epilogue scratch*/ + BN * 4 /*row scales*/ + BN * 16 /*row info*/;
   static_assert(STAGES >= 2, "pipeline too shallow");
-  // the own tile plus the reduced slice (at most half the rows, splits >= 2) fit in the stage ring
+  // the own tile plus the reduced slice (at most half the rows, splits >= 2) fit in the stage ring, and
+  // so does the LM head's padded tile
   static_assert(BN * 128 * 4 * 3 / 2 <= STAGES * STAGE_BYTES, "epilogue tiles must fit in the stage ring");
+  static_assert(BN * kLmLd * 4 <= STAGES * STAGE_BYTES, "LM-head tile must fit in the stage ring");
 };
 
 struct TcParams {
@@ -62,7 +68,8 @@ struct TcParams {
 template <int BN, bool LMHEAD, bool SPLIT>
 __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtensorMap tmW,
                                                  const __grid_constant__ CUtensorMap tmX,
-                                                 const __grid_constant__ CUtensorMap tmXlo, const TcParams p) {
+                                                 const __grid_constant__ CUtensorMap tmXlo,
+                                                 const __grid_constant__ TcParams p) {
   using C = TcCfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -74,11 +81,18 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
   uint64_t* accb = empty + C::STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   int* s_prog = reinterpret_cast<int*>(tmem_slot + 1);  // [0] stages issued, [1] stages consumed
-  float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+  float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + 256);  // [BN][4] epilogue scratch
+  float* s_rs = red + 4 * BN;                             // folded-RMSNorm row scales of rows m0 .. m0 + BN - 1
+  int4* s_ri = reinterpret_cast<int4*>(s_rs + BN);        // per-row epilogue facts (epi_row_info; LM head: skip)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * BN, split = blockIdx.z;
-  if (p.m_valid != nullptr && m0 >= __ldg(p.m_valid)) return;  // uniform: nothing allocated yet
+  // m_valid is written two kernels upstream (page allocation), never by the
+  // predecessor, so it may be read before pdl_wait
+  if (p.m_valid != nullptr && m0 >= __ldg(p.m_valid)) {  // uniform: nothing allocated yet
+    pdl_wait();
+    return;
+  }
   const int kb0 = split * p.kb_per_split;
   const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
   const int nkb = kb1 - kb0;
@@ -109,7 +123,22 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      for (int it = 0; it < nkb; ++it) {
+      // the weights do not depend on the predecessor: fill the ring with them
+      // while it finishes, then add the activations once it has completed
+      const int pre = min(nkb, C::STAGES);
+      for (int it = 0; it < pre; ++it) {
+        mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
+        tma_load_2d_hint(sW + it * C::W_BYTES, &tmW, &full[it], (kb0 + it) * kTileK, n0, pol);
+      }
+      pdl_wait();
+      pdl_trigger();
+      for (int it = 0; it < pre; ++it) {
+        const int kx = (kb0 + it) * kTileK;
+        tma_load_2d(sX + it * XS, &tmX, &full[it], kx, m0);
+        if (SPLIT) tma_load_2d(sX + it * XS + C::X_BYTES, &tmXlo, &full[it], kx, m0);
+      }
+      s_prog[0] = pre;
+      for (int it = pre; it < nkb; ++it) {
         const int s = it % C::STAGES;
         const uint32_t ph = (it / C::STAGES) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, p.status)) break;
@@ -144,7 +173,22 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
       tc_commit(accb);
     }
     __syncwarp();
+  } else {
+    // idle during the main loop: gather what the epilogue reads from global
+    // memory (folded-RMSNorm row scales, row positions and pages)
+    pdl_wait();
+    const int mv = p.m_valid != nullptr ? min(p.M, *p.m_valid) : p.M;
+    for (int j = threadIdx.x - 64; j < BN; j += 64) {
+      const int m = m0 + j;
+      const bool ok = m < mv;
+      if (p.epi.ss_in != nullptr) s_rs[j] = ok ? norm_row_scale(p.epi, m) : 0.f;
+      if (LMHEAD)
+        s_ri[j] = make_int4(0, 0, 0, ok && (p.skip_rows == nullptr || p.skip_rows[m] == 0) ? 1 : 0);
+      else
+        s_ri[j] = ok ? epi_row_info(p.epi, m) : make_int4(0, 0, 0, 0);
+    }
   }
+  pdl_wait();  // everything below may read the predecessor's output
 
   // ---- epilogue: TMEM lane (32*warp + lane) holds weight row n, columns = activation rows
   mbar_wait(accb, 0, p.status);
@@ -178,8 +222,9 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
         if (nv) o[static_cast<long long>(m0 + j) * p.ldo + n] = tile[j * 128 + t];
     }
     if (p.epi.kind != EPI_NONE) {
+      const float* rs = p.epi.ss_in != nullptr ? s_rs : nullptr;
       if (p.splits == 1) {
-        apply_epilogue<__nv_bfloat16, __half>(p.epi, tile, m0, BN, n0);
+        apply_epilogue<__nv_bfloat16, __half>(p.epi, tile, m0, BN, n0, rs, s_ri, red);
       } else {
         // split-K reduction inside the cluster of this tile's `splits` CTAs:
         // each CTA sums a contiguous slice of the rows over every CTA's tile
@@ -204,62 +249,71 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
           *reinterpret_cast<float4*>(sub + (j - r_begin) * 128 + c4) = acc;
         }
         cluster_sync_all();  // no CTA's tile is read after this point
-        if (r_end > r_begin) apply_epilogue<__nv_bfloat16, __half>(p.epi, sub, m0 + r_begin, r_end - r_begin, n0);
+        if (r_end > r_begin)
+          apply_epilogue<__nv_bfloat16, __half>(p.epi, sub, m0 + r_begin, r_end - r_begin, n0,
+                                                rs != nullptr ? rs + r_begin : nullptr, s_ri + r_begin, red);
       }
     }
   } else {
+    // LM head: the scaled logits go to a padded [BN][kLmLd] tile (and, when
+    // asked for, to global memory); then 8 threads per row reduce it to the
+    // tile's (max, lowest argmax, sum of exp(z - max)), 16 rows at a time.
+    float* tile = reinterpret_cast<float*>(smem);
+    __syncthreads();
 #pragma unroll 1
     for (int c = 0; c < BN; c += 16) {
       float v[16];
       tc_ld_32x32b_x16(tbase + c, v);
-#pragma unroll 1
+#pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = m0 + c + j;
-        const float val = nv ? v[j] : -INFINITY;
-        if (p.logits != nullptr && nv && m < p.M && (p.skip_rows == nullptr || p.skip_rows[m] == 0))
-          p.logits[m * p.ld_logits + n] = val;
-        float mx = val;
-        int ix = n;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float om = __shfl_xor_sync(0xffffffffu, mx, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
-          if (om > mx || (om == mx && oi < ix)) {
-            mx = om;
-            ix = oi;
-          }
-        }
-        const float e = nv ? expf(val - mx) : 0.f;
-        const float se = warp_sum(e);
-        if (lane == 0) {
-          red[(0 * 4 + warp) * BN + c + j] = mx;
-          red[(1 * 4 + warp) * BN + c + j] = se;
-          red[(2 * 4 + warp) * BN + c + j] = __int_as_float(ix);
-        }
+        const float val = nv ? (p.epi.ss_in != nullptr ? v[j] * s_rs[c + j] : v[j]) : -INFINITY;
+        tile[(c + j) * kLmLd + warp * 32 + lane] = val;
+        if (p.logits != nullptr && nv && s_ri[c + j].w != 0) p.logits[m * p.ld_logits + n] = val;
       }
     }
+    tc_fence_before();
     __syncthreads();
-    for (int j = threadIdx.x; j < BN; j += blockDim.x) {
-      const int m = m0 + j;
-      if (m >= p.M) continue;
-      float mx = red[0 * BN + j];
-      int ix = __float_as_int(red[2 * 4 * BN + j]);
-      for (int w = 1; w < 4; ++w) {  // warps cover increasing columns: strict > keeps the lowest id
-        const float wm = red[(0 * 4 + w) * BN + j];
-        if (wm > mx) {
-          mx = wm;
-          ix = __float_as_int(red[(2 * 4 + w) * BN + j]);
+    const int seg = threadIdx.x & 7;
+#pragma unroll 1
+    for (int rb = 0; rb < BN; rb += 16) {
+      const int j = rb + (threadIdx.x >> 3);
+      const float* row = tile + j * kLmLd;
+      float z[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) z[k] = row[seg + 8 * k];
+      // columns seg, seg + 8, ... are scanned in increasing order: strict >
+      // keeps the lowest column among equal maxima
+      float mx = z[0];
+      int ix = seg;
+#pragma unroll
+      for (int k = 1; k < 16; ++k)
+        if (z[k] > mx) {
+          mx = z[k];
+          ix = seg + 8 * k;
+        }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+        if (om > mx || (om == mx && oi < ix)) {
+          mx = om;
+          ix = oi;
         }
       }
       float se = 0.f;
-      for (int w = 0; w < 4; ++w) {
-        const float wm = red[(0 * 4 + w) * BN + j];
-        if (wm > -INFINITY) se += red[(1 * 4 + w) * BN + j] * expf(wm - mx);
+      if (mx > -INFINITY)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) se += expf(z[k] - mx);
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+      const int m = m0 + j;
+      if (seg == 0 && m < p.M) {
+        const long long o = static_cast<long long>(m) * p.lm.n_tiles + blockIdx.x;
+        p.lm.mx[o] = mx;
+        p.lm.se[o] = se;
+        p.lm.idx[o] = n0 + ix;
       }
-      const long long o = static_cast<long long>(m) * p.lm.n_tiles + blockIdx.x;
-      p.lm.mx[o] = mx;
-      p.lm.se[o] = se;
-      p.lm.idx[o] = ix;
     }
     tc_fence_before();
   }
@@ -274,13 +328,15 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
 // (128-column, 16-row) tile runs the same epilogue as the tensor-core path.
 __global__ void __launch_bounds__(128) k_epilogue_apply_f32(const float* __restrict__ y, int M, int N, EpiArgs e) {
   __shared__ float tile[16 * 128];
+  __shared__ float rs[16], scratch[4 * 16];
   const int n0 = blockIdx.x * 128, m0 = blockIdx.y * 16, t = threadIdx.x;
   for (int j = 0; j < 16; ++j) {
     const int m = m0 + j, n = n0 + t;
     tile[j * 128 + t] = (m < M && n < N) ? y[static_cast<long long>(m) * N + n] : 0.f;
   }
+  if (e.ss_in != nullptr && t < 16) rs[t] = m0 + t < M ? norm_row_scale(e, m0 + t) : 0.f;
   __syncthreads();
-  apply_epilogue<float, float>(e, tile, m0, 16, n0);
+  apply_epilogue<float, float>(e, tile, m0, 16, n0, e.ss_in != nullptr ? rs : nullptr, nullptr, scratch);
 }
 
 // --------------------------------------------------------------- fp32 SIMT kernel
@@ -399,24 +455,10 @@ static cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorM
   p.skip_rows = g.skip_rows;
   // splits come from gemm_splits: every split owns at least one k-block
   dim3 grid((g.N + kTileN - 1) / kTileN, (g.M + BN - 1) / BN, g.splits);
-  if (LM || g.epi.kind == EPI_NONE || g.splits == 1) {
-    k_gemm_tc<BN, LM, SPLIT><<<grid, 128, C::SMEM, s>>>(tw, tx, txlo, p);
-    return cudaGetLastError();
-  }
   // the splits of one output tile form a thread-block cluster (reduced over DSMEM)
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = grid;
-  lc.blockDim = dim3(128);
-  lc.dynamicSmemBytes = C::SMEM;
-  lc.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = g.splits;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, k_gemm_tc<BN, LM, SPLIT>, tw, tx, txlo, p);
+  const bool clustered = !(LM || g.epi.kind == EPI_NONE || g.splits == 1);
+  return launch_k(k_gemm_tc<BN, LM, SPLIT>, grid, dim3(128), C::SMEM, s, dim3(1, 1, clustered ? g.splits : 1),
+                  c->pdl, tw, tx, txlo, p);
 }
 
 template <bool SPLIT>
@@ -441,58 +483,55 @@ static cudaError_t launch_tc_bn(dflash_ctx* c, const GemmLaunch& g, int bn, cons
   }
 }
 
-// How many clusters of `cluster` CTAs of the projection kernel (tile width
-// bn, hi+lo operands or not) can be resident at once on this device.  GPCs
-// have uneven SM counts, so this is not simply SMs x CTAs-per-SM / cluster.
+// How many CTAs of the projection kernel (tile width bn, hi+lo operands or
+// not) one SM holds at once.
+// Shared memory is the only limit that binds (128 threads, few registers,
+// at most 512 TMEM columns per SM across resident CTAs).
 template <int BN, bool SPLIT>
-static int max_clusters_t(int cluster) {
+static int blocks_per_sm_t() {
   using C = TcCfg<BN, SPLIT>;
-  if (cudaFuncSetAttribute(k_gemm_tc<BN, false, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-      cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(1, 1, cluster);
-  lc.blockDim = dim3(128);
-  lc.dynamicSmemBytes = C::SMEM;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = cluster;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<BN, false, SPLIT>, &lc) != cudaSuccess) return 0;
-  return n;
+  int dev = 0, per_sm = 0, reserved = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  const int by_smem = per_sm / (C::SMEM + reserved);
+  const int by_tmem = 512 / C::TMEM_COLS;
+  return std::max(1, std::min(by_smem, by_tmem));
 }
 
-int gemm_max_clusters(int bn, bool split, int cluster) {
-  static int cache[2][5][9] = {};  // [split][log2(bn/16)][cluster]
+int gemm_blocks_per_sm(int bn, bool split) {
+  static int cache[2][5] = {};  // [split][log2(bn/16)]
   int bi = 0;
   while ((16 << bi) < bn && bi < 4) ++bi;
-  if (cluster < 1 || cluster > 8) return 0;
-  int& c = cache[split ? 1 : 0][bi][cluster];
+  int& c = cache[split ? 1 : 0][bi];
   if (c == 0) {
     switch (bi) {
-      case 0: c = split ? max_clusters_t<16, true>(cluster) : max_clusters_t<16, false>(cluster); break;
-      case 1: c = split ? max_clusters_t<32, true>(cluster) : max_clusters_t<32, false>(cluster); break;
-      case 2: c = split ? max_clusters_t<64, true>(cluster) : max_clusters_t<64, false>(cluster); break;
-      case 3: c = split ? max_clusters_t<128, true>(cluster) : max_clusters_t<128, false>(cluster); break;
-      default: c = split ? 0 : max_clusters_t<256, false>(cluster); break;
+      case 0: c = split ? blocks_per_sm_t<16, true>() : blocks_per_sm_t<16, false>(); break;
+      case 1: c = split ? blocks_per_sm_t<32, true>() : blocks_per_sm_t<32, false>(); break;
+      case 2: c = split ? blocks_per_sm_t<64, true>() : blocks_per_sm_t<64, false>(); break;
+      case 3: c = split ? blocks_per_sm_t<128, true>() : blocks_per_sm_t<128, false>(); break;
+      default: c = split ? 1 : blocks_per_sm_t<256, false>(); break;
     }
-    if (c <= 0) c = -1;
   }
   return c;
 }
 
-// Split-K count for `n_tiles` output tiles of width bn: the largest split
-// count S <= 8 (a portable cluster) such that all n_tiles clusters of S CTAs
-// are resident at once, with at least 4 k-blocks per split; normalised so that
-// every split owns at least one k-block.
-int gemm_splits(int n_tiles, int n_kb, int bn, bool split) {
-  int s = std::min(8, std::max(1, n_kb / 4));
-  for (; s > 1; --s)
-    if (n_tiles <= gemm_max_clusters(bn, split, s)) break;
+// Split-K count for `n_tiles` output tiles of width bn.  A CTA streams its
+// weights at a fraction of the HBM bandwidth an SM can draw, so the grid
+// must keep every SM streaming: aim for about 1.25 CTAs per SM (all
+// resident at once, at most max_ctas when positive), with at most 8 splits
+// (a portable cluster) and at least 4 k-blocks per split; normalised so that
+// every split owns a k-block.
+int gemm_splits(int n_tiles, int n_kb, int bn, bool split, int num_sms, int max_ctas) {
+  int cap = gemm_blocks_per_sm(bn, split) * num_sms;
+  if (max_ctas > 0) cap = std::min(cap, max_ctas);
+  const int want = std::min(cap, (5 * num_sms + 3) / 4);
+  int s = (want + n_tiles - 1) / n_tiles;
+  while (s > 1 && n_tiles * s > cap) --s;
+  s = std::max(1, std::min({s, 8, n_kb / 4}));
   const int per = (n_kb + s - 1) / s;
   return (n_kb + per - 1) / per;
 }

@@ -81,14 +81,21 @@ struct dflash_ctx {
   float *attn_o, *attn_ml;
   int attn_max_splits;
   bool attn_maps_ready = false;
-  int attn_tc_max_splits = 0;  // 8 or 16, queried on first use
   CUtensorMap attn_map_k, attn_map_v;  // 4-D maps over the fp16 pool
+  CUtensorMap attn_map_q;              // 2-D map over the fp16 block queries
+  int attn_fit[17] = {};               // resident clusters per split count (0: not queried, -1: none)
   dflash::LmPartials lm;
   float* logits_ws;  // fp32 mode: full logits [M][V]
   int32_t* tok1;
   float* conf1;
   int32_t* commit;
   std::vector<dflash::TmapEntry> tmaps;
+  // launch the inject / draft / accept chain with programmatic dependent
+  // launch (each kernel may start while its predecessor finishes)
+  bool pdl = false;
+  // folded RMSNorm: partial sums of squares, [ceil(hidden/128)][rows]
+  float* ss_x;   // draft rows (row stride max_batch * 16)
+  float* ss_h;   // inject rows (row stride max_inject_rows)
   // launch timing (dflash_profile_enable)
   bool prof_on = false;
   struct ProfRec {
@@ -101,12 +108,50 @@ struct dflash_ctx {
 
 namespace dflash {
 
+// Every kernel of the library runs with the largest shared-memory carveout:
+// CTAs of different kernels share an SM only under the same carveout, and
+// the chain relies on a kernel's CTAs starting beside its predecessor's.
+// Returns false if the attribute could not be set.
+bool prefer_max_smem(const void* kernel);
+
+// Launches kernel k on stream s, as a grid of thread-block clusters when
+// cluster has more than one CTA, and with programmatic stream serialisation
+// (the kernel may start before its predecessor completes; it must follow
+// the pdl_wait / pdl_trigger rule of common.cuh) when pdl is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, dim3 cluster,
+                     bool pdl, Args&&... args) {
+  if (!prefer_max_smem(reinterpret_cast<const void*>(k))) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  if (cluster.x * cluster.y * cluster.z > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster.x;
+    at[n].val.clusterDim.y = cluster.y;
+    at[n].val.clusterDim.z = cluster.z;
+    ++n;
+  }
+  if (pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  lc.attrs = at;
+  lc.numAttrs = n;
+  return cudaLaunchKernelEx(&lc, k, static_cast<Args&&>(args)...);
+}
+
 // gemm.cu
 cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
 int gemm_kb(int K);
 int gemm_bn(int M, bool split);
-int gemm_max_clusters(int bn, bool split, int cluster);
-int gemm_splits(int n_tiles, int n_kb, int bn, bool split);
+int gemm_blocks_per_sm(int bn, bool split);
+int gemm_splits(int n_tiles, int n_kb, int bn, bool split, int num_sms, int max_ctas = 0);
 cudaError_t gemm_launch_uncached(int* status, const GemmLaunch& g, cudaStream_t s);
 
 }  // namespace dflash

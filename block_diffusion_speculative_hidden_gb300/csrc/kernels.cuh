@@ -17,12 +17,10 @@ cudaError_t launch_alloc(dflash_ctx* c, const int32_t* n_rows, int first_seq, in
 cudaError_t launch_rope_table(dflash_ctx* c, cudaStream_t s);
 
 // pointwise.cu (T = the config element type, chosen by c->cfg.dtype)
-cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, int max_rows, int first_seq,
-                               cudaStream_t s);
-cudaError_t launch_fc_norm(dflash_ctx* c, int rows, cudaStream_t s);
-cudaError_t launch_embed_norm(dflash_ctx* c, int M, bool second_pass, cudaStream_t s);
-cudaError_t launch_rmsnorm_rows(dflash_ctx* c, int M, const void* gain, cudaStream_t s);
-cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, cudaStream_t s);
+cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, cudaStream_t s);
+cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, cudaStream_t s);
+cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, const EpiArgs& norm,
+                                cudaStream_t s);
 cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,
                             cudaStream_t s);
 cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s);
@@ -30,15 +28,15 @@ cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s);
 // attention.cu
 int attn_splits(dflash_ctx* c, int B);
 cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
-// attention_tc.cu (fp16 pool)
-cudaError_t launch_attention_tc(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
-int attention_tc_max_splits(dflash_ctx* c);
+// attention_mma.cu (fp16 pool, tcgen05)
+cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
+int attention_mma_splits(dflash_ctx* c, int B);
 
 // accept.cu
 cudaError_t launch_accept_greedy(int B, int K, const int32_t* d, const int32_t* y, int32_t* tau, int32_t* emitted,
-                                 int32_t* n_emit, cudaStream_t s);
+                                 int32_t* n_emit, bool pdl, cudaStream_t s);
 cudaError_t launch_accept_stochastic(int B, int K, int V, const int32_t* d, const float* z, const float* q,
                                      float temperature, uint64_t seed, uint64_t round, int32_t* tau,
-                                     int32_t* emitted, int32_t* n_emit, cudaStream_t s);
+                                     int32_t* emitted, int32_t* n_emit, bool pdl, cudaStream_t s);
 
 }  // namespace dflash

@@ -68,6 +68,8 @@ __global__ void k_alloc(const int32_t* __restrict__ n_rows, int first_seq, int B
   extern __shared__ int s_off[];  // [B + 1] row offsets, then [B] old lengths
   int* s_len = s_off + B + 1;
   __shared__ int s_ok;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) {
     int bad = 0, total_need = 0, rows = 0;
     for (int i = 0; i < B; ++i) {
@@ -153,9 +155,9 @@ cudaError_t launch_truncate(dflash_ctx* c, int b, int new_len, cudaStream_t s) {
 
 cudaError_t launch_alloc(dflash_ctx* c, const int32_t* n_rows, int first_seq, int B, int max_rows, cudaStream_t s) {
   const size_t smem = sizeof(int) * (2 * B + 1);
-  k_alloc<<<1, 256, smem, s>>>(n_rows, first_seq, B, max_rows, c->cfg.n_pages, c->cfg.max_pages_per_seq, c->seq_len,
-                               c->page_table, c->free_ring, c->scal, c->row_seq, c->row_pos, c->row_src, c->status);
-  return cudaGetLastError();
+  return launch_k(k_alloc, dim3(1), dim3(256), smem, s, dim3(1), c->pdl, n_rows, first_seq, B, max_rows,
+                  c->cfg.n_pages, c->cfg.max_pages_per_seq, c->seq_len, c->page_table, c->free_ring, c->scal,
+                  c->row_seq, c->row_pos, c->row_src, c->status);
 }
 
 cudaError_t launch_rope_table(dflash_ctx* c, cudaStream_t s) {

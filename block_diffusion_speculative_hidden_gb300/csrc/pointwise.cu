@@ -1,7 +1,7 @@
-// Row-wise kernels around the projections: the feature-fusion RMSNorm, the
-// pre-norms of the draft layers, the block input embedding, the LM-head
-// argmax merge and the S = 2 commit.  (Residual adds, SwiGLU, RoPE and the
-// paged K/V stores run inside the projection epilogues, epilogue.cuh.)
+// Row-wise kernels around the projections: the gather of the injected
+// feature rows, the block input embedding, the LM-head argmax merge and the
+// S = 2 commit.  (Residual adds, the RMSNorms, SwiGLU, RoPE and the paged
+// K/V stores run inside the projection epilogues, epilogue.cuh.)
 //
 // Passages: the DFlash Guide, "2. Target Hidden-State Conditioning" (fused
 // features) and "3. Cross-Layer KV Injection" (K, V of every draft layer
@@ -21,6 +21,8 @@ namespace dflash {
 template <typename T>
 __global__ void k_gather_rows(const T* __restrict__ feats, T* __restrict__ out, const int* scal,
                               const int32_t* row_src, int F) {
+  pdl_wait();  // the row map comes from the page allocation just before
+  pdl_trigger();
   const int r = blockIdx.x;
   if (r >= scal[0]) return;
   const long long src = row_src[r];
@@ -30,87 +32,57 @@ __global__ void k_gather_rows(const T* __restrict__ feats, T* __restrict__ out, 
   for (int i = threadIdx.x; i < n16; i += blockDim.x) d[i] = s[i];
 }
 
-// h[r] = RMSNorm(u[r]) * g_fc, u = the fused-feature FC output (fp32)
-template <typename T>
-__global__ void k_fc_norm(const float* __restrict__ u, const T* __restrict__ gain, ActOut<T> h, const int* scal,
-                          int d, float eps) {
-  __shared__ float red[32];
-  const int r = blockIdx.x;
-  if (r >= scal[0]) return;
-  const float* row = u + static_cast<long long>(r) * d;
-  float ss = 0.f;
-  for (int n = threadIdx.x; n < d; n += blockDim.x) ss += row[n] * row[n];
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / d + eps);
-  for (int n = threadIdx.x; n < d; n += blockDim.x)
-    h.put(static_cast<long long>(r) * d + n, row[n] * inv * to_f32(gain[n]));
-}
-
 // ------------------------------------------------------------ draft side
 
 // Block input: x[m] = E[token] (token = [MASK], or in pass 2 the committed
-// pass-1 token), a[m] = RMSNorm(x[m]) * g_in of layer 0.
+// pass-1 token).  Also the first layer's pre-norm in folded form (see
+// epilogue.cuh): a[m] = g_in . x[m] and the per-128-column sums of x^2.
+// One CTA of 128 threads per (column tile, row).
 template <typename T>
-__global__ void k_embed_norm(const T* __restrict__ embed, const T* __restrict__ gain, float* __restrict__ x,
-                             ActOut<T> a, int d, int mask_id, int vocab, const int32_t* commit,
-                             const int32_t* tok1, int* status, float eps) {
-  __shared__ float red[32];
-  const int m = blockIdx.x;
+__global__ void __launch_bounds__(128) k_embed(const T* __restrict__ embed, const T* __restrict__ gain,
+                                               float* __restrict__ x, ActOut<T> a, float* __restrict__ ss, int ss_ld,
+                                               int d, int mask_id, int vocab, const int32_t* commit,
+                                               const int32_t* tok1, int* status) {
+  __shared__ float red[4];
+  pdl_wait();
+  pdl_trigger();
+  const int tile = blockIdx.x, m = blockIdx.y, n = tile * 128 + threadIdx.x;
   int tok = mask_id;
   if (commit != nullptr && commit[m] != 0) tok = tok1[m];
   if (tok < 0 || tok >= vocab) {
-    if (threadIdx.x == 0) atomicOr(status, ST_BAD_TOKEN);
+    if (threadIdx.x == 0 && tile == 0) atomicOr(status, ST_BAD_TOKEN);
     tok = mask_id;
   }
-  float ss = 0.f;
-  for (int n = threadIdx.x; n < d; n += blockDim.x) {
-    const float v = to_f32(embed[static_cast<long long>(tok) * d + n]);
-    x[static_cast<long long>(m) * d + n] = v;
-    ss += v * v;
-  }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / d + eps);
-  for (int n = threadIdx.x; n < d; n += blockDim.x) {
+  float v = 0.f;
+  if (n < d) {
+    v = to_f32(embed[static_cast<long long>(tok) * d + n]);
     const long long e = static_cast<long long>(m) * d + n;
-    a.put(e, x[e] * inv * to_f32(gain[n]));
+    x[e] = v;
+    a.put(e, v * to_f32(gain[n]));
   }
-}
-
-// a[m] = RMSNorm(x[m]) * gain (the pre-norm of the next projection)
-template <typename T>
-__global__ void k_rmsnorm_rows(const float* __restrict__ x, ActOut<T> a, const T* __restrict__ gain, int d,
-                               float eps) {
-  __shared__ float red[32];
-  const int m = blockIdx.x;
-  const float4* row = reinterpret_cast<const float4*>(x + static_cast<long long>(m) * d);
-  float ss = 0.f;
-  for (int n = threadIdx.x; n < d / 4; n += blockDim.x) {
-    const float4 v = row[n];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-  }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / d + eps);
-  for (int n = threadIdx.x; n < d / 4; n += blockDim.x) {
-    const float4 v = row[n];
-    const long long e = static_cast<long long>(m) * d + 4 * n;
-    a.put(e + 0, v.x * inv * to_f32(gain[4 * n + 0]));
-    a.put(e + 1, v.y * inv * to_f32(gain[4 * n + 1]));
-    a.put(e + 2, v.z * inv * to_f32(gain[4 * n + 2]));
-    a.put(e + 3, v.w * inv * to_f32(gain[4 * n + 3]));
-  }
+  const float q = warp_sum(v * v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = q;
+  __syncthreads();
+  if (threadIdx.x == 0) ss[static_cast<long long>(tile) * ss_ld + m] = (red[0] + red[1]) + (red[2] + red[3]);
 }
 
 // fp32 path: per (row, 128-column tile) max / argmax / sum-exp of the logits,
 // same format as the tensor-core LM-head epilogue; optional copy-out.
-__global__ void k_logits_tiles(const float* __restrict__ z, int V, LmPartials lm, float* user, const int32_t* skip) {
+// The final RMSNorm arrives folded: z holds W (g . x) and row m is scaled
+// by the row's 1 / RMS here.
+__global__ void k_logits_tiles(const float* __restrict__ z, int V, LmPartials lm, float* user, const int32_t* skip,
+                               EpiArgs norm) {
   __shared__ float smx[4];
   __shared__ int sidx[4];
   __shared__ float sse[4];
+  __shared__ float s_r;
   const int m = blockIdx.y, tile = blockIdx.x;
   const int n = tile * kTileN + threadIdx.x;  // blockDim = 128
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) s_r = norm_row_scale(norm, m);
+  __syncthreads();
   const bool nv = n < V;
-  const float val = nv ? z[static_cast<long long>(m) * V + n] : -INFINITY;
+  const float val = nv ? z[static_cast<long long>(m) * V + n] * s_r : -INFINITY;
   if (user != nullptr && nv && (skip == nullptr || skip[m] == 0)) user[static_cast<long long>(m) * V + n] = val;
   float mx = val;
   int ix = n;
@@ -164,6 +136,8 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmPartials lm, int M, const in
                                                   const float* conf1, int32_t* tok_out, float* conf_out) {
   __shared__ float s_mx[8], s_se[8];
   __shared__ int s_ix[8];
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (commit != nullptr && commit[m] != 0) {
@@ -198,6 +172,8 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmPartials lm, int M, const in
 // S = 2: commit the K/2 most confident positions of each block (ties to the
 // lower position).  One warp per sequence.
 __global__ void k_commit(const float* __restrict__ conf1, int32_t* commit, int B) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -212,14 +188,14 @@ __global__ void k_commit(const float* __restrict__ conf1, int32_t* commit, int B
 
 // ------------------------------------------------------------ launchers
 
-#define DFLASH_DISPATCH(c, KERNEL_CALL)               \
+#define DFLASH_DISPATCH(c, ...)                       \
   do {                                                \
     if ((c)->cfg.dtype == DFLASH_BF16) {              \
       using T = __nv_bfloat16;                        \
-      KERNEL_CALL;                                    \
+      __VA_ARGS__;                                    \
     } else {                                          \
       using T = float;                                \
-      KERNEL_CALL;                                    \
+      __VA_ARGS__;                                    \
     }                                                 \
   } while (0)
 
@@ -228,56 +204,37 @@ static ActOut<T> act_out(void* hi, void* lo) {
   return ActOut<T>{static_cast<T*>(hi), static_cast<T*>(lo)};
 }
 
-cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, int max_rows, int first_seq,
-                               cudaStream_t s) {
-  (void)max_rows;
-  (void)first_seq;
+cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, cudaStream_t s) {
   const int F = c->cfg.n_taps * c->cfg.tap_width;
-  DFLASH_DISPATCH(c, (k_gather_rows<T><<<rows, 128, 0, s>>>(static_cast<const T*>(feats), static_cast<T*>(c->fc_in),
-                                                            c->scal, c->row_src, F)));
-  return cudaGetLastError();
+  DFLASH_DISPATCH(c, return launch_k(k_gather_rows<T>, dim3(rows), dim3(128), 0, s, dim3(1), c->pdl,
+                                     static_cast<const T*>(feats), static_cast<T*>(c->fc_in), c->scal, c->row_src,
+                                     F));
 }
 
-cudaError_t launch_fc_norm(dflash_ctx* c, int rows, cudaStream_t s) {
-  const int d = c->cfg.hidden;
-  DFLASH_DISPATCH(c, (k_fc_norm<T><<<rows, 256, 0, s>>>(c->y, static_cast<const T*>(c->g_fc),
-                                                        act_out<T>(c->h_fused, c->h_lo), c->scal, d,
-                                                        c->cfg.rms_eps)));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_embed_norm(dflash_ctx* c, int M, bool second_pass, cudaStream_t s) {
+cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, cudaStream_t s) {
   const auto& g = c->cfg;
-  DFLASH_DISPATCH(c, (k_embed_norm<T><<<M, 256, 0, s>>>(static_cast<const T*>(c->embed),
-                                                        static_cast<const T*>(c->g_in[0]), c->x,
-                                                        act_out<T>(c->a, c->a_lo), g.hidden, g.mask_id, g.vocab,
-                                                        second_pass ? c->commit : nullptr, c->tok1, c->status,
-                                                        g.rms_eps)));
-  return cudaGetLastError();
+  const dim3 grid((g.hidden + 127) / 128, M);
+  DFLASH_DISPATCH(c, return launch_k(k_embed<T>, grid, dim3(128), 0, s, dim3(1), c->pdl,
+                                     static_cast<const T*>(c->embed), static_cast<const T*>(c->g_in[0]), c->x,
+                                     act_out<T>(c->a, c->a_lo), c->ss_x, g.max_batch * kBlockK, g.hidden,
+                                     g.mask_id, g.vocab, second_pass ? c->commit : nullptr, c->tok1, c->status));
 }
 
-cudaError_t launch_rmsnorm_rows(dflash_ctx* c, int M, const void* gain, cudaStream_t s) {
-  const int d = c->cfg.hidden;
-  DFLASH_DISPATCH(c, (k_rmsnorm_rows<T><<<M, 256, 0, s>>>(c->x, act_out<T>(c->a, c->a_lo),
-                                                          static_cast<const T*>(gain), d, c->cfg.rms_eps)));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, cudaStream_t s) {
+cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, const EpiArgs& norm,
+                                cudaStream_t s) {
   dim3 grid(c->lm.n_tiles, M);
-  k_logits_tiles<<<grid, kTileN, 0, s>>>(c->logits_ws, c->cfg.vocab, c->lm, user_logits, skip);
+  k_logits_tiles<<<grid, kTileN, 0, s>>>(c->logits_ws, c->cfg.vocab, c->lm, user_logits, skip, norm);
   return cudaGetLastError();
 }
 
 cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,
                             cudaStream_t s) {
-  k_lm_merge<<<M, 256, 0, s>>>(c->lm, M, commit, c->tok1, c->conf1, tok_out, conf_out);
-  return cudaGetLastError();
+  return launch_k(k_lm_merge, dim3(M), dim3(256), 0, s, dim3(1), c->pdl, c->lm, M, commit, c->tok1, c->conf1,
+                  tok_out, conf_out);
 }
 
 cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s) {
-  k_commit<<<(B + 3) / 4, 128, 0, s>>>(c->conf1, c->commit, B);
-  return cudaGetLastError();
+  return launch_k(k_commit, dim3((B + 3) / 4), dim3(128), 0, s, dim3(1), c->pdl, c->conf1, c->commit, B);
 }
 
 }  // namespace dflash

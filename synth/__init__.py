@@ -133,6 +133,12 @@ MINI_CONFIGS: Dict[str, DraftConfig] = {
                           hidden=384, n_q_heads=16, n_kv_heads=2, head_dim=64,
                           ffn=776, vocab=3001, n_taps=3, tap_width=384,
                           s_passes=2, accept="stochastic", rounds=3, seed=2002),
+    # dh = 64, G = 1, many sequences with long contexts: few key splits per
+    # (sequence, kv head), each streaming several 8-page blocks
+    "mini_c": DraftConfig("mini_c", batch=12, ctx_lo=150, ctx_hi=1400, n_layers=1,
+                          hidden=512, n_q_heads=8, n_kv_heads=8, head_dim=64,
+                          ffn=1024, vocab=3000, n_taps=2, tap_width=512,
+                          match_prob=0.8, rounds=3, seed=2004),
     # fp32 mini: ragged, several pages, G = 2
     "mini_f32": DraftConfig("mini_f32", batch=2, ctx_lo=17, ctx_hi=90, n_layers=2,
                             hidden=192, n_q_heads=6, n_kv_heads=3, head_dim=32,
