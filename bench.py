@@ -152,6 +152,31 @@ def barrier(world: int):
         dist.barrier()
 
 
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "k_gemm_tc_c2_layer.md")
+GEMM_SOURCES = ("gemm.cu", "epilogue.cuh", "common.cuh", "internal.h")
+
+
+def gemm_traffic(cfg):
+    """DRAM bytes per k_gemm_tc launch measured by ncu for the c2 round (see
+    the profile file), or None when the workload differs or the GEMM sources
+    changed since the capture."""
+    import hashlib
+    if cfg.name != "c2_qwen3_8b_shaped" or not os.path.exists(GEMM_PROFILE):
+        return None
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "block_diffusion_speculative_hidden_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    fields = {}
+    for line in open(GEMM_PROFILE):
+        if ":" in line and line.split(":")[0] in ("traffic_per_launch_bytes", "source_fingerprint"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_fingerprint") != h.hexdigest()[:16]:
+        return None
+    return float(fields["traffic_per_launch_bytes"])
+
+
 def algorithmic_bytes(cfg):
     """Bytes the hot path must move per round (B sequences), by kernel class.
 
@@ -505,7 +530,9 @@ def main(argv=None):
                        synthetic_target="one torch elementwise op per step forms y from the drafts; inside the region"),
         "roofline": {"kernel": "k_gemm_tc (tcgen05 projections + LM head)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "traffic": gemm_traffic(cfg),
+                     "traffic_unit": "bytes per launch (ncu dram read+write; profiles/k_gemm_tc_c2_layer.md)",
+                     "algorithmic_bytes_per_launch": (ab["proj"] + ab["lm_head"]) * steps / max(gemm_launches, 1),
                      "bytes_per_step": ab["proj"] + ab["lm_head"], "launches_per_step": gemm_launches / steps,
                      "timed_in": "second timed region of the same loop, per-launch CUDA events"},
         "kernels": per_class,

@@ -56,7 +56,6 @@ struct MmaAttnCfg {
   static constexpr int SUB = M / 64;               // 16-lane row blocks per TMEM quadrant
   static constexpr int QUADS = R <= 64 ? R / 16 : 4;  // quadrants holding real rows
   static constexpr int RPT = 2 * SUB;              // rows per softmax thread
-  static constexpr int RPT_MAX = 4;
   static constexpr int NCH = DH / 64;              // 128-byte column chunks of a head
   static constexpr int Q_CH = R * 128;             // stride of the Q chunks (real rows only)
   static constexpr int Q_BYTES = NCH * Q_CH;
@@ -71,7 +70,7 @@ struct MmaAttnCfg {
   static constexpr int OFF_P = Q_BYTES;
   static constexpr int OFF_KV = OFF_P + (P_IN_K ? 0 : P_BYTES);
   static constexpr int OFF_BAR = OFF_KV + NST * STAGE_BYTES;
-  static constexpr int BAR_BYTES = 128 + 8 * 32 * RPT_MAX * 4;  // barriers, then the pair-exchange slots
+  static constexpr int BAR_BYTES = 128 + 8 * 32 * RPT * 4;  // barriers, then the pair-exchange slots
   static constexpr int SMEM_FIXED = 1024 + OFF_BAR + BAR_BYTES;  // + 4 bytes per page id
   static constexpr int TMEM_COLS = 256;
   static_assert(KBP * 16 <= 256 && DH <= 256, "S and O share 256 TMEM columns");
@@ -706,10 +705,11 @@ int max_clusters_t(dflash_ctx* c, int splits) {
   return n;
 }
 
-// Short splits (at most 13 pages): all keys in one block, no ring, and a CTA
-// small enough to share an SM with a projection CTA (so the context streams
-// in while the QKV projection runs); longer splits stream 8-page blocks
-// through a 2-deep ring.
+// Short splits (at most 13 pages): all keys in one block, no ring, and (for
+// up to 64 query rows of dh 128) a CTA of at most 124 KB, small enough to
+// share an SM with a 102 KB projection CTA (so the context streams in while
+// the QKV projection runs); longer splits stream 8-page blocks through a
+// 2-deep ring.
 constexpr int kShortPages = 13;
 
 // Runs F<DH, G, KBP, NST>(args) for the kernel instance serving `splits`.
