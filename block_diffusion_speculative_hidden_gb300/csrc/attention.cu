@@ -211,8 +211,8 @@ static cudaError_t launch_attn_ty(dflash_ctx* c, int layer, int B, int splits, c
 
 // fp32 workloads: the fp32 SIMT kernel above; bf16 workloads (fp16 pool):
 // the tcgen05 kernel of attention_mma.cu.
-cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
-  if (c->cfg.dtype == DFLASH_BF16) return launch_attention_mma(c, layer, B, splits, s);
+cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next) {
+  if (c->cfg.dtype == DFLASH_BF16) return launch_attention_mma(c, layer, B, splits, s, next);
   return launch_attn_ty<float>(c, layer, B, splits, s);
 }
 

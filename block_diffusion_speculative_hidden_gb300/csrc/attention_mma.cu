@@ -95,6 +95,7 @@ struct MmaAttnParams {
   void* o_hi;         // ActOut<bf16> of the attention output [B*16][Hq*DH]
   void* o_lo;
   int* status;
+  L2Plan l2;          // the O projection's weights, prefetched into L2 once QKV completed
 };
 
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
@@ -128,17 +129,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to the
-// shared memory of cluster CTA `rank` (same offsets), completing as
-// transaction bytes on that CTA's mbarrier `bar`.
-__device__ __forceinline__ void bulk_copy_to_rank(uint32_t dst_local, uint32_t src_local, uint32_t bytes,
-                                                  uint64_t* bar, uint32_t rank) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dsmem_map(dst_local, rank)),
-      "r"(src_local), "r"(bytes), "r"(dsmem_map(smem_u32(bar), rank))
-      : "memory");
-}
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -147,6 +137,7 @@ template <int DH, int G, int KBP, int NST>
 __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_constant__ CUtensorMap tmQ,
                                                               const __grid_constant__ CUtensorMap tmK,
                                                               const __grid_constant__ CUtensorMap tmV,
+                                                              const __grid_constant__ CUtensorMap tmNext,
                                                               const __grid_constant__ MmaAttnParams p) {
   using C = MmaAttnCfg<DH, G, KBP, NST>;
   constexpr int R = C::R;
@@ -285,6 +276,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_const
         for (int c = 0; c < C::NCH; ++c)
           tma_load_2d(sQ + c * C::Q_CH + g * 2048, &tmQ, q_full, (kvh * G + g) * DH + c * 64, b * kBlockK);
       pdl_trigger();
+      // HBM is mostly idle from here on: stream the O projection's weights into L2
+      if (p.l2.ctas > 0) l2_prefetch_plan(&tmNext, p.l2);
       int issued = blk;
       for (; blk < nblk; ++blk) {
         if (blk >= NST && !mbar_wait(&kv_empty[blk % NST], ((blk / NST) & 1) ^ 1, p.status)) break;
@@ -528,17 +521,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_const
     if (threadIdx.x == 0) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(S * (r1 - r0) * LD * 4));
     fence_proxy_async_smem();
     __syncthreads();
-    cluster_sync_all();  // every receive area is idle and armed
+    // every receive area is idle (a receive count may follow the bytes it counts)
+    cluster_arrive_relaxed();
+    cluster_wait();
     if (threadIdx.x == 0) {
       for (int k = 0; k < S; ++k) {
         const int k0 = min(R, k * rpr), k1 = min(R, k0 + rpr);
         if (k1 > k0)
-          bulk_copy_to_rank(smem_u32(recv + cr * rpr * LD), smem_u32(stage + k0 * LD),
+          bulk_copy_smem_to_rank(smem_u32(recv + cr * rpr * LD), smem_u32(stage + k0 * LD),
                             static_cast<uint32_t>((k1 - k0) * LD * 4), recv_bar, static_cast<uint32_t>(k));
       }
     }
     mbar_wait(recv_bar, 0, p.status);
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    cluster_arrive_relaxed();  // my incoming copies have landed
     for (int e = threadIdx.x; e < (r1 - r0) * (DH / 4); e += blockDim.x) {
       const int j = e / (DH / 4), d4 = (e % (DH / 4)) * 4, r = r0 + j;
       float M = -INFINITY;
@@ -564,7 +559,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_const
       out.put(base + 2, num.z * inv);
       out.put(base + 3, num.w * inv);
     }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_wait();
   }
   tc_fence_before();
   __syncthreads();
@@ -644,7 +639,7 @@ int split_pages_bound(const dflash_ctx* c, int splits) {
 }
 
 template <int DH, int G, int KBP, int NST>
-cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
+cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next) {
   const auto& g = c->cfg;
   const int page_slots = split_pages_bound(c, splits);
   const int smem = smem_bytes<DH, G, KBP, NST>(page_slots);
@@ -672,8 +667,10 @@ cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s
   p.o_hi = c->o;
   p.o_lo = c->o_lo;
   p.status = c->status;
+  CUtensorMap tn = c->attn_map_k;  // placeholder when there is no plan
+  if (!gemm_l2_plan(c, next, &p.l2, &tn)) p.l2 = L2Plan{};
   return launch_k(k_attn_mma<DH, G, KBP, NST>, dim3(splits, g.n_kv_heads, B), dim3(kAttnThreads), smem, s,
-                  dim3(splits, 1, 1), c->pdl, c->attn_map_q, c->attn_map_k, c->attn_map_v, p);
+                  dim3(splits, 1, 1), c->pdl, c->attn_map_q, c->attn_map_k, c->attn_map_v, tn, p);
 }
 
 // How many clusters of `splits` CTAs of this kernel instance can be
@@ -731,8 +728,8 @@ auto dispatch(dflash_ctx* c, int splits, A... args) {
 
 template <int DH, int G, int KBP, int NST>
 struct LaunchF {
-  static cudaError_t run(dflash_ctx* c, int splits, int layer, int B, cudaStream_t s) {
-    return launch_t<DH, G, KBP, NST>(c, layer, B, splits, s);
+  static cudaError_t run(dflash_ctx* c, int splits, int layer, int B, cudaStream_t s, const NextGemm* next) {
+    return launch_t<DH, G, KBP, NST>(c, layer, B, splits, s, *next);
   }
   static cudaError_t invalid() { return cudaErrorInvalidValue; }
 };
@@ -761,8 +758,8 @@ int attention_mma_splits(dflash_ctx* c, int B) {
   return s0;
 }
 
-cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
-  return dispatch<LaunchF>(c, splits, layer, B, s);
+cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next) {
+  return dispatch<LaunchF>(c, splits, layer, B, s, &next);
 }
 
 }  // namespace dflash

@@ -107,6 +107,19 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync_all, for work between arriving and waiting.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrive without ordering this thread's earlier memory operations (loads
+// still in flight do not delay it); for barriers that only order progress,
+// e.g. "every CTA of the cluster is past its main loop".
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Address of the same shared-memory location in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -120,6 +133,17 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// the same-offset shared memory of cluster CTA `rank`, completing as
+// transaction bytes on that CTA's mbarrier `bar` (same offset as ours).
+__device__ __forceinline__ void bulk_copy_smem_to_rank(uint32_t dst_local, uint32_t src_local, uint32_t bytes,
+                                                       uint64_t* bar, uint32_t rank) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dsmem_map(dst_local, rank)),
+      "r"(src_local), "r"(bytes), "r"(dsmem_map(smem_u32(bar), rank))
+      : "memory");
 }
 __device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
@@ -161,6 +185,40 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// ----------------------------------------------------------------- L2 prefetch of the next projection
+// The next projection's weight k-blocks that its CTAs read right after
+// their shared-memory ring, in its CTA geometry (grid x = 128-row weight
+// tiles, grid z = k-splits).  A kernel whose own HBM streaming is done (a
+// projection past its last load, the latency-bound attention) pulls them
+// into L2, so that HBM keeps streaming through its tail.
+struct L2Plan {
+  int ctas;          // weight tiles x splits of the next projection (0: nothing)
+  int n_tiles;       // its 128-row weight tiles
+  int kb_per_split;  // its k-blocks per split
+  int n_kb;          // its k-blocks in total
+  int first;         // first k-block (within a split) to prefetch: its ring holds the ones before
+  int count;         // k-blocks per weight tile and split to prefetch
+};
+
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+// This CTA's share of the plan (one thread issues it).
+__device__ __forceinline__ void l2_prefetch_plan(const CUtensorMap* map, const L2Plan& pl) {
+  const int G = gridDim.x * gridDim.y * gridDim.z;
+  const int me = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  for (int j = me; j < pl.ctas; j += G) {
+    const int x = j % pl.n_tiles, z = j / pl.n_tiles;
+    const int kb0 = z * pl.kb_per_split, kb1 = min(pl.n_kb, kb0 + pl.kb_per_split);
+    for (int i = pl.first; i < pl.first + pl.count && kb0 + i < kb1; ++i)
+      tma_prefetch_l2_2d(map, (kb0 + i) * 64, x * 128);
+  }
 }
 
 // ----------------------------------------------------------------- tcgen05

@@ -205,7 +205,8 @@ int device_sms() {
   } while (0)
 
 dflash_status run_gemm(dflash_ctx* c, const void* W, int N, int K, const void* X, const void* X_lo, int M,
-                       int M_alloc, int splits, const int* m_valid, const EpiArgs& epi, cudaStream_t s) {
+                       int M_alloc, int splits, const int* m_valid, const EpiArgs& epi, cudaStream_t s,
+                       const NextGemm& next = NextGemm{}) {
   GemmLaunch g{};
   g.W = W;
   g.X = X;
@@ -220,8 +221,24 @@ dflash_status run_gemm(dflash_ctx* c, const void* W, int N, int K, const void* X
   g.ldo = N;
   g.m_valid = m_valid;
   g.epi = epi;
+  g.next = next;
   DF_CHECK(gemm_launch(c, g, s));
   return DFLASH_OK;
+}
+
+// The projection after a launch, for the L2 prefetch of its weights (only the
+// latency-bound attention issues one: between projections HBM is busy and
+// the prefetch would only compete).
+NextGemm next_gemm(const void* W, int N, int K, int M, int splits, long long budget) {
+  NextGemm n;
+  n.W = W;
+  n.N = N;
+  n.K = K;
+  n.M = M;
+  n.split = true;
+  n.splits = splits;
+  n.budget_bytes = budget;
+  return n;
 }
 
 EpiArgs epi_base(dflash_ctx* c, int kind, int M, int N) {
@@ -505,7 +522,9 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
       }
       {
         ProfScope p(ctx, DFLASH_PROF_ATTN, g.dtype == DFLASH_BF16 ? 1 : 2, s);
-        DF_CHECK(launch_attention(ctx, l, B, a_sp, s));
+        // attention is latency-bound: it streams all of the O projection's
+        // weights beyond that kernel's ring into L2
+        DF_CHECK(launch_attention(ctx, l, B, a_sp, s, next_gemm(ctx->w_o[l], d, qd, M, s_o, 1ll << 40)));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);

@@ -110,17 +110,75 @@ __device__ __forceinline__ int4 epi_row_info(const EpiArgs& e, int m) {
   return make_int4(0, 0, 0, 0);
 }
 
-constexpr int kEpiBatch = 8;  // rows finished together (their loads in flight at once)
+constexpr int kEpiBatch = 8;  // rows finished together (their loads in flight at once); the
+                              // sum-of-squares butterfly below assumes 8
+
+// Global inputs of the first kEpiBatch rows of an epilogue, loaded ahead of
+// it by the thread that finishes column n0 + threadIdx.x, so that their
+// latency overlaps the accumulator readout and the split-K reduction.
+struct EpiPre {
+  float a[kEpiBatch];  // RESIDUAL: x; QKV / KV_INJECT: RoPE cos
+  float b[kEpiBatch];  // QKV / KV_INJECT: RoPE sin
+  float gn;            // STORE / RESIDUAL: gain of the next norm at this column
+};
+
+template <typename T>
+__device__ __forceinline__ void epilogue_preload(const EpiArgs& e, int m0, int rows, int n0, const int4* ri,
+                                                 EpiPre& pre) {
+  const int t = threadIdx.x, n = n0 + t;
+  if (e.m_valid != nullptr) rows = min(rows, *e.m_valid - m0);
+  rows = min(rows, e.M - m0);
+  pre.gn = 0.f;
+#pragma unroll
+  for (int u = 0; u < kEpiBatch; ++u) pre.a[u] = pre.b[u] = 0.f;
+  if (rows <= 0 || n >= e.N) return;
+  switch (e.kind) {
+    case EPI_STORE:
+    case EPI_RESIDUAL:
+      if (e.nx_hi != nullptr) pre.gn = to_f32(static_cast<const T*>(e.nx_gain)[n]);
+      if (e.kind == EPI_RESIDUAL)
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u)
+          if (u < rows) pre.a[u] = e.out[static_cast<long long>(m0 + u) * e.N + n];
+      break;
+    case EPI_QKV:
+    case EPI_KV_INJECT: {
+      bool is_v;
+      int i;
+      if (e.kind == EPI_QKV) {
+        const int qd = e.Hq * e.dh, kvd = e.Hkv * e.dh;
+        is_v = n >= qd + kvd;
+        i = n % e.dh;
+      } else {
+        const int kvd = e.Hkv * e.dh, w = n % (2 * kvd);
+        is_v = w >= kvd;
+        i = w % e.dh;
+      }
+      if (is_v) break;
+      const int half = e.dh / 2, jr = i < half ? i : i - half;
+#pragma unroll
+      for (int u = 0; u < kEpiBatch; ++u)
+        if (u < rows) {
+          pre.a[u] = e.rope_cos[ri[u].x * half + jr];
+          pre.b[u] = e.rope_sin[ri[u].x * half + jr];
+        }
+      break;
+    }
+    default:
+      break;
+  }
+}
 
 // Finishes one tile.  All threads of the block call it (blockDim.x == 128);
 // thread t handles output column n0 + t.  `rs` (nullable) holds the row
 // scales of rows m0 .. m0 + rows - 1 and `ri` (nullable) their epi_row_info;
-// `scratch` holds 4 * rows floats and is used when e.ss_out is set.  Rows
+// `scratch` holds 4 * rows floats and is used when e.ss_out is set; `pre`
+// (nullable) holds the first batch's global inputs (epilogue_preload).  Rows
 // are processed kEpiBatch at a time with every global load of a batch
 // issued before any of its results is used.
 template <typename T, typename KT>
 __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int rows, int n0, const float* rs,
-                               const int4* ri, float* scratch) {
+                               const int4* ri, float* scratch, const EpiPre* pre = nullptr) {
   const int t = threadIdx.x;
   const int n = n0 + t;
   if (e.m_valid != nullptr) rows = min(rows, *e.m_valid - m0);
@@ -134,7 +192,8 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
     case EPI_RESIDUAL: {
       const bool nv = n < e.N;
       const ActOut<T> nx{static_cast<T*>(e.nx_hi), static_cast<T*>(e.nx_lo)};
-      const float gn = (e.nx_hi != nullptr && nv) ? to_f32(static_cast<const T*>(e.nx_gain)[n]) : 0.f;
+      const float gn = pre != nullptr ? pre->gn
+                                      : (e.nx_hi != nullptr && nv) ? to_f32(static_cast<const T*>(e.nx_gain)[n]) : 0.f;
       const int warp = t >> 5, lane = t & 31;
       for (int j0 = 0; j0 < rows; j0 += kEpiBatch) {
         float z[kEpiBatch];
@@ -144,7 +203,8 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
           z[u] = 0.f;
           if (nv && j < rows) {
             z[u] = tile[j * 128 + t] * (rs != nullptr ? rs[j] : 1.f);
-            if (e.kind == EPI_RESIDUAL) z[u] += e.out[static_cast<long long>(m0 + j) * e.N + n];
+            if (e.kind == EPI_RESIDUAL)
+              z[u] += (pre != nullptr && j0 == 0) ? pre->a[u] : e.out[static_cast<long long>(m0 + j) * e.N + n];
           }
         }
 #pragma unroll
@@ -157,12 +217,26 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
           }
         }
         if (e.ss_out != nullptr) {
+          // the warp's sums of z^2 for the 8 rows of the batch at once: a
+          // transposing butterfly halves the rows a lane holds at each of the
+          // first three steps (lane bits 4, 3, 2 pick the half), then two
+          // steps finish the sums; lane 4r + (0..3) ends with row r
+          float q[kEpiBatch];
 #pragma unroll
-          for (int u = 0; u < kEpiBatch; ++u) z[u] = warp_sum(z[u] * z[u]);
-          if (lane == 0)
+          for (int u = 0; u < kEpiBatch; ++u) q[u] = z[u] * z[u];
 #pragma unroll
-            for (int u = 0; u < kEpiBatch; ++u)
-              if (j0 + u < rows) scratch[(j0 + u) * 4 + warp] = z[u];
+          for (int o = 16, c = kEpiBatch; o >= 4; o >>= 1, c >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < c / 2; ++i) {
+              const float keep = up ? q[i + c / 2] : q[i], send = up ? q[i] : q[i + c / 2];
+              q[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          q[0] += __shfl_xor_sync(0xffffffffu, q[0], 1);
+          q[0] += __shfl_xor_sync(0xffffffffu, q[0], 2);
+          const int r = (lane >> 2) & 7;
+          if ((lane & 3) == 0 && j0 + r < rows) scratch[(j0 + r) * 4 + warp] = q[0];
         }
       }
       if (e.ss_out != nullptr) {
@@ -174,16 +248,19 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
       break;
     }
     case EPI_SWIGLU: {
-      const int f = (n0 >> 7) * 64 + t;  // tile = 64 gate rows then the 64 matching up rows
-      if (t < 64 && f < e.F) {
+      // tile = 64 gate rows then the 64 matching up rows; thread t takes
+      // feature t % 64 of the rows of parity t / 64
+      const int c = t & 63, h0 = t >> 6;
+      const int f = (n0 >> 7) * 64 + c;
+      if (f < e.F) {
         ActOut<T> a{static_cast<T*>(e.act_hi), static_cast<T*>(e.act_lo)};
-        for (int j0 = 0; j0 < rows; j0 += kEpiBatch) {
+        for (int j0 = h0; j0 < rows; j0 += 2 * kEpiBatch) {
 #pragma unroll
           for (int u = 0; u < kEpiBatch; ++u) {
-            const int j = j0 + u;
+            const int j = j0 + 2 * u;
             if (j < rows) {
               const float sc = rs != nullptr ? rs[j] : 1.f;
-              const float g = tile[j * 128 + t] * sc, up = tile[j * 128 + t + 64] * sc;
+              const float g = tile[j * 128 + c] * sc, up = tile[j * 128 + c + 64] * sc;
               a.put(static_cast<long long>(m0 + j) * e.F + f, g / (1.f + expf(-g)) * up);
             }
           }
@@ -232,8 +309,13 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
           info[u] = ri != nullptr ? ri[j] : epi_row_info(e, m0 + j);
           cs[u] = sn[u] = 0.f;
           if (kind != 2) {
-            cs[u] = e.rope_cos[info[u].x * half + jr];
-            sn[u] = e.rope_sin[info[u].x * half + jr];
+            if (pre != nullptr && j0 == 0) {
+              cs[u] = pre->a[u];
+              sn[u] = pre->b[u];
+            } else {
+              cs[u] = e.rope_cos[info[u].x * half + jr];
+              sn[u] = e.rope_sin[info[u].x * half + jr];
+            }
           }
         }
 #pragma unroll

@@ -37,13 +37,18 @@ struct TcCfg {
   static constexpr int W_BYTES = kTileN * kTileK * 2;  // 16 KB
   static constexpr int X_BYTES = BN * kTileK * 2;
   static constexpr int STAGE_BYTES = W_BYTES + (SPLIT ? 2 : 1) * X_BYTES;
-  // BN <= 64: two CTAs per SM; wider tiles: one CTA with a deeper ring
-  static constexpr int BUDGET = BN <= 64 ? 110 * 1024 : 200 * 1024;
+  // BN = 16 (single-sequence drafting): a 4-stage ring, so that a CTA fits
+  // beside another one or beside an attention CTA; BN 32-64: two CTAs per SM;
+  // wider tiles: one CTA with a deeper ring
+  static constexpr int BUDGET = BN <= 16 ? 90 * 1024 : BN <= 64 ? 110 * 1024 : 200 * 1024;
   static constexpr int STAGES = (BUDGET / STAGE_BYTES) < 8 ? (BUDGET / STAGE_BYTES) : 8;
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
   static constexpr int SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/ +
                               4 * BN * 4 /*epilogue scratch*/ + BN * 4 /*row scales*/ + BN * 16 /*row info*/;
   static_assert(STAGES >= 2, "pipeline too shallow");
+  // split-K with bulk-copy reduction when the tile, the receive slots (at most BN + 8 rows) and the
+  // reduced slice fit in the stage ring; otherwise the slices are read over distributed shared memory
+  static constexpr bool PUSH_REDUCE = (2 * BN + 8 + BN / 2 + 8) * 128 * 4 <= STAGES * STAGE_BYTES;
   // the own tile plus the reduced slice (at most half the rows, splits >= 2) fit in the stage ring, and
   // so does the LM head's padded tile
   static_assert(BN * 128 * 4 * 3 / 2 <= STAGES * STAGE_BYTES, "epilogue tiles must fit in the stage ring");
@@ -63,12 +68,14 @@ struct TcParams {
   float* logits;
   long long ld_logits;
   const int* skip_rows;
+  L2Plan l2;  // the next projection's weights, prefetched into L2 after this CTA's last load
 };
 
 template <int BN, bool LMHEAD, bool SPLIT>
 __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtensorMap tmW,
                                                  const __grid_constant__ CUtensorMap tmX,
                                                  const __grid_constant__ CUtensorMap tmXlo,
+                                                 const __grid_constant__ CUtensorMap tmNext,
                                                  const __grid_constant__ TcParams p) {
   using C = TcCfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
@@ -79,7 +86,8 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
   uint64_t* full = reinterpret_cast<uint64_t*>(sX + C::STAGES * XS);
   uint64_t* empty = full + C::STAGES;
   uint64_t* accb = empty + C::STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  uint64_t* recvb = accb + 1;  // split-K: this CTA's rows from every split have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recvb + 1);
   int* s_prog = reinterpret_cast<int*>(tmem_slot + 1);  // [0] stages issued, [1] stages consumed
   float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + 256);  // [BN][4] epilogue scratch
   float* s_rs = red + 4 * BN;                             // folded-RMSNorm row scales of rows m0 .. m0 + BN - 1
@@ -106,6 +114,7 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
       mbar_init(&empty[s], 1);
     }
     mbar_init(accb, 1);
+    mbar_init(recvb, 1);
     s_prog[0] = 0;
     s_prog[1] = 0;
     fence_mbar_init();
@@ -149,6 +158,8 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
         if (SPLIT) tma_load_2d(sX + s * XS + C::X_BYTES, &tmXlo, &full[s], kx, m0);
         s_prog[0] = it + 1;
       }
+      // this CTA's weights are all requested: start the next projection's
+      if (p.l2.ctas > 0) l2_prefetch_plan(&tmNext, p.l2);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -215,6 +226,19 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
     }
     tc_fence_before();
     __syncthreads();
+    // the epilogue's global inputs of the rows this CTA finishes, loaded now
+    // (after the TMEM reads, whose waits would otherwise also wait for
+    // them) so that their latency overlaps the split-K reduction
+    EpiPre pre;
+    if (p.epi.kind != EPI_NONE) {
+      int r0 = 0, nr = BN;
+      if (p.splits > 1) {
+        const int rpr = (BN + p.splits - 1) / p.splits;
+        r0 = min(BN, static_cast<int>(cluster_ctarank()) * rpr);
+        nr = min(BN, r0 + rpr) - r0;
+      }
+      epilogue_preload<__nv_bfloat16>(p.epi, m0 + r0, nr, n0, s_ri + r0, pre);
+    }
     const int t = threadIdx.x;
     if (p.epi.kind == EPI_NONE) {
       float* o = p.out + split * p.split_stride;
@@ -224,15 +248,58 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
     if (p.epi.kind != EPI_NONE) {
       const float* rs = p.epi.ss_in != nullptr ? s_rs : nullptr;
       if (p.splits == 1) {
-        apply_epilogue<__nv_bfloat16, __half>(p.epi, tile, m0, BN, n0, rs, s_ri, red);
+        apply_epilogue<__nv_bfloat16, __half>(p.epi, tile, m0, BN, n0, rs, s_ri, red, &pre);
       } else {
         // split-K reduction inside the cluster of this tile's `splits` CTAs:
         // each CTA sums a contiguous slice of the rows over every CTA's tile
-        // (distributed shared memory, split order) and finishes those rows
-        cluster_sync_all();
+        // (split order) and finishes those rows
         const int S = p.splits, cr = static_cast<int>(cluster_ctarank());
         const int rpr = (BN + S - 1) / S;
         const int r_begin = min(BN, cr * rpr), r_end = min(BN, r_begin + rpr);
+        if constexpr (C::PUSH_REDUCE) {
+          // every split copies the rows owned by cluster rank k into slot
+          // [split] of k's receive area with a bulk shared-memory copy that
+          // completes on k's mbarrier; the owner then adds the slots from
+          // local memory.  The cluster barrier is split around the epilogue
+          // so that no CTA leaves while a copy it sources may still read.
+          float* recv = tile + BN * 128;          // [S][rpr][128]
+          float* sub = recv + S * rpr * 128;      // [rpr][128]
+          if (t == 0) mbar_arrive_expect_tx(recvb, static_cast<uint32_t>(S * (r_end - r_begin) * 128 * 4));
+          fence_proxy_async_smem();
+          __syncthreads();  // this CTA's tile is complete and visible to the copy engine
+          // every CTA of the cluster is past its main loop: every receive area
+          // is idle (relaxed: the preloaded epilogue inputs may still be in
+          // flight; a receive count may follow the bytes it counts)
+          cluster_arrive_relaxed();
+          cluster_wait();
+          if (t == 0)
+            for (int k = 0; k < S; ++k) {
+              const int k0 = min(BN, k * rpr), k1 = min(BN, k0 + rpr);
+              if (k1 > k0)
+                bulk_copy_smem_to_rank(smem_u32(recv + cr * rpr * 128), smem_u32(tile + k0 * 128),
+                                       static_cast<uint32_t>((k1 - k0) * 128 * 4), recvb, static_cast<uint32_t>(k));
+            }
+          mbar_wait(recvb, 0, p.status);
+          cluster_arrive_relaxed();  // my incoming copies have landed
+          for (int e = t; e < (r_end - r_begin) * 32; e += 128) {
+            const int j = e / 32, c4 = (e % 32) * 4;
+            float4 acc = *reinterpret_cast<const float4*>(recv + j * 128 + c4);
+            for (int r = 1; r < S; ++r) {
+              const float4 v = *reinterpret_cast<const float4*>(recv + (r * rpr + j) * 128 + c4);
+              acc.x += v.x;
+              acc.y += v.y;
+              acc.z += v.z;
+              acc.w += v.w;
+            }
+            *reinterpret_cast<float4*>(sub + j * 128 + c4) = acc;
+          }
+          __syncthreads();
+          if (r_end > r_begin)
+            apply_epilogue<__nv_bfloat16, __half>(p.epi, sub, m0 + r_begin, r_end - r_begin, n0,
+                                                  rs != nullptr ? rs + r_begin : nullptr, s_ri + r_begin, red, &pre);
+          cluster_wait();
+        } else {
+        cluster_sync_all();
         float* sub = tile + BN * 128;
         const uint32_t tile_s = smem_u32(tile);
         for (int e = t; e < (r_end - r_begin) * 32; e += 128) {
@@ -251,7 +318,8 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
         cluster_sync_all();  // no CTA's tile is read after this point
         if (r_end > r_begin)
           apply_epilogue<__nv_bfloat16, __half>(p.epi, sub, m0 + r_begin, r_end - r_begin, n0,
-                                                rs != nullptr ? rs + r_begin : nullptr, s_ri + r_begin, red);
+                                                rs != nullptr ? rs + r_begin : nullptr, s_ri + r_begin, red, &pre);
+        }
       }
     }
   } else {
@@ -453,12 +521,14 @@ static cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorM
   p.logits = g.logits;
   p.ld_logits = g.ld_logits;
   p.skip_rows = g.skip_rows;
+  CUtensorMap tn = tw;  // the next projection's weights (a placeholder when there is no plan)
+  if (!gemm_l2_plan(c, g.next, &p.l2, &tn)) p.l2 = L2Plan{};
   // splits come from gemm_splits: every split owns at least one k-block
   dim3 grid((g.N + kTileN - 1) / kTileN, (g.M + BN - 1) / BN, g.splits);
   // the splits of one output tile form a thread-block cluster (reduced over DSMEM)
   const bool clustered = !(LM || g.epi.kind == EPI_NONE || g.splits == 1);
   return launch_k(k_gemm_tc<BN, LM, SPLIT>, grid, dim3(128), C::SMEM, s, dim3(1, 1, clustered ? g.splits : 1),
-                  c->pdl, tw, tx, txlo, p);
+                  c->pdl, tw, tx, txlo, tn, p);
 }
 
 template <bool SPLIT>
@@ -534,6 +604,36 @@ int gemm_splits(int n_tiles, int n_kb, int bn, bool split, int num_sms, int max_
   s = std::max(1, std::min({s, 8, n_kb / 4}));
   const int per = (n_kb + s - 1) / s;
   return (n_kb + per - 1) / per;
+}
+
+int gemm_ring_stages(int bn, bool split) {
+  switch (bn) {
+    case 16: return split ? TcCfg<16, true>::STAGES : TcCfg<16, false>::STAGES;
+    case 32: return split ? TcCfg<32, true>::STAGES : TcCfg<32, false>::STAGES;
+    case 64: return split ? TcCfg<64, true>::STAGES : TcCfg<64, false>::STAGES;
+    case 128: return split ? TcCfg<128, true>::STAGES : TcCfg<128, false>::STAGES;
+    default: return TcCfg<256, false>::STAGES;
+  }
+}
+
+bool gemm_l2_plan(dflash_ctx* c, const NextGemm& nx, L2Plan* pl, CUtensorMap* map) {
+  *pl = L2Plan{};
+  if (nx.W == nullptr || c->cfg.dtype != DFLASH_BF16 || nx.splits < 1) return true;
+  const int bn = gemm_bn(nx.M, nx.split);
+  const int n_tiles = (nx.N + kTileN - 1) / kTileN, n_kb = gemm_kb(nx.K);
+  const int kbps = (n_kb + nx.splits - 1) / nx.splits;
+  const int first = std::min(kbps, gemm_ring_stages(bn, nx.split));
+  const long long per_kb = static_cast<long long>(n_tiles) * nx.splits * kTileN * kTileK * 2;
+  const int count = static_cast<int>(std::min<long long>(kbps - first, nx.budget_bytes / per_kb));
+  if (count <= 0) return true;
+  if (!get_tmap(c, nx.W, nx.N, nx.K, kTileN, map)) return false;
+  pl->ctas = n_tiles * nx.splits;
+  pl->n_tiles = n_tiles;
+  pl->kb_per_split = kbps;
+  pl->n_kb = n_kb;
+  pl->first = first;
+  pl->count = count;
+  return true;
 }
 
 int gemm_bn(int M, bool split) {

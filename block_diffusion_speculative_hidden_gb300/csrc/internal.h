@@ -24,6 +24,16 @@ struct LmPartials {
   int n_tiles;  // row stride of the three arrays
 };
 
+// The projection that follows a launch in the chain, for its L2 prefetch
+// (W == nullptr: none).  budget_bytes bounds the bytes prefetched.
+struct NextGemm {
+  const void* W = nullptr;
+  int N = 0, K = 0, M = 0;
+  bool split = true;  // hi+lo activations
+  int splits = 1;
+  long long budget_bytes = 0;
+};
+
 struct GemmLaunch {
   // out[split][m][n] = sum_{k in split} X[m][k] * W[n][k]
   const void* W;  // [N][K]
@@ -44,6 +54,7 @@ struct GemmLaunch {
   float* logits;       // nullable: raw logits [M][ld_logits]
   long long ld_logits;
   const int* skip_rows;  // nullable: rows whose logits are not stored
+  NextGemm next;         // the projection after this one (L2 prefetch of its weights)
 };
 
 struct TmapEntry {
@@ -151,6 +162,9 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
 int gemm_kb(int K);
 int gemm_bn(int M, bool split);
 int gemm_blocks_per_sm(int bn, bool split);
+int gemm_ring_stages(int bn, bool split);
+// The L2 prefetch plan (and the weight tensor map) of projection `nx`.
+bool gemm_l2_plan(dflash_ctx* c, const NextGemm& nx, L2Plan* plan, CUtensorMap* map);
 int gemm_splits(int n_tiles, int n_kb, int bn, bool split, int num_sms, int max_ctas = 0);
 cudaError_t gemm_launch_uncached(int* status, const GemmLaunch& g, cudaStream_t s);
 

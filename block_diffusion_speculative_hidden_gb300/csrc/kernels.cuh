@@ -27,9 +27,9 @@ cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s);
 
 // attention.cu
 int attn_splits(dflash_ctx* c, int B);
-cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
+cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next);
 // attention_mma.cu (fp16 pool, tcgen05)
-cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s);
+cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next);
 int attention_mma_splits(dflash_ctx* c, int B);
 
 // accept.cu
