@@ -113,9 +113,15 @@ __device__ __forceinline__ int4 epi_row_info(const EpiArgs& e, int m) {
 constexpr int kEpiBatch = 8;  // rows finished together (their loads in flight at once); the
                               // sum-of-squares butterfly below assumes 8
 
-// Global inputs of the first kEpiBatch rows of an epilogue, loaded ahead of
-// it by the thread that finishes column n0 + threadIdx.x, so that their
-// latency overlaps the accumulator readout and the split-K reduction.
+// The epilogue runs on kEpiThreads threads: thread t finishes output column
+// n0 + t % 128 of the rows j with j % NH == t / 128 (NH = kEpiThreads / 128),
+// kEpiBatch of its rows at a time.
+constexpr int kEpiThreads = 128;
+__device__ __forceinline__ constexpr int epi_phases() { return kEpiThreads / 128; }
+
+// Global inputs of the first kEpiBatch rows a thread finishes, loaded ahead
+// of the epilogue so that their latency overlaps the accumulator readout and
+// the split-K reduction.
 struct EpiPre {
   float a[kEpiBatch];  // RESIDUAL: x; QKV / KV_INJECT: RoPE cos
   float b[kEpiBatch];  // QKV / KV_INJECT: RoPE sin
@@ -125,7 +131,7 @@ struct EpiPre {
 template <typename T>
 __device__ __forceinline__ void epilogue_preload(const EpiArgs& e, int m0, int rows, int n0, const int4* ri,
                                                  EpiPre& pre) {
-  const int t = threadIdx.x, n = n0 + t;
+  const int NH = epi_phases(), h = threadIdx.x >> 7, n = n0 + (threadIdx.x & 127);
   if (e.m_valid != nullptr) rows = min(rows, *e.m_valid - m0);
   rows = min(rows, e.M - m0);
   pre.gn = 0.f;
@@ -138,8 +144,10 @@ __device__ __forceinline__ void epilogue_preload(const EpiArgs& e, int m0, int r
       if (e.nx_hi != nullptr) pre.gn = to_f32(static_cast<const T*>(e.nx_gain)[n]);
       if (e.kind == EPI_RESIDUAL)
 #pragma unroll
-        for (int u = 0; u < kEpiBatch; ++u)
-          if (u < rows) pre.a[u] = e.out[static_cast<long long>(m0 + u) * e.N + n];
+        for (int u = 0; u < kEpiBatch; ++u) {
+          const int j = u * NH + h;
+          if (j < rows) pre.a[u] = e.out[static_cast<long long>(m0 + j) * e.N + n];
+        }
       break;
     case EPI_QKV:
     case EPI_KV_INJECT: {
@@ -157,11 +165,13 @@ __device__ __forceinline__ void epilogue_preload(const EpiArgs& e, int m0, int r
       if (is_v) break;
       const int half = e.dh / 2, jr = i < half ? i : i - half;
 #pragma unroll
-      for (int u = 0; u < kEpiBatch; ++u)
-        if (u < rows) {
-          pre.a[u] = e.rope_cos[ri[u].x * half + jr];
-          pre.b[u] = e.rope_sin[ri[u].x * half + jr];
+      for (int u = 0; u < kEpiBatch; ++u) {
+        const int j = u * NH + h;
+        if (j < rows) {
+          pre.a[u] = e.rope_cos[ri[j].x * half + jr];
+          pre.b[u] = e.rope_sin[ri[j].x * half + jr];
         }
+      }
       break;
     }
     default:
@@ -169,17 +179,16 @@ __device__ __forceinline__ void epilogue_preload(const EpiArgs& e, int m0, int r
   }
 }
 
-// Finishes one tile.  All threads of the block call it (blockDim.x == 128);
-// thread t handles output column n0 + t.  `rs` (nullable) holds the row
-// scales of rows m0 .. m0 + rows - 1 and `ri` (nullable) their epi_row_info;
-// `scratch` holds 4 * rows floats and is used when e.ss_out is set; `pre`
-// (nullable) holds the first batch's global inputs (epilogue_preload).  Rows
-// are processed kEpiBatch at a time with every global load of a batch
-// issued before any of its results is used.
+// Finishes one tile.  All kEpiThreads threads of the block call it (128 or
+// 256, see above).  `rs` (nullable) holds the row scales of rows
+// m0 .. m0 + rows - 1 and `ri` (nullable) their epi_row_info; `scratch`
+// holds 4 * rows floats and is used when e.ss_out is set; `pre` (nullable)
+// holds each thread's first batch of global inputs (epilogue_preload).
+// Every global load of a batch is issued before any of its results is used.
 template <typename T, typename KT>
 __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int rows, int n0, const float* rs,
                                const int4* ri, float* scratch, const EpiPre* pre = nullptr) {
-  const int t = threadIdx.x;
+  const int NH = epi_phases(), h = threadIdx.x >> 7, t = threadIdx.x & 127;
   const int n = n0 + t;
   if (e.m_valid != nullptr) rows = min(rows, *e.m_valid - m0);
   rows = min(rows, e.M - m0);
@@ -187,6 +196,7 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
   KT* q = static_cast<KT*>(e.q);
   KT* pk = static_cast<KT*>(e.pool_k);
   KT* pv = static_cast<KT*>(e.pool_v);
+  const int step = kEpiBatch * NH;  // rows covered by one batch of all phases
   switch (e.kind) {
     case EPI_STORE:
     case EPI_RESIDUAL: {
@@ -194,12 +204,12 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
       const ActOut<T> nx{static_cast<T*>(e.nx_hi), static_cast<T*>(e.nx_lo)};
       const float gn = pre != nullptr ? pre->gn
                                       : (e.nx_hi != nullptr && nv) ? to_f32(static_cast<const T*>(e.nx_gain)[n]) : 0.f;
-      const int warp = t >> 5, lane = t & 31;
-      for (int j0 = 0; j0 < rows; j0 += kEpiBatch) {
+      const int warp = t >> 5, lane = t & 31;  // warp within this phase
+      for (int j0 = 0; j0 < rows; j0 += step) {
         float z[kEpiBatch];
 #pragma unroll
         for (int u = 0; u < kEpiBatch; ++u) {
-          const int j = j0 + u;
+          const int j = j0 + u * NH + h;
           z[u] = 0.f;
           if (nv && j < rows) {
             z[u] = tile[j * 128 + t] * (rs != nullptr ? rs[j] : 1.f);
@@ -209,7 +219,7 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
         }
 #pragma unroll
         for (int u = 0; u < kEpiBatch; ++u) {
-          const int j = j0 + u;
+          const int j = j0 + u * NH + h;
           if (nv && j < rows) {
             const long long o = static_cast<long long>(m0 + j) * e.N + n;
             if (e.out != nullptr) e.out[o] = z[u];
@@ -217,31 +227,31 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
           }
         }
         if (e.ss_out != nullptr) {
-          // the warp's sums of z^2 for the 8 rows of the batch at once: a
+          // the warp's sums of z^2 for its 8 rows of the batch at once: a
           // transposing butterfly halves the rows a lane holds at each of the
           // first three steps (lane bits 4, 3, 2 pick the half), then two
-          // steps finish the sums; lane 4r + (0..3) ends with row r
-          float q[kEpiBatch];
+          // steps finish the sums; lane 4u + (0..3) ends with row u
+          float sq[kEpiBatch];
 #pragma unroll
-          for (int u = 0; u < kEpiBatch; ++u) q[u] = z[u] * z[u];
+          for (int u = 0; u < kEpiBatch; ++u) sq[u] = z[u] * z[u];
 #pragma unroll
           for (int o = 16, c = kEpiBatch; o >= 4; o >>= 1, c >>= 1) {
             const bool up = (lane & o) != 0;
 #pragma unroll
             for (int i = 0; i < c / 2; ++i) {
-              const float keep = up ? q[i + c / 2] : q[i], send = up ? q[i] : q[i + c / 2];
-              q[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+              const float keep = up ? sq[i + c / 2] : sq[i], send = up ? sq[i] : sq[i + c / 2];
+              sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
           }
-          q[0] += __shfl_xor_sync(0xffffffffu, q[0], 1);
-          q[0] += __shfl_xor_sync(0xffffffffu, q[0], 2);
-          const int r = (lane >> 2) & 7;
-          if ((lane & 3) == 0 && j0 + r < rows) scratch[(j0 + r) * 4 + warp] = q[0];
+          sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 1);
+          sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 2);
+          const int j = j0 + ((lane >> 2) & 7) * NH + h;
+          if ((lane & 3) == 0 && j < rows) scratch[j * 4 + warp] = sq[0];
         }
       }
       if (e.ss_out != nullptr) {
         __syncthreads();
-        for (int j = t; j < rows; j += 128)
+        for (int j = threadIdx.x; j < rows; j += kEpiThreads)
           e.ss_out[static_cast<long long>(n0 >> 7) * e.ss_ld + m0 + j] =
               (scratch[j * 4 + 0] + scratch[j * 4 + 1]) + (scratch[j * 4 + 2] + scratch[j * 4 + 3]);
       }
@@ -249,15 +259,16 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
     }
     case EPI_SWIGLU: {
       // tile = 64 gate rows then the 64 matching up rows; thread t takes
-      // feature t % 64 of the rows of parity t / 64
-      const int c = t & 63, h0 = t >> 6;
+      // feature t % 64 of the rows j with j % P == t / 64 (P = kEpiThreads / 64)
+      constexpr int P = kEpiThreads / 64;
+      const int c = threadIdx.x & 63, ph = threadIdx.x >> 6;
       const int f = (n0 >> 7) * 64 + c;
       if (f < e.F) {
         ActOut<T> a{static_cast<T*>(e.act_hi), static_cast<T*>(e.act_lo)};
-        for (int j0 = h0; j0 < rows; j0 += 2 * kEpiBatch) {
+        for (int j0 = ph; j0 < rows; j0 += P * kEpiBatch) {
 #pragma unroll
           for (int u = 0; u < kEpiBatch; ++u) {
-            const int j = j0 + 2 * u;
+            const int j = j0 + P * u;
             if (j < rows) {
               const float sc = rs != nullptr ? rs[j] : 1.f;
               const float g = tile[j * 128 + c] * sc, up = tile[j * 128 + c + 64] * sc;
@@ -300,12 +311,12 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
       const int jr = i < half ? i : i - half;  // RoPE frequency index
       const int base = t - i;                   // tile column of the head's element 0
       const long long lbase = static_cast<long long>(l) * e.layer_stride;
-      for (int j0 = 0; j0 < rows; j0 += kEpiBatch) {
+      for (int j0 = 0; j0 < rows; j0 += step) {
         int4 info[kEpiBatch];
         float cs[kEpiBatch], sn[kEpiBatch];
 #pragma unroll
         for (int u = 0; u < kEpiBatch; ++u) {
-          const int j = min(j0 + u, rows - 1);
+          const int j = min(j0 + u * NH + h, rows - 1);
           info[u] = ri != nullptr ? ri[j] : epi_row_info(e, m0 + j);
           cs[u] = sn[u] = 0.f;
           if (kind != 2) {
@@ -320,7 +331,7 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
         }
 #pragma unroll
         for (int u = 0; u < kEpiBatch; ++u) {
-          const int j = j0 + u;
+          const int j = j0 + u * NH + h;
           if (j >= rows) continue;
           const float* row = tile + j * 128;
           const float sc = rs != nullptr ? rs[j] : 1.f;

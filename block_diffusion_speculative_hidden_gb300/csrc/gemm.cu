@@ -71,8 +71,15 @@ struct TcParams {
   L2Plan l2;  // the next projection's weights, prefetched into L2 after this CTA's last load
 };
 
+// Warp 0 lane 0 issues TMA, warp 1 lane 0 the MMAs (warp 1 owns the TMEM
+// allocation), the other warps gather the epilogue's row facts while the
+// main loop runs; all warps read the accumulator and run the epilogue (the
+// code also runs with 256 threads: warps w and w + 4 then share a TMEM lane
+// quadrant and split its columns; measured no faster at 16 rows).
+constexpr int kGemmThreads = kEpiThreads;
+
 template <int BN, bool LMHEAD, bool SPLIT>
-__global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtensorMap tmW,
+__global__ void __launch_bounds__(kGemmThreads) k_gemm_tc(const __grid_constant__ CUtensorMap tmW,
                                                  const __grid_constant__ CUtensorMap tmX,
                                                  const __grid_constant__ CUtensorMap tmXlo,
                                                  const __grid_constant__ CUtensorMap tmNext,
@@ -189,7 +196,7 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
     // memory (folded-RMSNorm row scales, row positions and pages)
     pdl_wait();
     const int mv = p.m_valid != nullptr ? min(p.M, *p.m_valid) : p.M;
-    for (int j = threadIdx.x - 64; j < BN; j += 64) {
+    for (int j = threadIdx.x - 64; j < BN; j += kGemmThreads - 64) {
       const int m = m0 + j;
       const bool ok = m < mv;
       if (p.epi.ss_in != nullptr) s_rs[j] = ok ? norm_row_scale(p.epi, m) : 0.f;
@@ -210,19 +217,22 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
     // a wait gave up: let every copy still in flight land before the ring is reused
     for (int it = s_prog[1]; it < s_prog[0]; ++it) mbar_wait(&full[it % C::STAGES], (it / C::STAGES) & 1, p.status);
   }
-  const int n = n0 + warp * 32 + lane;
+  // TMEM lane quadrant of this warp (warps w and w + 4 share one and split
+  // the accumulator's columns in chunks of 16)
+  const int quad = warp & 3, wg = warp >> 2;
+  const int n = n0 + quad * 32 + lane;
   const bool nv = n < p.N;
-  const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   if constexpr (!LMHEAD) {
     // the accumulator goes to a [BN][128] fp32 tile in the (now idle) stage ring
     float* tile = reinterpret_cast<float*>(smem);
     __syncthreads();
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = 16 * wg; c < BN; c += 16 * (kGemmThreads / 128)) {
       float v[16];
       tc_ld_32x32b_x16(tbase + c, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) tile[(c + j) * 128 + warp * 32 + lane] = v[j];
+      for (int j = 0; j < 16; ++j) tile[(c + j) * 128 + quad * 32 + lane] = v[j];
     }
     tc_fence_before();
     __syncthreads();
@@ -242,8 +252,9 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
     const int t = threadIdx.x;
     if (p.epi.kind == EPI_NONE) {
       float* o = p.out + split * p.split_stride;
-      for (int j = 0; j < BN && m0 + j < p.M; ++j)
-        if (nv) o[static_cast<long long>(m0 + j) * p.ldo + n] = tile[j * 128 + t];
+      const int col = t & 127, nc = n0 + col;
+      for (int j = t >> 7; j < BN && m0 + j < p.M; j += kGemmThreads >> 7)
+        if (nc < p.N) o[static_cast<long long>(m0 + j) * p.ldo + nc] = tile[j * 128 + col];
     }
     if (p.epi.kind != EPI_NONE) {
       const float* rs = p.epi.ss_in != nullptr ? s_rs : nullptr;
@@ -281,7 +292,7 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
             }
           mbar_wait(recvb, 0, p.status);
           cluster_arrive_relaxed();  // my incoming copies have landed
-          for (int e = t; e < (r_end - r_begin) * 32; e += 128) {
+          for (int e = t; e < (r_end - r_begin) * 32; e += kGemmThreads) {
             const int j = e / 32, c4 = (e % 32) * 4;
             float4 acc = *reinterpret_cast<const float4*>(recv + j * 128 + c4);
             for (int r = 1; r < S; ++r) {
@@ -302,7 +313,7 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
         cluster_sync_all();
         float* sub = tile + BN * 128;
         const uint32_t tile_s = smem_u32(tile);
-        for (int e = t; e < (r_end - r_begin) * 32; e += 128) {
+        for (int e = t; e < (r_end - r_begin) * 32; e += kGemmThreads) {
           const int j = r_begin + e / 32, c4 = (e % 32) * 4;
           const uint32_t off = static_cast<uint32_t>((j * 128 + c4) * 4);
           float4 acc = ld_dsmem_f4(dsmem_map(tile_s + off, 0));
@@ -329,14 +340,14 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
     float* tile = reinterpret_cast<float*>(smem);
     __syncthreads();
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = 16 * wg; c < BN; c += 16 * (kGemmThreads / 128)) {
       float v[16];
       tc_ld_32x32b_x16(tbase + c, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = m0 + c + j;
         const float val = nv ? (p.epi.ss_in != nullptr ? v[j] * s_rs[c + j] : v[j]) : -INFINITY;
-        tile[(c + j) * kLmLd + warp * 32 + lane] = val;
+        tile[(c + j) * kLmLd + quad * 32 + lane] = val;
         if (p.logits != nullptr && nv && s_ri[c + j].w != 0) p.logits[m * p.ld_logits + n] = val;
       }
     }
@@ -344,8 +355,9 @@ __global__ void __launch_bounds__(128) k_gemm_tc(const __grid_constant__ CUtenso
     __syncthreads();
     const int seg = threadIdx.x & 7;
 #pragma unroll 1
-    for (int rb = 0; rb < BN; rb += 16) {
+    for (int rb = 0; rb < BN; rb += kGemmThreads >> 3) {
       const int j = rb + (threadIdx.x >> 3);
+      if (j >= BN) continue;  // uniform per warp (4 rows a warp, BN a multiple of 16)
       const float* row = tile + j * kLmLd;
       float z[16];
 #pragma unroll
@@ -527,7 +539,7 @@ static cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorM
   dim3 grid((g.N + kTileN - 1) / kTileN, (g.M + BN - 1) / BN, g.splits);
   // the splits of one output tile form a thread-block cluster (reduced over DSMEM)
   const bool clustered = !(LM || g.epi.kind == EPI_NONE || g.splits == 1);
-  return launch_k(k_gemm_tc<BN, LM, SPLIT>, grid, dim3(128), C::SMEM, s, dim3(1, 1, clustered ? g.splits : 1),
+  return launch_k(k_gemm_tc<BN, LM, SPLIT>, grid, dim3(kGemmThreads), C::SMEM, s, dim3(1, 1, clustered ? g.splits : 1),
                   c->pdl, tw, tx, txlo, tn, p);
 }
 
