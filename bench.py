@@ -45,6 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-rounds", type=int, default=4, help="oracle rounds timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay leg")
     ap.add_argument("--reset-every", type=int, default=16,
                     help="roll each sequence back to its prompt length every N rounds")
     ap.add_argument("--kernel", choices=["gemm"], default=None,
@@ -153,7 +154,7 @@ def barrier(world: int):
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "k_gemm_tc_c2_layer.md")
-GEMM_SOURCES = ("gemm.cu", "epilogue.cuh", "common.cuh", "internal.h")
+GEMM_SOURCES = ("gemm.cu", "epilogue.cuh", "common.cuh")
 
 
 def gemm_traffic(cfg):
@@ -336,8 +337,51 @@ def run_ours(args, cfg, world, rank, local):
     launches_per_step = sum(v[1] for v in prof.values()) / args.steps
     # ---- e2e: host buffers through the public API, copies inside the region
     e2e = run_e2e(wl, args, device)
+    graph = None if args.no_graph else run_graph(wl, args, device)
     return dict(value=value, ms=ms_max, tokens=tokens, mean_tau=mean_tau, clocks=clocks, prof=prof, ms_b=ms_b,
-                launches_per_step=launches_per_step, e2e=e2e, wl=wl)
+                launches_per_step=launches_per_step, e2e=e2e, graph=graph, wl=wl)
+
+
+def run_graph(wl, args, device):
+    """The same rounds replayed as CUDA graphs (dflash_graph_*): one recording
+    per round slot r mod rounds (inject, draft, the synthetic target's
+    verify, accept, bookkeeping and the periodic rollback, exactly the eager
+    round), then the timed region launches one graph per round."""
+    import torch
+    gs = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    graphs = []
+    with torch.cuda.stream(gs):
+        for r in range(wl.rounds):
+            wl.dr.graph_begin(stream=gs)
+            wl.step(r)
+            wl.maybe_reset(r, args.reset_every)
+            graphs.append(wl.dr.graph_end(stream=gs))
+    n = wl.rounds
+    # start from the prompts, so that the rollback schedule of the recorded
+    # rounds (round index mod reset_every) applies from replay 0
+    with torch.cuda.stream(gs):
+        for b in range(wl.cfg.batch):
+            wl.dr.truncate(b, int(wl.lens[b]), stream=gs)
+    for i in range(args.warmup):
+        graphs[i % n].launch(stream=gs)
+    gs.synchronize()
+    wl.tau_sum.zero_()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(gs)
+    for i in range(args.steps):
+        graphs[(args.warmup + i) % n].launch(stream=gs)
+    e1.record(gs)
+    gs.synchronize()
+    ms = e0.elapsed_time(e1)
+    assert wl.dr.device_status() == 0
+    tau = float(wl.tau_sum.sum().item()) / (args.steps * wl.cfg.batch)
+    for g in graphs:
+        g.close()
+    return {"value": args.steps * wl.cfg.batch * K_BLOCK / (ms / 1e3), "unit": UNIT,
+            "ms_per_step": ms / args.steps, "steps": args.steps, "mean_tau": tau,
+            "launch": "one CUDA graph per round (dflash_graph_launch), inputs resident"}
 
 
 def run_e2e(wl, args, device):
@@ -538,6 +582,7 @@ def main(argv=None):
         "kernels": per_class,
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
+        "graph": res["graph"],
         "gpu_launches": int(round(res["launches_per_step"] * steps)),
         "clocks": res["clocks"],
     }

@@ -14,14 +14,16 @@ LIB_PATH = os.path.join(_HERE, "libdflash.so")
 DFLASH_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "pool exhausted",
                 4: "CUDA error", 5: "device status set", 6: "workspace too small",
-                7: "too large for the fixed scratch"}
+                7: "too large for the fixed scratch", 8: "not allowed while capturing"}
+ROUND_DEVICE = (1 << 64) - 1   # dflash_accept: take the round from the device counter
 DEV_POOL_EXHAUSTED, DEV_SEQ_TOO_LONG, DEV_WAIT_TIMEOUT, DEV_BAD_TOKEN, DEV_BAD_ROWS = 1, 2, 4, 8, 16
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 EXPORTED = ("dflash_workspace_size", "dflash_kv_pool_size", "dflash_create", "dflash_destroy",
             "dflash_reset", "dflash_release", "dflash_inject_kv", "dflash_draft_block",
             "dflash_accept", "dflash_get_status", "dflash_status_string", "dflash_gemm_bf16",
-            "dflash_profile_enable", "dflash_profile_read", "dflash_truncate", "dflash_gemm_bf16_noalloc")
+            "dflash_profile_enable", "dflash_profile_read", "dflash_truncate", "dflash_gemm_bf16_noalloc",
+            "dflash_graph_begin", "dflash_graph_end", "dflash_graph_launch", "dflash_graph_destroy")
 PROF_CLASSES = ("proj", "lm_head", "inject", "attention", "rowwise", "accept")
 
 
@@ -91,6 +93,14 @@ def lib() -> ctypes.CDLL:
         L.dflash_profile_enable.argtypes = [_VP, ctypes.c_int]
         L.dflash_profile_read.restype = ctypes.c_int
         L.dflash_profile_read.argtypes = [_VP, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _VP]
+        L.dflash_graph_begin.restype = ctypes.c_int
+        L.dflash_graph_begin.argtypes = [_VP, _VP]
+        L.dflash_graph_end.restype = ctypes.c_int
+        L.dflash_graph_end.argtypes = [_VP, _VP, ctypes.POINTER(ctypes.c_void_p)]
+        L.dflash_graph_launch.restype = ctypes.c_int
+        L.dflash_graph_launch.argtypes = [_VP, _VP]
+        L.dflash_graph_destroy.restype = ctypes.c_int
+        L.dflash_graph_destroy.argtypes = [_VP]
         L.dflash_status_string.restype = ctypes.c_char_p
         L.dflash_status_string.argtypes = [ctypes.c_int]
         _lib = L

@@ -68,13 +68,20 @@ constexpr int kAccThreads = 1024;
 __global__ void __launch_bounds__(kAccThreads) k_accept_stochastic(int K, int V, const int32_t* __restrict__ d,
                                                                    const float* __restrict__ z,
                                                                    const float* __restrict__ q, float invT,
-                                                                   uint2 key, uint32_t rnd, int32_t* tau_out,
+                                                                   uint2 key, uint32_t rnd_host,
+                                                                   int* round_ctr, int32_t* tau_out,
                                                                    int32_t* emitted, int32_t* n_emit) {
   __shared__ float s_a[32], s_b[32], s_c[32];
   __shared__ int s_i[32], s_j[32];
+  __shared__ uint32_t s_rnd;
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // round_ctr (nullable): [0] the device round counter, [1] CTAs done with it
+  if (tid == 0)
+    s_rnd = round_ctr != nullptr ? static_cast<uint32_t>(*reinterpret_cast<volatile int*>(round_ctr)) : rnd_host;
+  __syncthreads();
+  const uint32_t rnd = s_rnd;
   int tau = K;
   for (int i = 0; i <= K; ++i) {
     const float* row = z + (static_cast<long long>(b) * (K + 1) + i) * V;
@@ -180,6 +187,16 @@ __global__ void __launch_bounds__(kAccThreads) k_accept_stochastic(int K, int V,
   if (tid == 0) {
     tau_out[b] = tau;
     n_emit[b] = tau + 1;
+    // every CTA read the counter before it arrives, so the last to arrive
+    // may advance it for the next call
+    if (round_ctr != nullptr) {
+      __threadfence();
+      if (atomicAdd(round_ctr + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        round_ctr[1] = 0;
+        atomicAdd(round_ctr, 1);
+        __threadfence();
+      }
+    }
   }
 }
 
@@ -190,11 +207,12 @@ cudaError_t launch_accept_greedy(int B, int K, const int32_t* d, const int32_t* 
 }
 
 cudaError_t launch_accept_stochastic(int B, int K, int V, const int32_t* d, const float* z, const float* q,
-                                     float temperature, uint64_t seed, uint64_t round, int32_t* tau,
-                                     int32_t* emitted, int32_t* n_emit, bool pdl, cudaStream_t s) {
+                                     float temperature, uint64_t seed, uint64_t round, int* round_ctr,
+                                     int32_t* tau, int32_t* emitted, int32_t* n_emit, bool pdl, cudaStream_t s) {
   const uint2 key = make_uint2(static_cast<uint32_t>(seed & 0xffffffffu), static_cast<uint32_t>(seed >> 32));
   return launch_k(k_accept_stochastic, dim3(B), dim3(kAccThreads), 0, s, dim3(1), pdl, K, V, d, z, q,
-                  1.0f / temperature, key, static_cast<uint32_t>(round & 0xffffffffu), tau, emitted, n_emit);
+                  1.0f / temperature, key, static_cast<uint32_t>(round & 0xffffffffu), round_ctr, tau, emitted,
+                  n_emit);
 }
 
 }  // namespace dflash

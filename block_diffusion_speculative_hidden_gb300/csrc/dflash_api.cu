@@ -328,6 +328,7 @@ const char* dflash_status_string(dflash_status s) {
     case DFLASH_ERR_STATE: return "device status word set";
     case DFLASH_ERR_WORKSPACE: return "workspace or pool buffer too small";
     case DFLASH_ERR_TOO_LARGE: return "request exceeds the fixed scratch of the no-allocation entry point";
+    case DFLASH_ERR_CAPTURE: return "not allowed in the context's capture state";
   }
   return "unknown";
 }
@@ -410,6 +411,10 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, v
 
 dflash_status dflash_destroy(dflash_ctx* ctx) {
   if (ctx == nullptr) return DFLASH_ERR_INVALID_ARG;
+  if (ctx->capturing) {  // leave the stream usable: drop the unfinished recording
+    cudaGraph_t g = nullptr;
+    if (cudaStreamEndCapture(ctx->capture, &g) == cudaSuccess && g != nullptr) cudaGraphDestroy(g);
+  }
   for (auto& r : ctx->prof_live) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -620,8 +625,9 @@ dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* dra
   }
   if (mode != 1 || target_logits == nullptr || !(temperature > 0.f)) return DFLASH_ERR_INVALID_ARG;
   ProfScope p(ctx, DFLASH_PROF_ACCEPT, 1, s);
+  int* round_ctr = round == DFLASH_ROUND_DEVICE ? ctx->status + 2 : nullptr;
   DF_CHECK(launch_accept_stochastic(B, kBlockK, ctx->cfg.vocab, draft_tokens, target_logits, draft_probs,
-                                    temperature, seed, round, accept_len, emitted, n_emit, ctx->pdl, s));
+                                    temperature, seed, round, round_ctr, accept_len, emitted, n_emit, ctx->pdl, s));
   return DFLASH_OK;
 }
 
@@ -658,14 +664,67 @@ dflash_status dflash_gemm_bf16(const void* W, int N, int K, const void* X, const
   return DFLASH_OK;
 }
 
+dflash_status dflash_graph_begin(dflash_ctx* ctx, dflash_stream stream) {
+  if (ctx == nullptr || stream == nullptr) return DFLASH_ERR_INVALID_ARG;
+  if (ctx->capturing || ctx->prof_on) return DFLASH_ERR_CAPTURE;
+  DF_CHECK(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal));
+  ctx->capturing = true;
+  ctx->capture = stream;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_graph_end(dflash_ctx* ctx, dflash_stream stream, dflash_graph** out) {
+  if (ctx == nullptr || out == nullptr) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!ctx->capturing || stream != ctx->capture) return DFLASH_ERR_CAPTURE;
+  ctx->capturing = false;
+  ctx->capture = nullptr;
+  cudaGraph_t g = nullptr;
+  if (cudaStreamEndCapture(stream, &g) != cudaSuccess || g == nullptr) {
+    if (g != nullptr) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return DFLASH_ERR_CUDA;
+  }
+  cudaGraphExec_t x = nullptr;
+  if (cudaGraphInstantiate(&x, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return DFLASH_ERR_CUDA;
+  }
+  auto* r = new (std::nothrow) dflash_graph{g, x};
+  if (r == nullptr) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    return DFLASH_ERR_CUDA;
+  }
+  *out = r;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_graph_launch(dflash_graph* graph, dflash_stream stream) {
+  if (graph == nullptr) return DFLASH_ERR_INVALID_ARG;
+  DF_CHECK(cudaGraphLaunch(graph->exec, stream));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_graph_destroy(dflash_graph* graph) {
+  if (graph == nullptr) return DFLASH_ERR_INVALID_ARG;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
+  return DFLASH_OK;
+}
+
 dflash_status dflash_profile_enable(dflash_ctx* ctx, int enable) {
   if (ctx == nullptr) return DFLASH_ERR_INVALID_ARG;
+  if (ctx->capturing) return DFLASH_ERR_CAPTURE;
   ctx->prof_on = enable != 0;
   return DFLASH_OK;
 }
 
 dflash_status dflash_profile_read(dflash_ctx* ctx, float* ms, int* launches, dflash_stream stream) {
   if (ctx == nullptr || ms == nullptr || launches == nullptr) return DFLASH_ERR_INVALID_ARG;
+  if (ctx->capturing) return DFLASH_ERR_CAPTURE;
   for (int i = 0; i < DFLASH_PROF_CLASSES; ++i) {
     ms[i] = 0.f;
     launches[i] = 0;
@@ -686,6 +745,7 @@ dflash_status dflash_profile_read(dflash_ctx* ctx, float* ms, int* launches, dfl
 
 dflash_status dflash_get_status(dflash_ctx* ctx, int* device_status, dflash_stream stream) {
   if (ctx == nullptr || device_status == nullptr) return DFLASH_ERR_INVALID_ARG;
+  if (ctx->capturing) return DFLASH_ERR_CAPTURE;
   DF_CHECK(cudaMemcpyAsync(device_status, ctx->status, sizeof(int), cudaMemcpyDeviceToHost, stream));
   DF_CHECK(cudaStreamSynchronize(stream));
   return DFLASH_OK;

@@ -65,6 +65,11 @@ struct TmapEntry {
 
 }  // namespace dflash
 
+struct dflash_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
 struct dflash_ctx {
   dflash_config cfg;
   int elem;  // bytes per element of the config dtype
@@ -107,6 +112,9 @@ struct dflash_ctx {
   // folded RMSNorm: partial sums of squares, [ceil(hidden/128)][rows]
   float* ss_x;   // draft rows (row stride max_batch * 16)
   float* ss_h;   // inject rows (row stride max_inject_rows)
+  // stream being recorded into a graph (dflash_graph_begin), else null
+  cudaStream_t capture = nullptr;
+  bool capturing = false;
   // launch timing (dflash_profile_enable)
   bool prof_on = false;
   struct ProfRec {

@@ -21,7 +21,9 @@ __global__ void k_reset(int* status, int* scal, int32_t* free_ring, int P, int32
   for (int i = t; i < n_pt; i += stride) page_table[i] = -1;
   for (int i = t; i < B; i += stride) seq_len[i] = 0;
   if (t == 0) {
-    *status = 0;
+    status[0] = 0;
+    status[2] = 0;  // device round counter of the stochastic accept, and its arrivals
+    status[3] = 0;
     scal[0] = 0;
     scal[1] = 0;
     scal[2] = P;

@@ -72,6 +72,27 @@ def pack_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor) -> torch.Tensor:
     return torch.stack([g.reshape(G, 64, d), u.reshape(G, 64, d)], 1).reshape(G * 128, d)
 
 
+class RoundGraph:
+    """A recorded round (dflash_graph_end); launch() replays it."""
+
+    def __init__(self, L, handle: ctypes.c_void_p):
+        self.L, self.handle = L, handle
+
+    def launch(self, stream=None) -> None:
+        _lib.check(self.L.dflash_graph_launch(self.handle, _stream(stream)), "dflash_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            self.L.dflash_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Drafter:
     """One libdflash context plus the device buffers it borrows.
 
@@ -217,6 +238,18 @@ class Drafter:
     def truncate(self, b: int, new_len: int, stream=None) -> None:
         """Shorten sequence b to new_len tokens; freed pages go to the free-list tail."""
         _lib.check(self.L.dflash_truncate(self.ctx, b, new_len, _stream(stream)), "dflash_truncate")
+
+    # ------------------------------------------------------------------ host-free rounds
+    def graph_begin(self, stream=None) -> None:
+        """Start recording the stream (not the legacy default stream): calls on it,
+        this library's and torch's, are recorded until graph_end."""
+        _lib.check(self.L.dflash_graph_begin(self.ctx, _stream(stream)), "dflash_graph_begin")
+
+    def graph_end(self, stream=None) -> "RoundGraph":
+        """Stop recording; the recorded calls as a replayable graph."""
+        g = ctypes.c_void_p()
+        _lib.check(self.L.dflash_graph_end(self.ctx, _stream(stream), ctypes.byref(g)), "dflash_graph_end")
+        return RoundGraph(self.L, g)
 
     def profile(self, enable: bool) -> None:
         """Bracket every launch with CUDA events (read with profile_read)."""

@@ -59,7 +59,8 @@ typedef enum {
   DFLASH_ERR_CUDA = 4,              /* a CUDA runtime call failed */
   DFLASH_ERR_STATE = 5,             /* the device status word is non-zero */
   DFLASH_ERR_WORKSPACE = 6,         /* workspace or pool buffer too small */
-  DFLASH_ERR_TOO_LARGE = 7          /* request exceeds the fixed scratch of dflash_gemm_bf16_noalloc */
+  DFLASH_ERR_TOO_LARGE = 7,         /* request exceeds the fixed scratch of dflash_gemm_bf16_noalloc */
+  DFLASH_ERR_CAPTURE = 8            /* not allowed in the context's capture state (dflash_graph_begin) */
 } dflash_status;
 
 /* Bits of the device status word (dflash_get_status). */
@@ -215,14 +216,59 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
  *   accepted emit a draw from p_K.  Uniforms: Philox4x32-10 with key =
  *   seed and counter (v, i | stream << 16, b, round); stream 0 is the accept
  *   test (v = 0), stream 1 the exponential race argmax_v r(v) / -ln U_v.
+ *   round = DFLASH_ROUND_DEVICE takes the round from a counter on the
+ *   device instead: the call uses its current value and advances it by one
+ *   (dflash_create and dflash_reset set it to 0), so a captured round
+ *   (dflash_graph_begin) draws fresh uniforms at every replay.
  * Outputs (device): accept_len int32 [B] (tau), emitted int32 [B, K+1]
  * (-1 padded), n_emit int32 [B] = tau + 1.  The KV cache is not touched:
  * the next dflash_inject_kv appends n_emit rows. */
+#define DFLASH_ROUND_DEVICE UINT64_MAX
+
 dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* draft_tokens,
                             const int32_t* target_tokens, const float* target_logits,
                             const float* draft_probs, float temperature, uint64_t seed,
                             uint64_t round, int32_t* accept_len, int32_t* emitted, int32_t* n_emit,
                             dflash_stream stream);
+
+/* Host-free rounds.  [Chapter] "The systems side: Spec V2" (the host's
+ * bookkeeping of a round is overlapped with the GPU's work) and the
+ * [Guide]'s "Production Benchmarks on NVIDIA Blackwell B200" (the
+ * deployment runs on CUDA graphs).
+ *
+ * Every call of inject, draft and accept is asynchronous and keeps tau,
+ * lengths and pages on the device, so a whole round (dflash_inject_kv with
+ * the previous round's n_emit as n_rows, dflash_draft_block, the caller's
+ * own verification work, dflash_accept) can be recorded once and replayed
+ * as one CUDA graph launch.  dflash_graph_begin starts recording `stream`
+ * (a created stream, not the legacy default one) in thread-local capture
+ * mode: every call on that stream up to dflash_graph_end, of this library or
+ * of the caller (kernels, async copies), is recorded instead of run, with
+ * the arguments it had (pointers, B, S, mode, seed; use DFLASH_ROUND_DEVICE
+ * for stochastic rounds).  Make each recorded call once outside the capture
+ * first, with the same shapes: the first call of a shape sets up host-side
+ * state (tensor maps, occupancy figures) that capture does not allow.
+ * While recording, dflash_get_status, dflash_profile_enable and
+ * dflash_profile_read return DFLASH_ERR_CAPTURE, and so does a second
+ * dflash_graph_begin.  The graph borrows every buffer the recorded calls
+ * name; they must outlive it and stay where they are. */
+typedef struct dflash_graph dflash_graph; /* opaque, owned by the caller after dflash_graph_end */
+
+/* Start recording `stream`.  Errors: INVALID_ARG (NULL stream), CAPTURE
+ * (already recording, or per-launch profiling is on), CUDA. */
+dflash_status dflash_graph_begin(dflash_ctx* ctx, dflash_stream stream);
+
+/* Stop recording and instantiate the graph into *out.  If a call failed
+ * while recording (the capture was invalidated) returns CUDA and *out is
+ * NULL; the stream is no longer recording either way.  Errors: INVALID_ARG,
+ * CAPTURE (not recording, or another stream), CUDA. */
+dflash_status dflash_graph_end(dflash_ctx* ctx, dflash_stream stream, dflash_graph** out);
+
+/* Enqueue one replay of the recorded round on `stream` (any stream). */
+dflash_status dflash_graph_launch(dflash_graph* graph, dflash_stream stream);
+
+/* Free the graph (after its replays have completed). */
+dflash_status dflash_graph_destroy(dflash_graph* graph);
 
 /* The drafter's dense projection kernel on its own, for testing it in
  * isolation: out[s][m][n] = sum over the k-blocks of split s of

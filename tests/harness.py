@@ -160,6 +160,12 @@ class Pair:
         conf = conf.cpu().numpy()
         com = committed.cpu().numpy().astype(bool)
         zg = logits.cpu().numpy() if with_logits else None
+        return self.check_outputs(S, tok, conf, com, zg), tok
+
+    def check_outputs(self, S: int, tok: np.ndarray, conf: np.ndarray, com: np.ndarray, zg: Optional[np.ndarray]):
+        """The oracle's draft of every checked sequence against the GPU's
+        outputs of the same draft (host arrays); returns the oracle results."""
+        cfg = self.cfg
         res = {}
         for b in self.seqs:
             r = self.orc.draft(b, s_passes=S)
@@ -172,7 +178,7 @@ class Pair:
                 assert np.max(np.abs(lc - np.log(r["conf"]))) < 2 * LOGIT_TOL[cfg.dtype] + 1e-6
             else:
                 self._check_two_pass(b, r, tok[b], conf[b], com[b], zg[b] if zg is not None else None)
-        return res, tok
+        return res
 
     def _check_two_pass(self, b, r, tok, conf, com, zg):
         cfg = self.cfg

@@ -72,3 +72,12 @@ def test_null_arguments_rejected_before_device_work(L):
     assert L.dflash_accept(None, 0, 1, None, None, None, None, 1.0, 0, 0, None, None, None, None) == 1
     assert L.dflash_destroy(None) == 1
     assert L.dflash_status_string(3) == b"KV page pool exhausted"
+
+
+def test_graph_calls_validate_on_the_host(L):
+    out = ctypes.c_void_p(1)
+    assert L.dflash_graph_begin(None, None) == 1
+    assert L.dflash_graph_end(None, None, ctypes.byref(out)) == 1
+    assert L.dflash_graph_launch(None, None) == 1
+    assert L.dflash_graph_destroy(None) == 1
+    assert L.dflash_status_string(8) == b"not allowed in the context's capture state"
