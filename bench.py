@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rounds", type=int, default=4, help="oracle rounds timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay leg")
+    ap.add_argument("--sweep", action="store_true",
+                    help="draft-cost sweeps (1/3/5 draft layers; projections on 1 vs 16 rows), JSON line per item")
     ap.add_argument("--reset-every", type=int, default=16,
                     help="roll each sequence back to its prompt length every N rounds")
     ap.add_argument("--kernel", choices=["gemm"], default=None,
@@ -526,6 +528,85 @@ def run_kernel_gemm(args, cfg):
                       "frac_hbm": byts / (ms / 1e3) / 1e9 / hbm, "peak": f"{kind} {hbm}"}), flush=True)
 
 
+def _median_ms(fn, reps: int, flush) -> float:
+    import torch
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return float(np.median(times))
+
+
+def run_sweep(args, cfg):
+    """Draft-cost sweeps on the workload's shapes.
+
+    layers: a round (inject, draft, accept) and a draft pass alone with 1, 3
+    and 5 draft layers.  rows: the drafter's projections (one layer's QKV, O,
+    gate/up, down, and the LM head) on 1 activation row (one token per
+    sequence, an autoregressive step) and on 16 rows (the K = 16 block), each
+    from HBM (L2 flushed before every launch); one JSON line per item."""
+    import torch
+    from block_diffusion_speculative_hidden_gb300 import gemm_bf16
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    steps = args.steps
+    for L in (1, 3, 5):
+        c = cfg.replace(n_layers=L, name=f"{cfg.name}_{L}layer")
+        wl = Workload(c, 64, 0, device, reset_every=args.reset_every)
+        for i in range(args.warmup):
+            wl.step(i)
+            wl.maybe_reset(i, args.reset_every)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            wl.step(args.warmup + i)
+            wl.maybe_reset(args.warmup + i, args.reset_every)
+        e1.record()
+        torch.cuda.synchronize()
+        round_ms = e0.elapsed_time(e1) / steps
+        B = c.batch
+        draft_ms = _median_ms(lambda: wl.dr.draft_block(B, c.s_passes, tokens=wl.tok, conf=wl.conf), steps, flush)
+        assert wl.dr.device_status() == 0
+        print(json.dumps({"sweep": "draft_layers", "workload": c.name, "n_layers": L, "round_ms": round_ms,
+                          "draft_pass_ms": draft_ms, "draft_tok_per_s": B * K_BLOCK / (round_ms / 1e3)}), flush=True)
+        del wl
+        torch.cuda.empty_cache()
+    d, F, V = cfg.hidden, cfg.ffn, cfg.vocab
+    qkv = (cfg.n_q_heads + 2 * cfg.n_kv_heads) * cfg.head_dim
+    shapes = {"qkv": (qkv, d), "o": (d, cfg.n_q_heads * cfg.head_dim), "gate_up": (2 * F, d), "down": (d, F),
+              "lm_head": (V, d)}
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    g = torch.Generator(device=device).manual_seed(0)
+    tot = {1: 0.0, 16: 0.0}
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    for name, (N, Kd) in shapes.items():
+        W = (torch.randn((N, Kd), device=device, generator=g) * 0.02).bfloat16()
+        n_tiles, n_kb = -(-N // 128), -(-Kd // 64)
+        splits = max(1, min(2 * sms // n_tiles, max(1, n_kb // 4)))
+        row = {}
+        for M in (1, 16):
+            x = torch.randn((M, Kd), device=device, generator=g)
+            hi = x.bfloat16()
+            lo = (x - hi.float()).bfloat16()
+            for _ in range(args.warmup):
+                gemm_bf16(W, hi, splits=splits, X_lo=lo, status=st)
+            row[M] = _median_ms(lambda: gemm_bf16(W, hi, splits=splits, X_lo=lo, status=st), steps, flush)
+            tot[M] += row[M] * (cfg.n_layers if name != "lm_head" else 1)
+        print(json.dumps({"sweep": "block_rows", "projection": name, "N": N, "K": Kd, "us_1_row": row[1] * 1e3,
+                          "us_16_rows": row[16] * 1e3, "ratio_16_over_1": row[16] / row[1]}), flush=True)
+        del W
+    assert int(st.item()) == 0
+    print(json.dumps({"sweep": "block_rows", "projection": f"all ({cfg.n_layers} layers + LM head)",
+                      "ms_1_row": tot[1], "ms_16_rows": tot[16], "ratio_16_over_1": tot[16] / tot[1]}), flush=True)
+
+
 # --------------------------------------------------------------------------- main
 
 def main(argv=None):
@@ -535,6 +616,9 @@ def main(argv=None):
         cfg = cfg.replace(n_layers=1, vocab=16384, name=cfg.name + "_1layer_v16k")
     if args.kernel == "gemm":
         run_kernel_gemm(args, cfg)
+        return
+    if args.sweep:
+        run_sweep(args, cfg)
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":
