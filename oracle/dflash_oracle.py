@@ -34,6 +34,10 @@ Readings taken where the pages are silent (each repeated at its function):
   R13 residual / bonus sampling by an exponential race, ties to lowest v
   R14 page allocation: FIFO free list, sequences served in index order
   R15 optional shared pre-RoPE key offset on the injected keys (workload knob)
+  R16 FP8 weights (the Guide's "FP4/FP8 mixed execution" on Blackwell): a
+      projection weight is an e4m3 code per entry and an fp32 scale per
+      output row, W = diag(s) . decode(codes); the drafter's arithmetic is
+      otherwise that of the bf16 workload
 
 Pins (tests/test_oracle_pins.py): closed forms, textbook special cases,
 invariants, brute force and exact enumeration.  There is no worked numeric
@@ -573,6 +577,40 @@ def accept_stochastic_trials(p_rows: np.ndarray, q_rows: Optional[np.ndarray],
 
 
 # ---------------------------------------------------------------------------
+# FP8 (e4m3) weights (R16)
+# ---------------------------------------------------------------------------
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    """Values of 8-bit E4M3 codes (OCP 8-bit floating point, "FP8 E4M3"):
+    sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0
+    holds the subnormals m/8 * 2^-6; no infinities; S.1111.111 is NaN, so the
+    largest finite magnitude is 1.75 * 2^8 = 448."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7 == 1, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(F64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(F64)))
+    out = sign * mag
+    return np.where((e == 15) & ((c & 7) == 7), np.nan, out)
+
+
+def dequantize_weights(w: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
+    """A weight set whose projections are stored as e4m3 codes ("q:<name>",
+    uint8 [rows, cols]) with per-row scales ("s:<name>", fp32 [rows]) ->
+    the same set with "<name>" = s[:, None] * decode(codes) in fp64 (exact:
+    a product of an fp32 and a 4-significant-bit value).  Other entries pass
+    through."""
+    out = {}
+    for k, v in w.items():
+        if k.startswith("q:"):
+            name = k[2:]
+            out[name] = _f64(w["s:" + name])[:, None] * decode_e4m3(v)
+        elif not k.startswith("s:"):
+            out[k] = v
+    return out
+
+
+# ---------------------------------------------------------------------------
 # A whole round for a batch (driver used by tests and the CPU baseline)
 # ---------------------------------------------------------------------------
 
@@ -584,6 +622,8 @@ class OracleDrafter:
     def __init__(self, cfg, weights: Dict[str, np.ndarray], n_pages: int, max_pages_per_seq: int,
                  key_offsets: Optional[np.ndarray] = None, seqs: Optional[Sequence[int]] = None):
         self.cfg = cfg
+        if any(k.startswith("q:") for k in weights):
+            weights = dequantize_weights(weights)
         self.w = {k: _f64(v) for k, v in weights.items()}
         self.key_offsets = key_offsets
         B = cfg.batch if seqs is None else len(seqs)

@@ -34,7 +34,7 @@ __all__ = [
     "round_to_bf16", "bf16_bits", "make_weights", "make_ctx_lens",
     "make_prefill_features", "make_round_features", "make_key_offsets",
     "make_target_tokens", "make_target_match", "make_target_logits", "make_draft_tokens",
-    "make_draft_probs", "weight_names",
+    "make_draft_probs", "weight_names", "quantize_e4m3_rows", "PROJECTIONS",
 ]
 
 
@@ -66,6 +66,7 @@ class DraftConfig:
     rms_eps: float = 1.0e-6
     key_offset_std: float = 0.0  # >0: shared pre-RoPE key offset on even kv heads
     weight_std: float = 0.02
+    weight_format: str = "bf16"  # "bf16" | "e4m3": projection weights as FP8 codes + per-row scales
 
     @property
     def mask_id(self) -> int:
@@ -102,6 +103,11 @@ CONFIGS: Dict[str, DraftConfig] = {
                       n_layers=5, hidden=4096, n_q_heads=32, n_kv_heads=8,
                       head_dim=128, ffn=12288, vocab=151936, n_taps=5,
                       tap_width=4096, match_prob=0.85, rounds=8, seed=1002),
+    # c2 with FP8 (e4m3, per-row scale) projection weights: half the weight bytes
+    "c2w8": DraftConfig("c2_qwen3_8b_shaped_fp8w", batch=1, ctx_lo=2048, ctx_hi=2048,
+                        n_layers=5, hidden=4096, n_q_heads=32, n_kv_heads=8,
+                        head_dim=128, ffn=12288, vocab=151936, n_taps=5,
+                        tap_width=4096, match_prob=0.85, rounds=8, seed=1006, weight_format="e4m3"),
     "c3": DraftConfig("c3_serving_batch32", batch=32, ctx_lo=512, ctx_hi=4096,
                       n_layers=5, hidden=4096, n_q_heads=32, n_kv_heads=8,
                       head_dim=128, ffn=12288, vocab=151936, n_taps=5,
@@ -139,6 +145,11 @@ MINI_CONFIGS: Dict[str, DraftConfig] = {
                           hidden=512, n_q_heads=8, n_kv_heads=8, head_dim=64,
                           ffn=1024, vocab=3000, n_taps=2, tap_width=512,
                           match_prob=0.8, rounds=3, seed=2004),
+    # FP8 projection weights (e4m3 + per-row scales), otherwise like mini_a
+    "mini_w8": DraftConfig("mini_w8", batch=3, ctx_lo=9, ctx_hi=260, n_layers=2,
+                           hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                           ffn=1320, vocab=5000, n_taps=3, tap_width=448,
+                           match_prob=0.8, rounds=3, seed=2005, weight_format="e4m3"),
     # fp32 mini: ragged, several pages, G = 2
     "mini_f32": DraftConfig("mini_f32", batch=2, ctx_lo=17, ctx_hi=90, n_layers=2,
                             hidden=192, n_q_heads=6, n_kv_heads=3, head_dim=32,
@@ -211,6 +222,9 @@ def _weight_shape(cfg: DraftConfig, name: str):
     }[base]
 
 
+PROJECTIONS = ("w_fc", "w_lm", "w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down")
+
+
 def _one_weight(cfg: DraftConfig, idx: int, name: str) -> np.ndarray:
     shape = _weight_shape(cfg, name)
     if name.split(".")[0].startswith("g_"):
@@ -218,20 +232,55 @@ def _one_weight(cfg: DraftConfig, idx: int, name: str) -> np.ndarray:
     return _normal(cfg, shape, cfg.weight_std, 1, idx)
 
 
+def quantize_e4m3_rows(w: np.ndarray):
+    """Storage format of the FP8-weight workloads (input preparation, not
+    part of the method): per output row the fp32 scale s = max|w_row| / 448
+    (448 = the largest E4M3 magnitude) and the E4M3 codes of w_row / s,
+    rounded to nearest even by PyTorch's float8_e4m3fn cast.  Returns
+    (codes uint8 [rows, cols], scales fp32 [rows]); an all-zero row gets
+    scale 1 and zero codes."""
+    import torch
+    amax = np.abs(w).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    t = torch.from_numpy(np.ascontiguousarray(w / scale[:, None], dtype=np.float32))
+    codes = t.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    return codes, scale
+
+
+def _one_weight_e4m3(cfg: DraftConfig, idx: int, name: str):
+    shape = _weight_shape(cfg, name)
+    w = _rng(cfg, 1, idx).standard_normal(size=shape, dtype=np.float32) * np.float32(cfg.weight_std)
+    return quantize_e4m3_rows(w)
+
+
 def make_weights(cfg: DraftConfig, threads: Optional[int] = None) -> Dict[str, np.ndarray]:
     """All drafter weights as fp32 arrays (bf16-exact values for bf16 workloads).
 
     Layout: every matrix is [out_features, in_features], row-major.
     Keys: w_fc, g_fc, embed, g_final, w_lm and per layer l: w_q.l, w_k.l, w_v.l,
-    w_o.l, w_gate.l, w_up.l, w_down.l, g_in.l, g_post.l.
+    w_o.l, w_gate.l, w_up.l, w_down.l, g_in.l, g_post.l.  With
+    weight_format "e4m3" every projection <name> (w_fc, w_lm and the per-layer
+    w_q ... w_down) comes instead as "q:<name>" (E4M3 codes, uint8) and
+    "s:<name>" (fp32 per-row scales) from the same N(0, std) draw
+    (quantize_e4m3_rows); the embedding and the gains stay as they are.
     """
     names = weight_names(cfg)
     threads = threads or min(16, os.cpu_count() or 1)
     out: Dict[str, np.ndarray] = {}
+    fp8 = cfg.weight_format == "e4m3"
     with _fut.ThreadPoolExecutor(max_workers=threads) as ex:
-        futs = {ex.submit(_one_weight, cfg, i, n): n for i, n in enumerate(names)}
+        futs = {}
+        for i, n in enumerate(names):
+            if fp8 and n.split(".")[0] in PROJECTIONS:
+                futs[ex.submit(_one_weight_e4m3, cfg, i, n)] = n
+            else:
+                futs[ex.submit(_one_weight, cfg, i, n)] = n
         for f in futs:
-            out[futs[f]] = f.result()
+            n = futs[f]
+            if fp8 and n.split(".")[0] in PROJECTIONS:
+                out["q:" + n], out["s:" + n] = f.result()
+            else:
+                out[n] = f.result()
     return out
 
 

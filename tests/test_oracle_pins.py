@@ -499,3 +499,47 @@ def test_stochastic_accept_special_cases():
     tau_g, em_g, _ = O.accept_greedy(d3, y)
     np.testing.assert_array_equal(tau_s, tau_g)
     np.testing.assert_array_equal(em_s, em_g)
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) weights
+
+def test_e4m3_decode_matches_the_library_cast_on_every_code():
+    """All 256 codes against PyTorch's float8_e4m3fn -> float32 conversion
+    (an independent implementation of the same format)."""
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+    ours = O.decode_e4m3(codes)
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    ok = ~np.isnan(lib)
+    np.testing.assert_array_equal(ours[ok], lib[ok])
+
+
+def test_e4m3_decode_closed_forms():
+    d = O.decode_e4m3
+    assert d(np.uint8(0x38)) == 1.0            # exponent field 7 = bias: 2^0
+    assert d(np.uint8(0xB8)) == -1.0           # sign bit
+    assert d(np.uint8(0x7E)) == 448.0          # largest finite: 1.75 * 2^8
+    assert d(np.uint8(0x08)) == 2.0 ** -6      # smallest normal
+    assert d(np.uint8(0x01)) == 2.0 ** -9      # smallest subnormal: 1/8 * 2^-6
+    assert d(np.uint8(0x07)) == 7 * 2.0 ** -9  # largest subnormal
+    assert d(np.uint8(0x00)) == 0.0 and d(np.uint8(0x80)) == 0.0
+    assert np.isnan(d(np.uint8(0x7F))) and np.isnan(d(np.uint8(0xFF)))
+    # positive codes 0..126 are strictly increasing, and negation flips the sign bit
+    pos = d(np.arange(127, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)
+    np.testing.assert_array_equal(d(np.arange(128, 255, dtype=np.uint8)), -pos)
+
+
+def test_dequantized_weights_scale_each_output_row():
+    """W = diag(s) . decode(codes): a row scale multiplies exactly that
+    output feature of x . W^T."""
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 256, size=(5, 7)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38          # no NaN codes
+    s = np.array([1.0, 0.5, 2.0, 0.25, 3.0], np.float32)
+    w = O.dequantize_weights({"q:w_o.0": codes, "s:w_o.0": s, "g_in.0": np.ones(7, np.float32)})
+    assert set(w) == {"w_o.0", "g_in.0"}
+    x = rng.standard_normal((3, 7))
+    y1 = x @ O.decode_e4m3(codes).T
+    np.testing.assert_allclose(x @ w["w_o.0"].T, y1 * s.astype(np.float64), rtol=1e-15, atol=0)
