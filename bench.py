@@ -46,6 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rounds", type=int, default=4, help="oracle rounds timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay leg")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight leg of the default workload")
     ap.add_argument("--sweep", action="store_true",
                     help="draft-cost sweeps (1/3/5 draft layers; projections on 1 vs 16 rows), JSON line per item")
     ap.add_argument("--reset-every", type=int, default=16,
@@ -189,15 +190,20 @@ def algorithmic_bytes(cfg):
     B, d, F, V, L = cfg.batch, cfg.hidden, cfg.ffn, cfg.vocab, cfg.n_layers
     qd, kvd = cfg.q_dim, cfg.kv_dim
     M = B * K_BLOCK
+    w8 = cfg.weight_format == "e4m3"
+    wb = 1 if w8 else 2                       # weight bytes per entry (E4M3 codes: 1, plus a 4-byte row scale)
+
+    def wbytes(N, Kd):
+        return N * Kd * wb + (4 * N if w8 else 0)
 
     def proj(N, Kd, m=M):
-        return N * Kd * 2 + m * Kd * 4 + m * N * 4
+        return wbytes(N, Kd) + m * Kd * 4 + m * N * 4
 
     Fp = 64 * -(-F // 64)                     # gate/up rows are packed in groups of 64
     per_layer = proj(qd + 2 * kvd, d) + proj(d, qd) + proj(2 * Fp, d) + proj(d, F)
     return {"proj": L * per_layer * cfg.s_passes,
-            "lm_head": (V * d * 2 + M * d * 4) * cfg.s_passes,
-            "inject_weights": d * cfg.feat_dim * 2 + 2 * L * kvd * d * 2}
+            "lm_head": (wbytes(V, d) + M * d * 4) * cfg.s_passes,
+            "inject_weights": wbytes(d, cfg.feat_dim) + wbytes(2 * L * kvd, d)}
 
 
 def kv_bytes(cfg, ctx_len):
@@ -338,7 +344,7 @@ def run_ours(args, cfg, world, rank, local):
     assert wl.dr.device_status() == 0
     launches_per_step = sum(v[1] for v in prof.values()) / args.steps
     # ---- e2e: host buffers through the public API, copies inside the region
-    e2e = run_e2e(wl, args, device)
+    e2e = run_e2e(wl, args, device) if args.e2e_steps > 0 else None
     graph = None if args.no_graph else run_graph(wl, args, device)
     return dict(value=value, ms=ms_max, tokens=tokens, mean_tau=mean_tau, clocks=clocks, prof=prof, ms_b=ms_b,
                 launches_per_step=launches_per_step, e2e=e2e, graph=graph, wl=wl)
@@ -483,7 +489,8 @@ def run_reference(args, cfg, world, rank):
 
 
 def config_block(cfg, lens):
-    return {"workload": cfg.name, "batch": cfg.batch, "context": int(lens.max()), "block_k": K_BLOCK,
+    return {"workload": cfg.name, "weights": "e4m3 codes + fp32 row scales" if cfg.weight_format == "e4m3" else "bf16",
+            "batch": cfg.batch, "context": int(lens.max()), "block_k": K_BLOCK,
             "s_passes": cfg.s_passes, "draft_layers": cfg.n_layers, "hidden": cfg.hidden,
             "heads": f"{cfg.n_q_heads}/{cfg.n_kv_heads}x{cfg.head_dim}", "ffn": cfg.ffn, "vocab": cfg.vocab,
             "taps": f"{cfg.n_taps}x{cfg.tap_width}", "accept": cfg.accept, "match_prob": cfg.match_prob,
@@ -607,6 +614,56 @@ def run_sweep(args, cfg):
                       "ms_1_row": tot[1], "ms_16_rows": tot[16], "ratio_16_over_1": tot[16] / tot[1]}), flush=True)
 
 
+def roofline_block(cfg, res, args, hbm, peak_kind):
+    """The dominant kernel's roofline (k_gemm_tc: projections + LM head) and
+    the per-class figures, from the profiled (second) timed region."""
+    ab = algorithmic_bytes(cfg)
+    lens = res["wl"].lens
+    prof = res["prof"]
+    steps = args.steps
+    gemm_ms = prof["proj"][0] + prof["lm_head"][0]
+    gemm_launches = prof["proj"][1] + prof["lm_head"][1]
+    gemm_bytes = (ab["proj"] + ab["lm_head"]) * steps
+    achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
+    per_class = {k: {"ms_per_step": v[0] / steps, "launches_per_step": v[1] / steps} for k, v in prof.items()}
+    # the context grows by tau+1 per round and is rolled back every reset_every rounds
+    mean_ctx = float(lens.mean()) + 0.5 * max(args.reset_every, 1) * (res["mean_tau"] + 1)
+    attn_bytes = kv_bytes(cfg, int(mean_ctx)) * steps
+    if prof["attention"][0] > 0:
+        per_class["attention"]["GB_per_s"] = attn_bytes / (prof["attention"][0] / 1e3) / 1e9
+    per_class["proj"]["GB_per_s"] = ab["proj"] * steps / (prof["proj"][0] / 1e3) / 1e9
+    per_class["lm_head"]["GB_per_s"] = ab["lm_head"] * steps / (prof["lm_head"][0] / 1e3) / 1e9
+    inj_bytes = ab["inject_weights"] * steps
+    if prof["inject"][0] > 0:
+        per_class["inject"]["GB_per_s"] = inj_bytes / (prof["inject"][0] / 1e3) / 1e9
+    roof = {"kernel": "k_gemm_tc (tcgen05 projections + LM head)", "bound": "hbm",
+            "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "peak_kind": f"{peak_kind} hbm_gbs", "traffic": gemm_traffic(cfg),
+            "traffic_unit": "bytes per launch (ncu dram read+write; profiles/k_gemm_tc_c2_layer.md)",
+            "algorithmic_bytes_per_launch": (ab["proj"] + ab["lm_head"]) * steps / max(gemm_launches, 1),
+            "bytes_per_step": ab["proj"] + ab["lm_head"], "launches_per_step": gemm_launches / steps,
+            "timed_in": "second timed region of the same loop, per-launch CUDA events"}
+    return roof, per_class
+
+
+def run_fp8_leg(args, world, rank, local, hbm, peak_kind):
+    """The same workload with FP8 (E4M3, per-row scale) projection weights:
+    its own rounds, timed the same way (no e2e or graph legs)."""
+    import torch
+    cfg8 = synth.CONFIGS["c2w8"]
+    a8 = argparse.Namespace(**vars(args))
+    a8.no_graph = True
+    a8.e2e_steps = 0
+    torch.cuda.empty_cache()
+    res = run_ours(a8, cfg8, world, rank, local)
+    roof, per_class = roofline_block(cfg8, res, a8, hbm, peak_kind)
+    roof.pop("traffic_unit")
+    roof["traffic"] = None
+    return {"workload": cfg8.name, "value": res["value"], "unit": UNIT, "ms_per_step": res["ms"] / args.steps,
+            "mean_tau": res["mean_tau"], "roofline": roof,
+            "kernels": {k: v for k, v in per_class.items() if k in ("proj", "lm_head", "inject")}}
+
+
 # --------------------------------------------------------------------------- main
 
 def main(argv=None):
@@ -628,25 +685,12 @@ def main(argv=None):
     if rank != 0:
         return
     hbm, tc, peak_kind = load_peaks()
-    ab = algorithmic_bytes(cfg)
-    lens = res["wl"].lens
-    prof = res["prof"]
     steps = args.steps
-    gemm_ms = prof["proj"][0] + prof["lm_head"][0]
-    gemm_launches = prof["proj"][1] + prof["lm_head"][1]
-    gemm_bytes = (ab["proj"] + ab["lm_head"]) * steps
-    achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
-    per_class = {k: {"ms_per_step": v[0] / steps, "launches_per_step": v[1] / steps} for k, v in prof.items()}
-    # the context grows by tau+1 per round and is rolled back every reset_every rounds
-    mean_ctx = float(lens.mean()) + 0.5 * max(args.reset_every, 1) * (res["mean_tau"] + 1)
-    attn_bytes = kv_bytes(cfg, int(mean_ctx)) * steps
-    if prof["attention"][0] > 0:
-        per_class["attention"]["GB_per_s"] = attn_bytes / (prof["attention"][0] / 1e3) / 1e9
-    per_class["proj"]["GB_per_s"] = ab["proj"] * steps / (prof["proj"][0] / 1e3) / 1e9
-    per_class["lm_head"]["GB_per_s"] = ab["lm_head"] * steps / (prof["lm_head"][0] / 1e3) / 1e9
-    inj_bytes = ab["inject_weights"] * steps
-    if prof["inject"][0] > 0:
-        per_class["inject"]["GB_per_s"] = inj_bytes / (prof["inject"][0] / 1e3) / 1e9
+    lens = res["wl"].lens
+    roof, per_class = roofline_block(cfg, res, args, hbm, peak_kind)
+    fp8 = None
+    if not args.no_fp8 and cfg.name == synth.CONFIGS["c2"].name and world == 1:
+        fp8 = run_fp8_leg(args, world, rank, local, hbm, peak_kind)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(cfg, args, res["wl"].w_np)
@@ -656,17 +700,12 @@ def main(argv=None):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights, N(0,1) features)",
         "config": dict(config_block(cfg, lens), mean_tau=res["mean_tau"], parallelism=f"replicas x{world}",
                        synthetic_target="one torch elementwise op per step forms y from the drafts; inside the region"),
-        "roofline": {"kernel": "k_gemm_tc (tcgen05 projections + LM head)", "bound": "hbm",
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_kind": f"{peak_kind} hbm_gbs", "traffic": gemm_traffic(cfg),
-                     "traffic_unit": "bytes per launch (ncu dram read+write; profiles/k_gemm_tc_c2_layer.md)",
-                     "algorithmic_bytes_per_launch": (ab["proj"] + ab["lm_head"]) * steps / max(gemm_launches, 1),
-                     "bytes_per_step": ab["proj"] + ab["lm_head"], "launches_per_step": gemm_launches / steps,
-                     "timed_in": "second timed region of the same loop, per-launch CUDA events"},
+        "roofline": roof,
         "kernels": per_class,
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
         "graph": res["graph"],
+        "fp8_weights": fp8,
         "gpu_launches": int(round(res["launches_per_step"] * steps)),
         "clocks": res["clocks"],
     }

@@ -17,13 +17,14 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "pool
                 7: "too large for the fixed scratch", 8: "not allowed while capturing"}
 ROUND_DEVICE = (1 << 64) - 1   # dflash_accept: take the round from the device counter
 DEV_POOL_EXHAUSTED, DEV_SEQ_TOO_LONG, DEV_WAIT_TIMEOUT, DEV_BAD_TOKEN, DEV_BAD_ROWS = 1, 2, 4, 8, 16
-DTYPE_F32, DTYPE_BF16 = 0, 1
+DTYPE_F32, DTYPE_BF16, DTYPE_BF16_W8 = 0, 1, 2
 
 EXPORTED = ("dflash_workspace_size", "dflash_kv_pool_size", "dflash_create", "dflash_destroy",
             "dflash_reset", "dflash_release", "dflash_inject_kv", "dflash_draft_block",
             "dflash_accept", "dflash_get_status", "dflash_status_string", "dflash_gemm_bf16",
             "dflash_profile_enable", "dflash_profile_read", "dflash_truncate", "dflash_gemm_bf16_noalloc",
-            "dflash_graph_begin", "dflash_graph_end", "dflash_graph_launch", "dflash_graph_destroy")
+            "dflash_graph_begin", "dflash_graph_end", "dflash_graph_launch", "dflash_graph_destroy",
+            "dflash_gemm_w8")
 PROF_CLASSES = ("proj", "lm_head", "inject", "attention", "rowwise", "accept")
 
 
@@ -43,7 +44,9 @@ class DflashWeights(ctypes.Structure):
     _fields_ = [("w_fc", _VP), ("g_fc", _VP), ("embed", _VP), ("g_final", _VP), ("w_lm", _VP),
                 ("w_kv_inject", _VP), ("key_offset", _VP),
                 ("w_qkv", _PVP), ("w_o", _PVP), ("w_gu", _PVP), ("w_down", _PVP),
-                ("g_in", _PVP), ("g_post", _PVP)]
+                ("g_in", _PVP), ("g_post", _PVP),
+                ("s_fc", _VP), ("s_lm", _VP), ("s_kv_inject", _VP),
+                ("s_qkv", _PVP), ("s_o", _PVP), ("s_gu", _PVP), ("s_down", _PVP)]
 
 
 _lib = None
@@ -86,6 +89,9 @@ def lib() -> ctypes.CDLL:
         L.dflash_gemm_bf16.restype = ctypes.c_int
         L.dflash_gemm_bf16.argtypes = [_VP, ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int, _VP, ctypes.c_int,
                                        ctypes.POINTER(ctypes.c_int), _VP, _VP]
+        L.dflash_gemm_w8.restype = ctypes.c_int
+        L.dflash_gemm_w8.argtypes = [_VP, _VP, ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int, _VP, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_int), _VP, _VP]
         L.dflash_gemm_bf16_noalloc.restype = ctypes.c_int
         L.dflash_gemm_bf16_noalloc.argtypes = [_VP, ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int, _VP,
                                                ctypes.c_int, ctypes.POINTER(ctypes.c_int), _VP, _VP]

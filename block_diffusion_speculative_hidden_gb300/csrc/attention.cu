@@ -156,7 +156,7 @@ __global__ void k_attn_combine(const float* __restrict__ part_o, const float* __
 // Key splits per (sequence, kv head): enough CTAs for about two per SM; the
 // tensor-core kernel merges its splits inside one cluster (at most 16).
 int attn_splits(dflash_ctx* c, int B) {
-  if (c->cfg.dtype == DFLASH_BF16) return attention_mma_splits(c, B);
+  if (c->cfg.dtype != DFLASH_F32) return attention_mma_splits(c, B);
   const int heads = B * c->cfg.n_kv_heads;
   const int s = (2 * c->num_sms + heads - 1) / heads;
   return std::max(1, std::min(s, c->attn_max_splits));
@@ -212,7 +212,7 @@ static cudaError_t launch_attn_ty(dflash_ctx* c, int layer, int B, int splits, c
 // fp32 workloads: the fp32 SIMT kernel above; bf16 workloads (fp16 pool):
 // the tcgen05 kernel of attention_mma.cu.
 cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next) {
-  if (c->cfg.dtype == DFLASH_BF16) return launch_attention_mma(c, layer, B, splits, s, next);
+  if (c->cfg.dtype != DFLASH_F32) return launch_attention_mma(c, layer, B, splits, s, next);
   return launch_attn_ty<float>(c, layer, B, splits, s);
 }
 

@@ -249,6 +249,62 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, bf16 inputs, fp32 accumulator.  A
+// (M = 128 rows x 16 k) sits in TMEM: row i in lane i, k-pairs packed into
+// 32-bit columns (element 2j in the low half of column j).
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns from registers; lane i of the warp
+// writes TMEM lane (taddr.lane + i).  The warp must be converged; call
+// tc_wait_st() before signalling that the columns are written.
+__device__ __forceinline__ void tc_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns from registers (as tc_st_32x32b_x32).
+__device__ __forceinline__ void tc_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Four E4M3 codes (bytes of q, lowest byte first) -> four bf16 values as two
+// bf16x2 words (lower code in the low half).  A code c = s.eeee.mmm becomes
+// the bf16 bit pattern s at bit 15 and eeee.mmm at bits 4-10: a bf16 with
+// exponent field eeee and mantissa mmm0000, whose value is exactly the
+// code's value times 2^-120 (bf16's exponent bias is 127, E4M3's 7, and
+// bf16's subnormals line up with E4M3's: m/8 * 2^-126 against m/8 * 2^-6).
+// One bf16 multiply by 2^120 then restores the value; it is exact, since the
+// result has 4 significant bits and lies in bf16's normal range.  Integer
+// and bf16x2 instructions only, no conversion instructions.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t q, uint32_t& w0, uint32_t& w1) {
+  const uint32_t x0 = __byte_perm(q, 0u, 0x1404);  // bytes [0, c0, 0, c1]
+  const uint32_t x1 = __byte_perm(q, 0u, 0x3424);  // bytes [0, c2, 0, c3]
+  const uint32_t y0 = ((x0 & 0x7F007F00u) >> 4) | (x0 & 0x80008000u);
+  const uint32_t y1 = ((x1 & 0x7F007F00u) >> 4) | (x1 & 0x80008000u);
+  constexpr uint32_t k2p120 = 0x7B807B80u;  // bf16x2 {2^120, 2^120}
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w0) : "r"(y0), "r"(k2p120));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w1) : "r"(y1), "r"(k2p120));
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

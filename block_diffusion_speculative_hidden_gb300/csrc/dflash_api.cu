@@ -38,23 +38,26 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-int elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 4; }
+// bytes of an activation / feature element: bf16 for DFLASH_BF16 and
+// DFLASH_BF16_W8 (whose E4M3 weights are one byte), fp32 otherwise
+int elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_F32 ? 4 : 2; }
 // q and the KV pool: fp16 for bf16 workloads, fp32 for fp32 workloads
-int kv_elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_BF16 ? 2 : 4; }
+int kv_elem_bytes(const dflash_config& g) { return g.dtype == DFLASH_F32 ? 4 : 2; }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Split count of one draft-side GEMM for M activation rows (hi/lo inputs).
 int draft_splits(const dflash_config& g, int M, int N, int K, int num_sms, int max_ctas = 0) {
-  if (g.dtype != DFLASH_BF16) return 1;
-  const int bn = gemm_bn(M, true);
-  return gemm_splits(ceil_div(N, kTileN) * ceil_div(M, bn), gemm_kb(K), bn, true, num_sms, max_ctas);
+  if (g.dtype == DFLASH_F32) return 1;
+  const int bn = gemm_bn(M, true, g.dtype == DFLASH_BF16_W8);
+  return gemm_splits(ceil_div(N, kTileN) * ceil_div(M, bn), gemm_kb(K), bn, true, num_sms, max_ctas,
+                     g.dtype == DFLASH_BF16_W8);
 }
 // Split count of an inject-side GEMM: independent of the row count (sized
 // for a 32-row tile), so a row's result does not depend on how many rows
 // share the call.
 int inject_splits(const dflash_config& g, int N, int K, bool split, int num_sms) {
-  if (g.dtype != DFLASH_BF16) return 1;
-  return gemm_splits(ceil_div(N, kTileN), gemm_kb(K), 32, split, num_sms);
+  if (g.dtype == DFLASH_F32) return 1;
+  return gemm_splits(ceil_div(N, kTileN), gemm_kb(K), 32, split, num_sms, 0, g.dtype == DFLASH_BF16_W8);
 }
 
 // Rows of the packed gate/up weight: groups of 64 features, 64 gate rows then
@@ -69,21 +72,22 @@ int attn_max_splits_for(const dflash_config& g, int num_sms) {
 
 bool config_ok(const dflash_config* g) {
   if (g == nullptr) return false;
-  if (g->dtype != DFLASH_F32 && g->dtype != DFLASH_BF16) return false;
+  if (g->dtype != DFLASH_F32 && g->dtype != DFLASH_BF16 && g->dtype != DFLASH_BF16_W8) return false;
   if (g->block_k != kBlockK || g->page_size != kPage) return false;
   if (g->n_layers < 1 || g->hidden < 8 || g->n_q_heads < 1 || g->n_kv_heads < 1) return false;
   if (g->n_q_heads % g->n_kv_heads != 0) return false;
   const int G = g->n_q_heads / g->n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return false;
   if (g->head_dim != 32 && g->head_dim != 64 && g->head_dim != 128) return false;
-  if (g->dtype == DFLASH_BF16 && g->head_dim == 32) return false;  // the fp16 attention tiles 64-wide
+  if (g->dtype != DFLASH_F32 && g->head_dim == 32) return false;  // the fp16 attention tiles 64-wide
   if (g->ffn < 8 || g->vocab < 2 || g->mask_id < 0 || g->mask_id >= g->vocab) return false;
   if (g->n_taps < 1 || g->tap_width < 1) return false;
   if (g->max_batch < 1 || g->max_batch > 4096 || g->max_pages_per_seq < 1 || g->n_pages < 1) return false;
   if (g->max_rows < 1 || g->max_inject_rows < g->max_rows) return false;
   if (!(g->rope_theta > 0.f) || !(g->rms_eps >= 0.f)) return false;
   // TMA row strides must be multiples of 16 bytes; vector row copies need 16 bytes
-  const int q = elem_bytes(*g) == 2 ? 8 : 4;
+  // (E4M3 weight rows: one byte an element)
+  const int q = g->dtype == DFLASH_BF16_W8 ? 16 : elem_bytes(*g) == 2 ? 8 : 4;
   const int F = g->n_taps * g->tap_width;
   if (g->hidden % q || F % q || g->ffn % q || (g->n_q_heads * g->head_dim) % q) return false;
   return true;
@@ -125,7 +129,7 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   auto row_src = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
   auto rcos = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
   auto rsin = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
-  const bool lo = g.dtype == DFLASH_BF16;  // GEMM inputs carry a second bf16 term
+  const bool lo = g.dtype != DFLASH_F32;  // GEMM inputs carry a second bf16 term
   void* fc_in = w.take(R * Fin * e);
   void* h_fused = w.take(R * d * e);
   void* h_lo = lo ? w.take(R * d * e) : nullptr;
@@ -204,7 +208,11 @@ int device_sms() {
     if (st_ != DFLASH_OK) return st_; \
   } while (0)
 
-dflash_status run_gemm(dflash_ctx* c, const void* W, int N, int K, const void* X, const void* X_lo, int M,
+// Row scales of layer l's E4M3 projection weights, or null (bf16 weights).
+const float* w_row_scale(const std::vector<const float*>& v, int l) { return v.empty() ? nullptr : v[l]; }
+
+dflash_status run_gemm(dflash_ctx* c, const void* W, const float* w_scale, int N, int K, const void* X,
+                       const void* X_lo, int M,
                        int M_alloc, int splits, const int* m_valid, const EpiArgs& epi, cudaStream_t s,
                        const NextGemm& next = NextGemm{}) {
   GemmLaunch g{};
@@ -215,8 +223,9 @@ dflash_status run_gemm(dflash_ctx* c, const void* W, int N, int K, const void* X
   g.K = K;
   g.M = M;
   g.M_alloc = M_alloc;
-  g.splits = c->cfg.dtype == DFLASH_BF16 ? splits : 1;
-  g.out = c->cfg.dtype == DFLASH_BF16 ? nullptr : c->y;  // fp32 staging (bf16: epilogues write directly)
+  g.splits = c->cfg.dtype != DFLASH_F32 ? splits : 1;
+  g.out = c->cfg.dtype != DFLASH_F32 ? nullptr : c->y;  // fp32 staging (bf16: epilogues write directly)
+  g.w_scale = w_scale;
   g.split_stride = static_cast<long long>(M) * N;
   g.ldo = N;
   g.m_valid = m_valid;
@@ -361,6 +370,14 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, v
     if (w->w_qkv[l] == nullptr || w->w_o[l] == nullptr || w->w_gu[l] == nullptr || w->w_down[l] == nullptr ||
         w->g_in[l] == nullptr || w->g_post[l] == nullptr)
       return DFLASH_ERR_INVALID_ARG;
+  if (cfg->dtype == DFLASH_BF16_W8) {
+    if (w->s_fc == nullptr || w->s_lm == nullptr || w->s_kv_inject == nullptr || w->s_qkv == nullptr ||
+        w->s_o == nullptr || w->s_gu == nullptr || w->s_down == nullptr)
+      return DFLASH_ERR_INVALID_ARG;
+    for (int l = 0; l < cfg->n_layers; ++l)
+      if (w->s_qkv[l] == nullptr || w->s_o[l] == nullptr || w->s_gu[l] == nullptr || w->s_down[l] == nullptr)
+        return DFLASH_ERR_INVALID_ARG;
+  }
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0 || reinterpret_cast<uintptr_t>(kv_pool) % 16 != 0)
     return DFLASH_ERR_INVALID_ARG;
   const int sms = device_sms();
@@ -385,6 +402,15 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, v
   c->w_down.assign(w->w_down, w->w_down + cfg->n_layers);
   c->g_in.assign(w->g_in, w->g_in + cfg->n_layers);
   c->g_post.assign(w->g_post, w->g_post + cfg->n_layers);
+  if (cfg->dtype == DFLASH_BF16_W8) {
+    c->s_fc = w->s_fc;
+    c->s_lm = w->s_lm;
+    c->s_kv_inj = w->s_kv_inject;
+    c->s_qkv.assign(w->s_qkv, w->s_qkv + cfg->n_layers);
+    c->s_o.assign(w->s_o, w->s_o + cfg->n_layers);
+    c->s_gu.assign(w->s_gu, w->s_gu + cfg->n_layers);
+    c->s_down.assign(w->s_down, w->s_down + cfg->n_layers);
+  }
   {
     const char* env = std::getenv("DFLASH_PDL");
     c->pdl = env == nullptr || std::strcmp(env, "0") != 0;
@@ -468,7 +494,7 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t
     EpiArgs e = epi_base(ctx, EPI_STORE, rows, d);
     e.m_valid = ctx->scal;
     norm_out(e, ctx->h_fused, ctx->h_lo, ctx->g_fc, ctx->ss_h, R);
-    DF_RUN(run_gemm(ctx, ctx->w_fc, d, Fin, ctx->fc_in, nullptr, rows, R, s_fc, ctx->scal, e, s));
+    DF_RUN(run_gemm(ctx, ctx->w_fc, ctx->s_fc, d, Fin, ctx->fc_in, nullptr, rows, R, s_fc, ctx->scal, e, s));
   }
   const int s_kv = inject_splits(g, Nkv, d, true, ctx->num_sms);
   {
@@ -484,7 +510,7 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, const void* feats, const int32_t
     e.page_table = ctx->page_table;
     e.max_pages = g.max_pages_per_seq;
     e.key_offset = ctx->key_offset;
-    DF_RUN(run_gemm(ctx, ctx->w_kv_inj, Nkv, d, ctx->h_fused, ctx->h_lo, rows, R, s_kv, ctx->scal, e, s));
+    DF_RUN(run_gemm(ctx, ctx->w_kv_inj, ctx->s_kv_inj, Nkv, d, ctx->h_fused, ctx->h_lo, rows, R, s_kv, ctx->scal, e, s));
   }
   return DFLASH_OK;
 }
@@ -523,10 +549,10 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         e.pool_v = pool_layer(ctx->pool_v, ctx, l);
         e.block_page0 = g.n_pages;
         e.seq_len = ctx->seq_len;
-        DF_RUN(run_gemm(ctx, ctx->w_qkv[l], Nqkv, d, ctx->a, ctx->a_lo, M, Mmax, s_qkv, nullptr, e, s));
+        DF_RUN(run_gemm(ctx, ctx->w_qkv[l], w_row_scale(ctx->s_qkv, l), Nqkv, d, ctx->a, ctx->a_lo, M, Mmax, s_qkv, nullptr, e, s));
       }
       {
-        ProfScope p(ctx, DFLASH_PROF_ATTN, g.dtype == DFLASH_BF16 ? 1 : 2, s);
+        ProfScope p(ctx, DFLASH_PROF_ATTN, g.dtype != DFLASH_F32 ? 1 : 2, s);
         // attention is latency-bound: it streams all of the O projection's
         // weights beyond that kernel's ring into L2
         DF_CHECK(launch_attention(ctx, l, B, a_sp, s, next_gemm(ctx->w_o[l], d, qd, M, s_o, 1ll << 40)));
@@ -536,7 +562,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         EpiArgs e = epi_base(ctx, EPI_RESIDUAL, M, d);
         e.out = ctx->x;
         norm_out(e, ctx->a, ctx->a_lo, ctx->g_post[l], ctx->ss_x, Mmax);
-        DF_RUN(run_gemm(ctx, ctx->w_o[l], d, qd, ctx->o, ctx->o_lo, M, Mmax, s_o, nullptr, e, s));
+        DF_RUN(run_gemm(ctx, ctx->w_o[l], w_row_scale(ctx->s_o, l), d, qd, ctx->o, ctx->o_lo, M, Mmax, s_o, nullptr, e, s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
@@ -545,23 +571,24 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         e.act_hi = ctx->act;
         e.act_lo = ctx->act_lo;
         e.F = F;
-        DF_RUN(run_gemm(ctx, ctx->w_gu[l], Ngu, d, ctx->a, ctx->a_lo, M, Mmax, s_gu, nullptr, e, s));
+        DF_RUN(run_gemm(ctx, ctx->w_gu[l], w_row_scale(ctx->s_gu, l), Ngu, d, ctx->a, ctx->a_lo, M, Mmax, s_gu, nullptr, e, s));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);
         EpiArgs e = epi_base(ctx, EPI_RESIDUAL, M, d);
         e.out = ctx->x;
         norm_out(e, ctx->a, ctx->a_lo, l + 1 < g.n_layers ? ctx->g_in[l + 1] : ctx->g_final, ctx->ss_x, Mmax);
-        DF_RUN(run_gemm(ctx, ctx->w_down[l], d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, e, s));
+        DF_RUN(run_gemm(ctx, ctx->w_down[l], w_row_scale(ctx->s_down, l), d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, e, s));
       }
     }
     EpiArgs fin = epi_base(ctx, EPI_NONE, M, g.vocab);  // the final norm, folded into the LM head
     norm_in(ctx, fin, ctx->ss_x, Mmax);
     const int32_t* skip = pass == 1 ? ctx->commit : nullptr;
-    ProfScope plm(ctx, DFLASH_PROF_LMHEAD, g.dtype == DFLASH_BF16 ? 1 : 2, s);
-    if (g.dtype == DFLASH_BF16) {
+    ProfScope plm(ctx, DFLASH_PROF_LMHEAD, g.dtype != DFLASH_F32 ? 1 : 2, s);
+    if (g.dtype != DFLASH_F32) {
       GemmLaunch lm{};
       lm.W = ctx->w_lm;
+      lm.w_scale = ctx->s_lm;
       lm.X = ctx->a;
       lm.X_lo = ctx->a_lo;
       lm.N = g.vocab;
@@ -660,6 +687,38 @@ dflash_status dflash_gemm_bf16(const void* W, int N, int K, const void* X, const
   g.out = out;
   g.split_stride = static_cast<long long>(M) * N;
   g.ldo = N;
+  DF_CHECK(gemm_launch(&tmp, g, stream));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_gemm_w8(const void* W, const float* w_scale, int N, int K, const void* X, const void* X_lo, int M, float* out,
+                               int splits, int* splits_used, int* status, dflash_stream stream) {
+  if (W == nullptr || w_scale == nullptr || X == nullptr || out == nullptr || status == nullptr || N < 1 || K < 16 ||
+      K % 16 || M < 1 || splits < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(W) % 16 || reinterpret_cast<uintptr_t>(X) % 16 ||
+      reinterpret_cast<uintptr_t>(X_lo) % 16)
+    return DFLASH_ERR_INVALID_ARG;
+  dflash_ctx tmp;
+  tmp.cfg = dflash_config{};
+  tmp.cfg.dtype = DFLASH_BF16_W8;
+  tmp.status = status;
+  const int n_kb = gemm_kb(K);
+  const int s_used = gemm_normalize_splits(n_kb, std::min(splits, n_kb), true);
+  if (splits_used != nullptr) *splits_used = s_used;
+  GemmLaunch g{};
+  g.W = W;
+  g.X = X;
+  g.X_lo = X_lo;
+  g.N = N;
+  g.K = K;
+  g.M = M;
+  g.M_alloc = M;
+  g.splits = s_used;
+  g.out = out;
+  g.split_stride = static_cast<long long>(M) * N;
+  g.ldo = N;
+  g.w_scale = w_scale;
   DF_CHECK(gemm_launch(&tmp, g, stream));
   return DFLASH_OK;
 }

@@ -118,6 +118,9 @@ constexpr int kEpiBatch = 8;  // rows finished together (their loads in flight a
 // kEpiBatch of its rows at a time.
 constexpr int kEpiThreads = 128;
 __device__ __forceinline__ constexpr int epi_phases() { return kEpiThreads / 128; }
+// The epilogue's threads (the first kEpiThreads of the block) meet at named
+// barrier 1, so a kernel may have other warps that take no part in it.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
 
 // Global inputs of the first kEpiBatch rows a thread finishes, loaded ahead
 // of the epilogue so that their latency overlaps the accumulator readout and
@@ -179,8 +182,8 @@ __device__ __forceinline__ void epilogue_preload(const EpiArgs& e, int m0, int r
   }
 }
 
-// Finishes one tile.  All kEpiThreads threads of the block call it (128 or
-// 256, see above).  `rs` (nullable) holds the row scales of rows
+// Finishes one tile.  The first kEpiThreads threads of the block call it
+// (see above).  `rs` (nullable) holds the row scales of rows
 // m0 .. m0 + rows - 1 and `ri` (nullable) their epi_row_info; `scratch`
 // holds 4 * rows floats and is used when e.ss_out is set; `pre` (nullable)
 // holds each thread's first batch of global inputs (epilogue_preload).
@@ -250,7 +253,7 @@ __device__ void apply_epilogue(const EpiArgs& e, const float* tile, int m0, int 
         }
       }
       if (e.ss_out != nullptr) {
-        __syncthreads();
+        epi_sync();
         for (int j = threadIdx.x; j < rows; j += kEpiThreads)
           e.ss_out[static_cast<long long>(n0 >> 7) * e.ss_ld + m0 + j] =
               (scratch[j * 4 + 0] + scratch[j * 4 + 1]) + (scratch[j * 4 + 2] + scratch[j * 4 + 3]);

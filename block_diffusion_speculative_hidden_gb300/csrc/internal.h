@@ -55,11 +55,13 @@ struct GemmLaunch {
   long long ld_logits;
   const int* skip_rows;  // nullable: rows whose logits are not stored
   NextGemm next;         // the projection after this one (L2 prefetch of its weights)
+  const float* w_scale;  // E4M3 weights (DFLASH_BF16_W8): fp32 scale of every weight row [N]
 };
 
 struct TmapEntry {
   const void* ptr;
   int rows, cols, box_rows;
+  int kind;  // 0 bf16, 1 E4M3 codes
   CUtensorMap map;
 };
 
@@ -78,6 +80,9 @@ struct dflash_ctx {
   const void *w_fc, *g_fc, *embed, *g_final, *w_lm, *w_kv_inj;
   const float* key_offset;
   std::vector<const void*> w_qkv, w_o, w_gu, w_down, g_in, g_post;
+  // DFLASH_BF16_W8: row scales of the E4M3 projection weights (else null)
+  const float *s_fc = nullptr, *s_lm = nullptr, *s_kv_inj = nullptr;
+  std::vector<const float*> s_qkv, s_o, s_gu, s_down;
   // cache
   void *pool_k, *pool_v;
   int32_t *page_table, *seq_len;
@@ -168,12 +173,17 @@ cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 // gemm.cu
 cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
 int gemm_kb(int K);
-int gemm_bn(int M, bool split);
-int gemm_blocks_per_sm(int bn, bool split);
-int gemm_ring_stages(int bn, bool split);
+int gemm_bn(int M, bool split, bool w8 = false);
+int gemm_kb_per_split(int n_kb, int splits, bool w8);
+int gemm_normalize_splits(int n_kb, int splits, bool w8);
+int gemm_blocks_per_sm(int bn, bool split, bool w8);
+int gemm_ring_stages(int bn, bool split, bool w8);
 // The L2 prefetch plan (and the weight tensor map) of projection `nx`.
 bool gemm_l2_plan(dflash_ctx* c, const NextGemm& nx, L2Plan* plan, CUtensorMap* map);
-int gemm_splits(int n_tiles, int n_kb, int bn, bool split, int num_sms, int max_ctas = 0);
+int gemm_splits(int n_tiles, int n_kb, int bn, bool split, int num_sms, int max_ctas = 0, bool w8 = false);
+// gemm_w8.cu: the E4M3-weight variants of the projection kernel
+cudaError_t launch_tc_w8(dflash_ctx* c, const GemmLaunch& g, int bn, const CUtensorMap& tw, const CUtensorMap& tx,
+                         const CUtensorMap& txlo, cudaStream_t s);
 cudaError_t gemm_launch_uncached(int* status, const GemmLaunch& g, cudaStream_t s);
 
 }  // namespace dflash

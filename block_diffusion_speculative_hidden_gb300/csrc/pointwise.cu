@@ -190,7 +190,7 @@ __global__ void k_commit(const float* __restrict__ conf1, int32_t* commit, int B
 
 #define DFLASH_DISPATCH(c, ...)                       \
   do {                                                \
-    if ((c)->cfg.dtype == DFLASH_BF16) {              \
+    if ((c)->cfg.dtype != DFLASH_F32) {               \
       using T = __nv_bfloat16;                        \
       __VA_ARGS__;                                    \
     } else {                                          \

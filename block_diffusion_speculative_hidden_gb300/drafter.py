@@ -28,11 +28,14 @@ def _stream(stream: Optional[torch.cuda.Stream]):
 
 
 def weights_to_device(np_weights: Dict[str, "object"], dtype: str, device="cuda") -> Dict[str, torch.Tensor]:
-    """numpy fp32 arrays (values exact in the target dtype) -> device tensors."""
+    """numpy fp32 arrays (values exact in the target dtype) -> device tensors.
+    E4M3 projection weights ("q:<name>" uint8 codes, "s:<name>" fp32 row
+    scales) keep their types."""
     tdt = _DTYPES[dtype][1]
     out = {}
     for k, v in np_weights.items():
-        out[k] = torch.from_numpy(v).to(device=device).to(tdt).contiguous()
+        t = torch.from_numpy(v).to(device=device)
+        out[k] = (t if k.startswith(("q:", "s:")) else t.to(tdt)).contiguous()
     return out
 
 
@@ -56,6 +59,31 @@ def gemm_bf16(W: torch.Tensor, X: torch.Tensor, splits: int = 1, status: Optiona
     got = ctypes.c_int(0)
     _lib.check(L.dflash_gemm_bf16(_ptr(W), N, K, _ptr(X), _ptr(X_lo), M, _ptr(out), splits, ctypes.byref(got),
                                   _ptr(status), _stream(stream)), "dflash_gemm_bf16")
+    assert got.value == used
+    return out
+
+
+def gemm_w8(W: torch.Tensor, w_scale: torch.Tensor, X: torch.Tensor, splits: int = 1,
+            status: Optional[torch.Tensor] = None, X_lo: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """gemm_bf16 with E4M3 weights: W uint8 codes [N, K], w_scale fp32 [N];
+    out[s] = w_scale * ((X + X_lo) . decode(W)^T over split s's k-blocks).
+    Every split but the last owns an even number of 64-wide k-blocks."""
+    L = _lib.lib()
+    N, K = W.shape
+    M = X.shape[0]
+    assert W.dtype == torch.uint8 and w_scale.dtype == torch.float32 and w_scale.numel() == N
+    assert X.dtype == torch.bfloat16 and X.shape[1] == K and W.is_contiguous() and X.is_contiguous()
+    n_kb = (K + 63) // 64
+    want = min(splits, n_kb)
+    per = (n_kb + want - 1) // want
+    per += per & 1                      # whole pipeline stages (two k-blocks) per split
+    used = (n_kb + per - 1) // per
+    out = torch.empty((used, M, N), dtype=torch.float32, device=W.device)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=W.device)
+    got = ctypes.c_int(0)
+    _lib.check(L.dflash_gemm_w8(_ptr(W), _ptr(w_scale), N, K, _ptr(X), _ptr(X_lo), M, _ptr(out), splits,
+                                ctypes.byref(got), _ptr(status), _stream(stream)), "dflash_gemm_w8")
     assert got.value == used
     return out
 
@@ -109,6 +137,11 @@ class Drafter:
                  key_offset: Optional[torch.Tensor] = None, device: str = "cuda"):
         self.L = _lib.lib()
         dcode, tdt = _DTYPES[shape.dtype]
+        w8 = "q:w_lm" in weights  # E4M3 projection weights with per-row scales
+        if w8:
+            assert shape.dtype == "bf16"
+            dcode = _lib.DTYPE_BF16_W8
+        self.w8 = w8
         self.tdtype = tdt
         self.shape = shape
         self.device = torch.device(device)
@@ -140,19 +173,41 @@ class Drafter:
         w = weights
         self._keep = []
 
-        def keep(t):
-            t = t.to(device=self.device, dtype=tdt).contiguous()
+        def keep(t, dt=tdt):
+            t = t.to(device=self.device, dtype=dt).contiguous()
             self._keep.append(t)
             return t
 
-        w_qkv = [keep(torch.cat([w[f"w_q.{l}"], w[f"w_k.{l}"], w[f"w_v.{l}"]], 0)) for l in range(nl)]
-        w_gu = [keep(pack_gate_up(w[f"w_gate.{l}"], w[f"w_up.{l}"])) for l in range(nl)]
-        w_kv = keep(torch.cat([torch.cat([w[f"w_k.{l}"], w[f"w_v.{l}"]], 0) for l in range(nl)], 0))
-        singles = {k: keep(w[k]) for k in ("w_fc", "g_fc", "embed", "g_final", "w_lm")}
-        w_o = [keep(w[f"w_o.{l}"]) for l in range(nl)]
-        w_dn = [keep(w[f"w_down.{l}"]) for l in range(nl)]
+        # projections: values (bf16 / fp32) or, for E4M3 weights, codes; their
+        # row scales are packed with the same row order
+        pre = "q:" if w8 else ""
+        wdt = torch.uint8 if w8 else tdt
+
+        def pw(name):
+            return w[pre + name]
+
+        def ps(name):
+            return w["s:" + name].reshape(-1, 1)
+
+        w_qkv = [keep(torch.cat([pw(f"w_q.{l}"), pw(f"w_k.{l}"), pw(f"w_v.{l}")], 0), wdt) for l in range(nl)]
+        w_gu = [keep(pack_gate_up(pw(f"w_gate.{l}"), pw(f"w_up.{l}")), wdt) for l in range(nl)]
+        w_kv = keep(torch.cat([torch.cat([pw(f"w_k.{l}"), pw(f"w_v.{l}")], 0) for l in range(nl)], 0), wdt)
+        singles = {k: keep(w[k]) for k in ("g_fc", "embed", "g_final")}
+        singles.update({k: keep(pw(k), wdt) for k in ("w_fc", "w_lm")})
+        w_o = [keep(pw(f"w_o.{l}"), wdt) for l in range(nl)]
+        w_dn = [keep(pw(f"w_down.{l}"), wdt) for l in range(nl)]
         g_in = [keep(w[f"g_in.{l}"]) for l in range(nl)]
         g_post = [keep(w[f"g_post.{l}"]) for l in range(nl)]
+        if w8:
+            f32 = torch.float32
+            s_qkv = [keep(torch.cat([ps(f"w_q.{l}"), ps(f"w_k.{l}"), ps(f"w_v.{l}")], 0).reshape(-1), f32)
+                     for l in range(nl)]
+            s_gu = [keep(pack_gate_up(ps(f"w_gate.{l}"), ps(f"w_up.{l}")).reshape(-1), f32) for l in range(nl)]
+            s_kv = keep(torch.cat([torch.cat([ps(f"w_k.{l}"), ps(f"w_v.{l}")], 0) for l in range(nl)], 0).reshape(-1),
+                        f32)
+            s_fc, s_lm = keep(w["s:w_fc"], f32), keep(w["s:w_lm"], f32)
+            s_o = [keep(w[f"s:w_o.{l}"], f32) for l in range(nl)]
+            s_dn = [keep(w[f"s:w_down.{l}"], f32) for l in range(nl)]
         self.key_offset = None
         if key_offset is not None:
             self.key_offset = key_offset.to(device=self.device, dtype=torch.float32).contiguous()
@@ -172,6 +227,9 @@ class Drafter:
         wt.key_offset = None if self.key_offset is None else self.key_offset.data_ptr()
         wt.w_qkv, wt.w_o, wt.w_gu, wt.w_down = arr(w_qkv), arr(w_o), arr(w_gu), arr(w_dn)
         wt.g_in, wt.g_post = arr(g_in), arr(g_post)
+        if w8:
+            wt.s_fc, wt.s_lm, wt.s_kv_inject = s_fc.data_ptr(), s_lm.data_ptr(), s_kv.data_ptr()
+            wt.s_qkv, wt.s_o, wt.s_gu, wt.s_down = arr(s_qkv), arr(s_o), arr(s_gu), arr(s_dn)
         self._wt = wt
         ctx = ctypes.c_void_p()
         _lib.check(self.L.dflash_create(ctypes.byref(cfg), ctypes.byref(wt), _ptr(self.kv_pool), pool,

@@ -70,7 +70,19 @@ typedef enum {
 #define DFLASH_DEV_BAD_TOKEN 8      /* a token id outside [0, vocab) */
 #define DFLASH_DEV_BAD_ROWS 16      /* an n_rows entry outside [0, max_rows] */
 
-typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
+/* DFLASH_BF16_W8: DFLASH_BF16 with FP8 projection weights.  Every projection
+ * weight (w_fc, w_kv_inject, w_qkv, w_o, w_gu, w_down, w_lm) is one E4M3 code
+ * per entry (OCP 8-bit floating point: 4 exponent bits, bias 7, 3 mantissa
+ * bits; code S.1111.111 must not occur) and the matrix is
+ * W = diag(s) . decode(codes) with one fp32 scale per row (the s_* arrays of
+ * dflash_weights).  The codes are widened exactly to bf16 inside the
+ * projection kernel, so the arithmetic is that of DFLASH_BF16 on W; only the
+ * weight bytes read from HBM halve.  Features, the embedding, norm gains and
+ * key_offset stay bf16 / fp32 as for DFLASH_BF16.  Row lengths of the
+ * projections (hidden, ffn, n_q_heads*head_dim, n_taps*tap_width) must be
+ * multiples of 16.  [Guide] "Production Benchmarks on NVIDIA Blackwell B200"
+ * (FP4/FP8 mixed execution). */
+typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_BF16_W8 = 2 } dflash_dtype;
 
 typedef struct {
   int n_layers;          /* draft layers L */
@@ -117,6 +129,16 @@ typedef struct {
   const void* const* w_down; /* per layer [hidden, ffn] */
   const void* const* g_in;   /* per layer [hidden]  pre-attention RMSNorm gain */
   const void* const* g_post; /* per layer [hidden]  pre-MLP RMSNorm gain */
+  /* DFLASH_BF16_W8 only (ignored otherwise): fp32 row scales of the E4M3
+     projection weights above, one per row in the same row order (packed
+     matrices: packed the same way; zero-padded rows may have any scale). */
+  const float* s_fc;                /* [hidden] */
+  const float* s_lm;                /* [vocab] */
+  const float* s_kv_inject;         /* [n_layers*2*n_kv_heads*head_dim] */
+  const float* const* s_qkv;        /* per layer [Hq*dh + 2*kvd] */
+  const float* const* s_o;          /* per layer [hidden] */
+  const float* const* s_gu;         /* per layer [128*ceil(ffn/64)] */
+  const float* const* s_down;       /* per layer [hidden] */
 } dflash_weights;
 
 /* Bytes of caller-provided scratch the context needs; 0 on a bad config. */
@@ -282,6 +304,16 @@ dflash_status dflash_graph_destroy(dflash_graph* graph);
  * three calls above, exposed so it can be checked on its own. */
 dflash_status dflash_gemm_bf16(const void* W, int N, int K, const void* X, const void* X_lo, int M, float* out,
                                int splits, int* splits_used, int* status, dflash_stream stream);
+
+/* dflash_gemm_bf16 with E4M3 weights (the DFLASH_BF16_W8 projection kernel
+ * on its own, for testing it in isolation): out[s][m][n] = w_scale[n] *
+ * sum over the k-blocks of split s of (X[m][k] + X_lo[m][k]) * decode(W[n][k]),
+ * with W device uint8 E4M3 codes [N, K] (K a multiple of 16, 16-byte
+ * aligned) and w_scale device fp32 [N]; everything else as for
+ * dflash_gemm_bf16.  No counterpart on the pages beyond the FP8 storage
+ * format itself. */
+dflash_status dflash_gemm_w8(const void* W, const float* w_scale, int N, int K, const void* X, const void* X_lo,
+                             int M, float* out, int splits, int* splits_used, int* status, dflash_stream stream);
 
 /* dflash_gemm_bf16 for callers that cannot allocate device memory.  Some
  * callers must not call cudaMalloc or have it called on their behalf: a

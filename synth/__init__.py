@@ -146,9 +146,11 @@ MINI_CONFIGS: Dict[str, DraftConfig] = {
                           ffn=1024, vocab=3000, n_taps=2, tap_width=512,
                           match_prob=0.8, rounds=3, seed=2004),
     # FP8 projection weights (e4m3 + per-row scales), otherwise like mini_a
+    # (FP8 rows must be a multiple of 16 bytes, so ffn = 1328: still ragged
+    # against the 64-wide k-blocks)
     "mini_w8": DraftConfig("mini_w8", batch=3, ctx_lo=9, ctx_hi=260, n_layers=2,
                            hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=128,
-                           ffn=1320, vocab=5000, n_taps=3, tap_width=448,
+                           ffn=1328, vocab=5000, n_taps=3, tap_width=448,
                            match_prob=0.8, rounds=3, seed=2005, weight_format="e4m3"),
     # fp32 mini: ragged, several pages, G = 2
     "mini_f32": DraftConfig("mini_f32", batch=2, ctx_lo=17, ctx_hi=90, n_layers=2,

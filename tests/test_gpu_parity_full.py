@@ -22,7 +22,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 K = 16
 # sampled sequences per workload (first, last, and one in between)
-SAMPLES = {"c2": [0], "c3": [0, 13, 31], "c4": [2], "c5": [0, 127]}
+SAMPLES = {"c2": [0], "c2w8": [0], "c3": [0, 13, 31], "c4": [2], "c5": [0, 127]}
 
 
 def paging_replay(cfg, lens, chunk, round_rows, mpps, n_pages):
@@ -40,7 +40,7 @@ def paging_replay(cfg, lens, chunk, round_rows, mpps, n_pages):
     return pk
 
 
-@pytest.mark.parametrize("name", ["c2", "c3", "c4", "c5"])
+@pytest.mark.parametrize("name", ["c2", "c2w8", "c3", "c4", "c5"])
 def test_full_size_sampled_parity(name):
     import torch
     import bench
