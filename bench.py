@@ -157,7 +157,7 @@ def barrier(world: int):
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "k_gemm_tc_c2_layer.md")
-GEMM_SOURCES = ("gemm.cu", "epilogue.cuh", "common.cuh")
+GEMM_SOURCES = ("gemm_kernel.cuh", "gemm.cu", "epilogue.cuh", "common.cuh")
 
 
 def gemm_traffic(cfg):
