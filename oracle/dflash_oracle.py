@@ -34,6 +34,12 @@ Readings taken where the pages are silent (each repeated at its function):
   R13 residual / bonus sampling by an exponential race, ties to lowest v
   R14 page allocation: FIFO free list, sequences served in index order
   R15 optional shared pre-RoPE key offset on the injected keys (workload knob)
+  R17 training-time block attention (P2 Fig. 4): a block of K positions
+      that starts at response position c sees the target context at
+      positions [0, c) ("causal consistency") and all K positions of its own
+      block (bidirectional, as at inference), and nothing of any other block
+      ("no inter-block leakage"); anchors (clean tokens inside a block)
+      change only the block's input embeddings, not the mask
   R16 FP8 weights (the Guide's "FP4/FP8 mixed execution" on Blackwell): a
       projection weight is an e4m3 code per entry and an fp32 scale per
       output row, W = diag(s) . decode(codes); the drafter's arithmetic is
@@ -118,6 +124,25 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
         p = np.exp(s)
         p /= p.sum(axis=1, keepdims=True)
         out[:, h, :] = p @ v[:, g, :]
+    return out
+
+
+def block_attention_train(q: np.ndarray, k_blk: np.ndarray, v_blk: np.ndarray,
+                          ctx_k: Sequence[np.ndarray], ctx_v: Sequence[np.ndarray],
+                          seq: np.ndarray, ctx_len: np.ndarray) -> np.ndarray:
+    """Training-time block attention (R17, P2 Fig. 4).
+
+    q [NB, K, Hq, dh]; k_blk, v_blk [NB, K, Hkv, dh] (the blocks' own keys,
+    positions already encoded, and values); ctx_k[s], ctx_v[s] [T_s, Hkv, dh]
+    the context of sequence s.  Block j belongs to sequence seq[j] and sees
+    that context's first ctx_len[j] positions and its own K keys, unmasked.
+    Returns o [NB, K, Hq, dh]."""
+    out = np.empty(np.shape(q), dtype=F64)
+    for j in range(len(seq)):
+        s, c = int(seq[j]), int(ctx_len[j])
+        keys = np.concatenate([_f64(ctx_k[s])[:c], _f64(k_blk[j])], axis=0)
+        vals = np.concatenate([_f64(ctx_v[s])[:c], _f64(v_blk[j])], axis=0)
+        out[j] = attention(q[j], keys, vals)
     return out
 
 

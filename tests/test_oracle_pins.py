@@ -543,3 +543,85 @@ def test_dequantized_weights_scale_each_output_row():
     x = rng.standard_normal((3, 7))
     y1 = x @ O.decode_e4m3(codes).T
     np.testing.assert_allclose(x @ w["w_o.0"].T, y1 * s.astype(np.float64), rtol=1e-15, atol=0)
+
+
+# ---------------------------------------------------------------- training-time block attention
+
+def _train_attn_case(rng, S=3, NB=7, K=4, Hq=4, Hkv=2, dh=8):
+    T = rng.integers(5, 30, size=S)
+    ctx_k = [rng.standard_normal((t, Hkv, dh)) for t in T]
+    ctx_v = [rng.standard_normal((t, Hkv, dh)) for t in T]
+    seq = rng.integers(0, S, size=NB)
+    ctx_len = np.array([rng.integers(0, T[s] + 1) for s in seq])
+    q = rng.standard_normal((NB, K, Hq, dh))
+    kb = rng.standard_normal((NB, K, Hkv, dh))
+    vb = rng.standard_normal((NB, K, Hkv, dh))
+    return q, kb, vb, ctx_k, ctx_v, seq, ctx_len
+
+
+def test_train_attention_equals_one_dense_masked_softmax():
+    """Every block at once as one attention over [all contexts ; all block
+    keys] with an explicit 0 / -inf mask (a second formulation: a single
+    dense score matrix, mask built from the rule, SciPy's softmax)."""
+    rng = np.random.default_rng(21)
+    q, kb, vb, ctx_k, ctx_v, seq, ctx_len = _train_attn_case(rng)
+    NB, K, Hq, dh = q.shape
+    Hkv = kb.shape[2]
+    G = Hq // Hkv
+    keys = np.concatenate(list(ctx_k) + [kb.reshape(NB * K, Hkv, dh)])
+    vals = np.concatenate(list(ctx_v) + [vb.reshape(NB * K, Hkv, dh)])
+    off = np.concatenate([[0], np.cumsum([c.shape[0] for c in ctx_k])])
+    n_ctx = off[-1]
+    mask = np.full((NB * K, keys.shape[0]), -np.inf)
+    for j in range(NB):
+        rows = slice(j * K, (j + 1) * K)
+        mask[rows, off[seq[j]]:off[seq[j]] + ctx_len[j]] = 0.0
+        mask[rows, n_ctx + j * K:n_ctx + (j + 1) * K] = 0.0
+    qf = q.reshape(NB * K, Hq, dh)
+    dense = np.empty_like(qf)
+    for h in range(Hq):
+        sc = qf[:, h] @ keys[:, h // G].T / math.sqrt(dh) + mask
+        dense[:, h] = scipy.special.softmax(sc, axis=1) @ vals[:, h // G]
+    got = O.block_attention_train(q, kb, vb, ctx_k, ctx_v, seq, ctx_len)
+    np.testing.assert_allclose(got.reshape(NB * K, Hq, dh), dense, rtol=1e-12, atol=1e-12)
+
+
+def test_train_attention_sees_no_other_block_and_no_later_context():
+    rng = np.random.default_rng(22)
+    q, kb, vb, ctx_k, ctx_v, seq, ctx_len = _train_attn_case(rng)
+    base = O.block_attention_train(q, kb, vb, ctx_k, ctx_v, seq, ctx_len)
+    # perturb block 0's own keys: only block 0 changes
+    kb2 = kb.copy()
+    kb2[0] += 1.0
+    o2 = O.block_attention_train(q, kb2, vb, ctx_k, ctx_v, seq, ctx_len)
+    assert not np.allclose(o2[0], base[0])
+    np.testing.assert_array_equal(o2[1:], base[1:])
+    # perturb every context position at or past each block's prefix of its sequence: nothing changes
+    for j in range(len(seq)):
+        ck = [c.copy() for c in ctx_k]
+        cv = [c.copy() for c in ctx_v]
+        ck[seq[j]][ctx_len[j]:] += 5.0
+        cv[seq[j]][ctx_len[j]:] -= 5.0
+        o3 = O.block_attention_train(q, kb, vb, ck, cv, seq, ctx_len)
+        np.testing.assert_array_equal(o3[j], base[j])
+
+
+def test_train_attention_reduces_to_inference_attention_and_own_block():
+    """A block whose prefix is the whole context is the inference block
+    attention over [context ; block]; an empty prefix attends to its own
+    block only; one key and one value make the output that value."""
+    rng = np.random.default_rng(23)
+    q, kb, vb, ctx_k, ctx_v, seq, ctx_len = _train_attn_case(rng, NB=3)
+    seq = np.array([0, 1, 2])
+    full = np.array([c.shape[0] for c in ctx_k])
+    o = O.block_attention_train(q, kb, vb, ctx_k, ctx_v, seq, full)
+    for j in range(3):
+        ref = O.attention(q[j], np.concatenate([ctx_k[j], kb[j]]), np.concatenate([ctx_v[j], vb[j]]))
+        np.testing.assert_allclose(o[j], ref, rtol=0, atol=0)
+    o0 = O.block_attention_train(q, kb, vb, ctx_k, ctx_v, seq, np.zeros(3, int))
+    for j in range(3):
+        np.testing.assert_allclose(o0[j], O.attention(q[j], kb[j], vb[j]), rtol=0, atol=0)
+    # K = 1, no context: softmax over one key is 1, the output is its value
+    o1 = O.block_attention_train(q[:, :1], kb[:, :1], vb[:, :1], ctx_k, ctx_v, seq, np.zeros(3, int))
+    G = q.shape[2] // kb.shape[2]
+    np.testing.assert_allclose(o1[:, 0], np.repeat(vb[:, 0], G, axis=1), rtol=1e-15)
