@@ -16,7 +16,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "pool
                 4: "CUDA error", 5: "device status set", 6: "workspace too small",
                 7: "too large for the fixed scratch", 8: "not allowed while capturing"}
 ROUND_DEVICE = (1 << 64) - 1   # dflash_accept: take the round from the device counter
-DEV_POOL_EXHAUSTED, DEV_SEQ_TOO_LONG, DEV_WAIT_TIMEOUT, DEV_BAD_TOKEN, DEV_BAD_ROWS = 1, 2, 4, 8, 16
+DEV_POOL_EXHAUSTED, DEV_SEQ_TOO_LONG, DEV_WAIT_TIMEOUT, DEV_BAD_TOKEN, DEV_BAD_ROWS, DEV_BAD_BLOCK = 1, 2, 4, 8, 16, 32
 DTYPE_F32, DTYPE_BF16, DTYPE_BF16_W8 = 0, 1, 2
 
 EXPORTED = ("dflash_workspace_size", "dflash_kv_pool_size", "dflash_create", "dflash_destroy",
@@ -24,7 +24,7 @@ EXPORTED = ("dflash_workspace_size", "dflash_kv_pool_size", "dflash_create", "df
             "dflash_accept", "dflash_get_status", "dflash_status_string", "dflash_gemm_bf16",
             "dflash_profile_enable", "dflash_profile_read", "dflash_truncate", "dflash_gemm_bf16_noalloc",
             "dflash_graph_begin", "dflash_graph_end", "dflash_graph_launch", "dflash_graph_destroy",
-            "dflash_gemm_w8")
+            "dflash_gemm_w8", "dflash_block_attention")
 PROF_CLASSES = ("proj", "lm_head", "inject", "attention", "rowwise", "accept")
 
 
@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.dflash_gemm_bf16.restype = ctypes.c_int
         L.dflash_gemm_bf16.argtypes = [_VP, ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int, _VP, ctypes.c_int,
                                        ctypes.POINTER(ctypes.c_int), _VP, _VP]
+        L.dflash_block_attention.restype = ctypes.c_int
+        L.dflash_block_attention.argtypes = [_VP, ctypes.c_int, ctypes.c_int, i32p, i32p, _VP, _VP, _VP, _VP, _VP]
         L.dflash_gemm_w8.restype = ctypes.c_int
         L.dflash_gemm_w8.argtypes = [_VP, _VP, ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int, _VP, ctypes.c_int,
                                      ctypes.POINTER(ctypes.c_int), _VP, _VP]

@@ -211,8 +211,10 @@ static cudaError_t launch_attn_ty(dflash_ctx* c, int layer, int B, int splits, c
 
 // fp32 workloads: the fp32 SIMT kernel above; bf16 workloads (fp16 pool):
 // the tcgen05 kernel of attention_mma.cu.
-cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next) {
-  if (c->cfg.dtype != DFLASH_F32) return launch_attention_mma(c, layer, B, splits, s, next);
+cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
+                             const AttnSrc& src) {
+  if (c->cfg.dtype != DFLASH_F32) return launch_attention_mma(c, layer, B, splits, s, next, src);
+  if (src.row_of != nullptr || src.seq_len != nullptr) return cudaErrorInvalidValue;  // bf16 family only
   return launch_attn_ty<float>(c, layer, B, splits, s);
 }
 

@@ -87,7 +87,8 @@ struct MmaAttnCfg {
 
 struct MmaAttnParams {
   const int32_t* page_table;
-  const int32_t* seq_len;
+  const int32_t* seq_len;  // context length of block b
+  const int32_t* row_of;   // page-table row of block b (null: row b)
   int max_pages, block_page0, pool_pages, layer;
   int Hkv, splits;
   int page_slots;     // capacity of the shared-memory page-id list
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_const
   const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.seq_len[b];
+  const int prow = p.row_of != nullptr ? p.row_of[b] : b;
   const int n_ctx_pages = (T + kPage - 1) / kPage;
   const int n_pages = n_ctx_pages + 1;  // + the block page
   const int per_split = (n_pages + p.splits - 1) / p.splits;
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_const
     // issuing a block never waits on a global load
     for (int j = lane; j < np; j += 32) {
       const int vp = vp_begin + j;
-      s_pages[j] = vp < n_ctx_pages ? p.page_table[b * p.max_pages + vp] : p.block_page0 + b;
+      s_pages[j] = vp < n_ctx_pages ? p.page_table[prow * p.max_pages + vp] : p.block_page0 + b;
     }
   }
   if (warp == kMmaWarp) {
@@ -639,7 +641,8 @@ int split_pages_bound(const dflash_ctx* c, int splits) {
 }
 
 template <int DH, int G, int KBP, int NST>
-cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next) {
+cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
+                     const AttnSrc& src) {
   const auto& g = c->cfg;
   const int page_slots = split_pages_bound(c, splits);
   const int smem = smem_bytes<DH, G, KBP, NST>(page_slots);
@@ -655,7 +658,8 @@ cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s
   }
   MmaAttnParams p;
   p.page_table = c->page_table;
-  p.seq_len = c->seq_len;
+  p.seq_len = src.seq_len != nullptr ? src.seq_len : c->seq_len;
+  p.row_of = src.row_of;
   p.max_pages = g.max_pages_per_seq;
   p.block_page0 = g.n_pages;
   p.pool_pages = c->pool_pages;
@@ -670,7 +674,7 @@ cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s
   CUtensorMap tn = c->attn_map_k;  // placeholder when there is no plan
   if (!gemm_l2_plan(c, next, &p.l2, &tn)) p.l2 = L2Plan{};
   return launch_k(k_attn_mma<DH, G, KBP, NST>, dim3(splits, g.n_kv_heads, B), dim3(kAttnThreads), smem, s,
-                  dim3(splits, 1, 1), c->pdl, c->attn_map_q, c->attn_map_k, c->attn_map_v, tn, p);
+                  dim3(splits, 1, 1), c->pdl && src.pdl, c->attn_map_q, c->attn_map_k, c->attn_map_v, tn, p);
 }
 
 // How many clusters of `splits` CTAs of this kernel instance can be
@@ -728,8 +732,9 @@ auto dispatch(dflash_ctx* c, int splits, A... args) {
 
 template <int DH, int G, int KBP, int NST>
 struct LaunchF {
-  static cudaError_t run(dflash_ctx* c, int splits, int layer, int B, cudaStream_t s, const NextGemm* next) {
-    return launch_t<DH, G, KBP, NST>(c, layer, B, splits, s, *next);
+  static cudaError_t run(dflash_ctx* c, int splits, int layer, int B, cudaStream_t s, const NextGemm* next,
+                         const AttnSrc* src) {
+    return launch_t<DH, G, KBP, NST>(c, layer, B, splits, s, *next, *src);
   }
   static cudaError_t invalid() { return cudaErrorInvalidValue; }
 };
@@ -758,8 +763,9 @@ int attention_mma_splits(dflash_ctx* c, int B) {
   return s0;
 }
 
-cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next) {
-  return dispatch<LaunchF>(c, splits, layer, B, s, &next);
+cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
+                                 const AttnSrc& src) {
+  return dispatch<LaunchF>(c, splits, layer, B, s, &next, &src);
 }
 
 }  // namespace dflash

@@ -23,6 +23,7 @@ enum : int {
   ST_WAIT_TIMEOUT = 4,     // a bounded device wait gave up
   ST_BAD_TOKEN = 8,        // a token id outside [0, vocab)
   ST_BAD_ROWS = 16,        // an n_rows entry outside [0, max_rows]
+  ST_BAD_BLOCK = 32,       // a training block's sequence or prefix length out of range
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait

@@ -127,6 +127,8 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   auto row_seq = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
   auto row_pos = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
   auto row_src = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
+  auto blk_row = static_cast<int32_t*>(w.take(sizeof(int32_t) * g.max_batch));
+  auto blk_len = static_cast<int32_t*>(w.take(sizeof(int32_t) * g.max_batch));
   auto rcos = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
   auto rsin = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
   const bool lo = g.dtype != DFLASH_F32;  // GEMM inputs carry a second bf16 term
@@ -161,6 +163,8 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
     c->row_seq = row_seq;
     c->row_pos = row_pos;
     c->row_src = row_src;
+    c->blk_row = blk_row;
+    c->blk_len = blk_len;
     c->rope_cos = rcos;
     c->rope_sin = rsin;
     c->rope_rows = rope_rows;
@@ -655,6 +659,23 @@ dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* dra
   int* round_ctr = round == DFLASH_ROUND_DEVICE ? ctx->status + 2 : nullptr;
   DF_CHECK(launch_accept_stochastic(B, kBlockK, ctx->cfg.vocab, draft_tokens, target_logits, draft_probs,
                                     temperature, seed, round, round_ctr, accept_len, emitted, n_emit, ctx->pdl, s));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_block_attention(dflash_ctx* ctx, int layer, int NB, const int32_t* seq, const int32_t* ctx_len,
+                                     const void* q, const void* k_blk, const void* v_blk, float* out,
+                                     dflash_stream stream) {
+  if (ctx == nullptr || seq == nullptr || ctx_len == nullptr || q == nullptr || k_blk == nullptr ||
+      v_blk == nullptr || out == nullptr)
+    return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& g = ctx->cfg;
+  if (g.dtype == DFLASH_F32) return DFLASH_ERR_UNSUPPORTED_SHAPE;  // the fp16-pool (tcgen05) attention only
+  if (layer < 0 || layer >= g.n_layers || NB < 1 || NB > g.max_batch) return DFLASH_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(k_blk) % 16 ||
+      reinterpret_cast<uintptr_t>(v_blk) % 16)
+    return DFLASH_ERR_INVALID_ARG;
+  ProfScope p(ctx, DFLASH_PROF_ATTN, 3, stream);
+  DF_CHECK(launch_block_attention(ctx, layer, NB, seq, ctx_len, q, k_blk, v_blk, out, stream));
   return DFLASH_OK;
 }
 

@@ -58,6 +58,15 @@ struct GemmLaunch {
   const float* w_scale;  // E4M3 weights (DFLASH_BF16_W8): fp32 scale of every weight row [N]
 };
 
+// Where block attention takes its sequences from: by default the context's
+// page table and lengths, block b being sequence b; the training-time block
+// attention passes a page-table row and a context length per block.
+struct AttnSrc {
+  const int32_t* row_of = nullptr;   // page-table row of block b (null: row b)
+  const int32_t* seq_len = nullptr;  // context length of block b (null: the context's seq_len)
+  bool pdl = true;                   // false: the immediate predecessor wrote row_of / seq_len
+};
+
 struct TmapEntry {
   const void* ptr;
   int rows, cols, box_rows;
@@ -90,6 +99,7 @@ struct dflash_ctx {
   int* status;
   int* scal;  // [0] rows of the current inject, [1] free-list head, [2] free count
   int32_t *free_ring, *row_seq, *row_pos, *row_src;
+  int32_t *blk_row, *blk_len;  // training-time block attention: page-table row and context length per block
   float *rope_cos, *rope_sin;
   int rope_rows;
   int pool_pages;  // pages per layer in the pool: n_pages context pages + max_batch block pages

@@ -27,9 +27,14 @@ cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s);
 
 // attention.cu
 int attn_splits(dflash_ctx* c, int B);
-cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next);
+cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
+                             const AttnSrc& src = AttnSrc{});
 // attention_mma.cu (fp16 pool, tcgen05)
-cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next);
+// train_attn.cu
+cudaError_t launch_block_attention(dflash_ctx* c, int layer, int NB, const int32_t* seq, const int32_t* ctx_len,
+                                   const void* q, const void* k_blk, const void* v_blk, float* out, cudaStream_t s);
+cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
+                                 const AttnSrc& src = AttnSrc{});
 int attention_mma_splits(dflash_ctx* c, int B);
 
 // accept.cu

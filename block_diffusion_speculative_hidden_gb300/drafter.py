@@ -286,6 +286,22 @@ class Drafter:
                                         _stream(stream)), "dflash_accept")
         return tau, emitted, n_emit
 
+    def block_attention(self, layer: int, seq: torch.Tensor, ctx_len: torch.Tensor, q: torch.Tensor,
+                        k_blk: torch.Tensor, v_blk: torch.Tensor, out: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+        """Training-time block attention: NB blocks; block j sees sequence seq[j]'s
+        context prefix of ctx_len[j] positions and its own 16 keys.  q fp16
+        [NB, 16, Hq, dh]; k_blk, v_blk fp16 [NB, 16, Hkv, dh]; returns fp32 [NB, 16, Hq, dh]."""
+        NB = q.shape[0]
+        assert q.dtype == torch.float16 and k_blk.dtype == torch.float16 and v_blk.dtype == torch.float16
+        assert q.is_contiguous() and k_blk.is_contiguous() and v_blk.is_contiguous()
+        assert seq.dtype == torch.int32 and ctx_len.dtype == torch.int32
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=self.device)
+        _lib.check(self.L.dflash_block_attention(self.ctx, layer, NB, _ptr(seq), _ptr(ctx_len), _ptr(q), _ptr(k_blk),
+                                                 _ptr(v_blk), _ptr(out), _stream(stream)), "dflash_block_attention")
+        return out
+
     def reset(self, stream=None) -> None:
         """Empty every sequence and clear the device status word."""
         _lib.check(self.L.dflash_reset(self.ctx, _stream(stream)), "dflash_reset")

@@ -69,6 +69,7 @@ typedef enum {
 #define DFLASH_DEV_WAIT_TIMEOUT 4   /* a bounded device wait gave up (2 s) */
 #define DFLASH_DEV_BAD_TOKEN 8      /* a token id outside [0, vocab) */
 #define DFLASH_DEV_BAD_ROWS 16      /* an n_rows entry outside [0, max_rows] */
+#define DFLASH_DEV_BAD_BLOCK 32     /* dflash_block_attention: a block's sequence or prefix out of range */
 
 /* DFLASH_BF16_W8: DFLASH_BF16 with FP8 projection weights.  Every projection
  * weight (w_fc, w_kv_inject, w_qkv, w_o, w_gu, w_down, w_lm) is one E4M3 code
@@ -252,6 +253,31 @@ dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* dra
                             const float* draft_probs, float temperature, uint64_t seed,
                             uint64_t round, int32_t* accept_len, int32_t* emitted, int32_t* n_emit,
                             dflash_stream stream);
+
+/* Training-time block attention.  [Paper] Figure 4 (DFlash training
+ * attention: within a masked block the positions attend to each other; the
+ * mask keeps "causal consistency" with the target context and prevents
+ * "inter-block information leakage").
+ *
+ * For NB blocks of K = 16 positions (NB <= max_batch): block j belongs to
+ * sequence seq[j] (device int32 [NB]) and sees that sequence's injected
+ * context at positions 0 .. ctx_len[j] - 1 (device int32 [NB], at most the
+ * sequence's length) and all 16 positions of its own block, nothing of any
+ * other block.  q: device fp16 [NB, 16, n_q_heads, head_dim]; k_blk, v_blk:
+ * device fp16 [NB, 16, n_kv_heads, head_dim], the blocks' own keys (their
+ * positions already encoded) and values; out: device fp32 [NB, 16,
+ * n_q_heads, head_dim], softmax(q k^T / sqrt(head_dim)) v with query head h
+ * reading kv head h / (n_q_heads / n_kv_heads).  layer selects the context
+ * K/V of that draft layer.  The blocks' keys and values are staged in the
+ * pool's block pages and the queries in the workspace, so the call must not
+ * overlap a dflash_draft_block on the same context.  A sequence index
+ * outside [0, max_batch) or a prefix outside [0, seq_len] sets
+ * DFLASH_DEV_BAD_BLOCK and is clamped.  DFLASH_BF16 and DFLASH_BF16_W8
+ * contexts (fp16 pool) only: DFLASH_F32 returns UNSUPPORTED_SHAPE.
+ * Asynchronous. */
+dflash_status dflash_block_attention(dflash_ctx* ctx, int layer, int NB, const int32_t* seq,
+                                     const int32_t* ctx_len, const void* q, const void* k_blk,
+                                     const void* v_blk, float* out, dflash_stream stream);
 
 /* Host-free rounds.  [Chapter] "The systems side: Spec V2" (the host's
  * bookkeeping of a round is overlapped with the GPU's work) and the
