@@ -51,7 +51,7 @@ def parse_args(argv=None):
                     help="draft-cost sweeps (1/3/5 draft layers; projections on 1 vs 16 rows), JSON line per item")
     ap.add_argument("--reset-every", type=int, default=16,
                     help="roll each sequence back to its prompt length every N rounds")
-    ap.add_argument("--kernel", choices=["gemm"], default=None,
+    ap.add_argument("--kernel", choices=["gemm", "train_attn"], default=None,
                     help="time one kernel alone on the workload's shapes (small case for profilers)")
     ap.add_argument("--small", action="store_true",
                     help="profiler case: the workload's layer shapes with 1 draft layer and a 16384 vocab")
@@ -664,6 +664,75 @@ def run_fp8_leg(args, world, rank, local, hbm, peak_kind):
             "kernels": {k: v for k, v in per_class.items() if k in ("proj", "lm_head", "inject")}}
 
 
+def run_kernel_train_attn(args, cfg):
+    """Training-time block attention (Fig. 4 mask) on the workload's attention
+    shape: S sequences of T context positions (seeded fp16 keys and values in
+    the pool), NB blocks at seeded prefix lengths, each launch from a flushed
+    L2; the oracle timed on a sample of the same blocks."""
+    import torch
+    from block_diffusion_speculative_hidden_gb300 import Drafter, weights_to_device
+    S, T, per_seq = 4, 4096, 64
+    NB = S * per_seq
+    c = cfg.replace(n_layers=1, ffn=256, vocab=512, n_taps=1, tap_width=cfg.hidden, name=cfg.name + "_attn")
+    Hq, Hkv, dh = c.n_q_heads, c.n_kv_heads, c.head_dim
+    mpps = T // 16
+    dev = torch.device("cuda", 0)
+    dr = Drafter(c, weights_to_device(synth.make_weights(c), c.dtype, device=dev), max_batch=NB,
+                 max_pages_per_seq=mpps, n_pages=S * mpps, max_rows=17, max_inject_rows=NB * 17)
+    g = torch.Generator(device=dev).manual_seed(7)
+    Kp, Vp = dr.pool_kv()
+    Kp[0, :S * mpps].copy_(torch.randn(Kp[0, :S * mpps].shape, generator=g, device=dev).half())
+    Vp[0, :S * mpps].copy_(torch.randn(Vp[0, :S * mpps].shape, generator=g, device=dev).half())
+    pt = torch.full((NB, mpps), -1, dtype=torch.int32)
+    pt[:S] = torch.arange(S * mpps, dtype=torch.int32).reshape(S, mpps)
+    dr.page_table.copy_(pt)
+    sl = torch.zeros(NB, dtype=torch.int32)
+    sl[:S] = T
+    dr.seq_len.copy_(sl)
+    rng = np.random.default_rng(8)
+    seq = np.repeat(np.arange(S, dtype=np.int32), per_seq)
+    ctx_len = rng.integers(T // 4, T + 1, size=NB).astype(np.int32)
+    q = torch.randn((NB, 16, Hq, dh), generator=g, device=dev).half()
+    kb = torch.randn((NB, 16, Hkv, dh), generator=g, device=dev).half()
+    vb = torch.randn((NB, 16, Hkv, dh), generator=g, device=dev).half()
+    sq, cl = torch.from_numpy(seq).to(dev), torch.from_numpy(ctx_len).to(dev)
+    out = torch.empty((NB, 16, Hq, dh), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        dr.block_attention(0, sq, cl, q, kb, vb, out=out)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    ms = _median_ms(lambda: dr.block_attention(0, sq, cl, q, kb, vb, out=out), max(10, min(args.steps, 50)), flush)
+    keys = ctx_len.astype(np.float64) + 16
+    flops = float(np.sum(4.0 * 16 * Hq * dh * keys))
+    logical = float(np.sum(2.0 * keys * Hkv * dh * 2))           # K and V each block reads
+    unique = 2.0 * S * T * Hkv * dh * 2 + 3.0 * NB * 16 * Hkv * dh * 2 + NB * 16 * Hq * dh * (2 + 4)
+    hbm, tc, kind = load_peaks()
+    # the oracle on a sample of blocks (fp64 NumPy), scaled to all NB
+    from oracle import dflash_oracle as O
+    Kh, Vh = Kp[0, :S * mpps].float().cpu().numpy(), Vp[0, :S * mpps].float().cpu().numpy()
+    ctx_k = [Kh[s * mpps:(s + 1) * mpps].transpose(0, 2, 1, 3).reshape(T, Hkv, dh) for s in range(S)]
+    ctx_v = [Vh[s * mpps:(s + 1) * mpps].transpose(0, 2, 1, 3).reshape(T, Hkv, dh) for s in range(S)]
+    sample = np.arange(0, NB, NB // 8)
+    t0 = time.time()
+    O.block_attention_train(q[sample].float().cpu().numpy(), kb[sample].float().cpu().numpy(),
+                            vb[sample].float().cpu().numpy(), ctx_k, ctx_v, seq[sample], ctx_len[sample])
+    cpu_s = (time.time() - t0) * NB / len(sample)
+    print(json.dumps({
+        "kernel": "k_attn_mma (training-time block attention, Fig. 4 mask; dflash_block_attention)",
+        "workload": f"{c.name}: {S} sequences x {T} context, {NB} blocks of 16, prefixes U[{T // 4}, {T}]",
+        "heads": f"{Hq}/{Hkv}x{dh}", "us": ms * 1e3, "blocks_per_s": NB / (ms / 1e3),
+        "roofline": {"bound": "tensor", "achieved": flops / (ms / 1e3) / 1e12, "peak": tc, "unit": "TFLOP/s",
+                     "frac": flops / (ms / 1e3) / 1e12 / tc, "peak_kind": f"{kind} bf16_tflops (fp16 MMA, same rate)",
+                     "flops_per_launch": flops},
+        "kv_bytes": {"logical_per_launch": logical, "unique_per_launch": unique,
+                     "logical_GB_per_s": logical / (ms / 1e3) / 1e9, "unique_frac_hbm": unique / (ms / 1e3) / 1e9 / hbm},
+        "l2": "L2 flushed before every launch",
+        "cpu_baseline": {"kind": "oracle", "seconds_per_launch": cpu_s, "sample": f"{len(sample)} of {NB} blocks",
+                         "cores": os.cpu_count()},
+    }), flush=True)
+
+
 # --------------------------------------------------------------------------- main
 
 def main(argv=None):
@@ -673,6 +742,9 @@ def main(argv=None):
         cfg = cfg.replace(n_layers=1, vocab=16384, name=cfg.name + "_1layer_v16k")
     if args.kernel == "gemm":
         run_kernel_gemm(args, cfg)
+        return
+    if args.kernel == "train_attn":
+        run_kernel_train_attn(args, cfg)
         return
     if args.sweep:
         run_sweep(args, cfg)
