@@ -395,7 +395,10 @@ def run_graph(wl, args, device):
 def run_e2e(wl, args, device):
     """Per step: pinned host feature rows and target coins -> device, the
     three library calls, drafts + emitted tokens + counts -> pinned host,
-    then a stream sync (the caller reads its result)."""
+    then a stream sync (the caller reads its result).  Timed twice: each
+    step's calls issued one by one, and each step as one replay of a CUDA
+    graph recorded from the same calls, copies included (dflash_graph_*);
+    the graph figure is the e2e value, the other is reported beside it."""
     torch = wl.torch
     cfg = wl.cfg
     B, F = cfg.batch, cfg.feat_dim
@@ -409,29 +412,72 @@ def run_e2e(wl, args, device):
     o_tok = torch.empty((B, K_BLOCK), dtype=torch.int32).pin_memory()
     o_em = torch.empty((B, 17), dtype=torch.int32).pin_memory()
     o_n = torch.empty((B,), dtype=torch.int32).pin_memory()
-    stream = torch.cuda.current_stream(device)
     h2d = d_feats.numel() * d_feats.element_size() + d_match.numel() + d_y.numel() * 4
     d2h = o_tok.numel() * 4 + o_em.numel() * 4 + o_n.numel() * 4
-    torch.cuda.synchronize(device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(n):
-        r = i % wl.rounds
+    gs = torch.cuda.Stream(device)
+
+    def one_step(r):
         d_feats.copy_(h_feats[r], non_blocking=True)
         d_match.copy_(h_match[r], non_blocking=True)
         d_y.copy_(h_y[r], non_blocking=True)
         wl.step(r, feats=d_feats, y=d_y, match=d_match)
-        wl.maybe_reset(i, args.reset_every)
+        wl.maybe_reset(r, args.reset_every)
         o_tok.copy_(wl.tok, non_blocking=True)
         o_em.copy_(wl.acc[1], non_blocking=True)
         o_n.copy_(wl.acc[2], non_blocking=True)
-        stream.synchronize()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    ms = e0.elapsed_time(e1)
-    return {"value": n * B * K_BLOCK / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n}
+
+    def restart():
+        # from the prompts, so that the rollback schedule (round index mod
+        # reset_every) bounds every sequence's growth
+        with torch.cuda.stream(gs):
+            for b in range(B):
+                wl.dr.truncate(b, int(wl.lens[b]), stream=gs)
+        gs.synchronize()
+
+    def timed(run_step):
+        restart()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(gs)
+        for i in range(n):
+            run_step(i % wl.rounds)
+            gs.synchronize()
+        e1.record(gs)
+        gs.synchronize()
+        return e0.elapsed_time(e1)
+
+    with torch.cuda.stream(gs):
+        ms_eager = timed(one_step)
+        graphs, why = None, None
+        if not args.no_graph:
+            graphs = []
+            try:
+                for r in range(wl.rounds):
+                    wl.dr.graph_begin(stream=gs)
+                    try:
+                        one_step(r)
+                    finally:
+                        g = wl.dr.graph_end(stream=gs)    # ends the recording either way
+                    graphs.append(g)
+            except Exception as e:                         # a copy the recording refuses: eager only
+                why = f"{type(e).__name__}: {e}"[:200]
+                graphs = None
+                gs.synchronize()
+        if graphs is not None:
+            ms_graph = timed(lambda r: graphs[r].launch(stream=gs))
+            for g in graphs:
+                g.close()
+    assert wl.dr.device_status() == 0
+    ms = ms_graph if graphs is not None else ms_eager
+    out = {"value": n * B * K_BLOCK / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "steps": n,
+           "calls": "one CUDA graph replay per step (dflash_graph_launch), copies inside" if graphs is not None
+           else "the three library calls per step"}
+    if graphs is not None:
+        out["eager_value"] = n * B * K_BLOCK / (ms_eager / 1e3)
+    elif why is not None:
+        out["graph_unavailable"] = why
+    return out
 
 
 # --------------------------------------------------------------------------- oracle (CPU)
