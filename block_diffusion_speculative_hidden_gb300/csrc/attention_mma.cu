@@ -135,7 +135,7 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 }
 
 template <int DH, int G, int KBP, int NST>
-__global__ void __launch_bounds__(kAttnThreads, 1) k_attn_mma(const __grid_constant__ CUtensorMap tmQ,
+__global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(const __grid_constant__ CUtensorMap tmQ,
                                                               const __grid_constant__ CUtensorMap tmK,
                                                               const __grid_constant__ CUtensorMap tmV,
                                                               const __grid_constant__ CUtensorMap tmNext,
@@ -713,16 +713,37 @@ int max_clusters_t(dflash_ctx* c, int splits) {
 // 2-deep ring.
 constexpr int kShortPages = 13;
 
+// The streaming variant with 4-page key blocks: half the shared memory and
+// at most 102 registers a thread, so two CTAs share an SM (for long prefixes
+// streamed through one CTA, as in the training-time block attention).  It
+// exists where the split partials still fit its smaller ring.
+template <int DH, int G>
+constexpr bool narrow_fits() {
+  // MmaAttnCfg<DH, G, 4, 2>'s layout and its three static checks, computed
+  // here without instantiating it (its checks would fail to compile)
+  constexpr int KBP = 4, NST = 2, R = G * 16, M = R <= 64 ? 64 : 128, NCH = DH / 64;
+  constexpr int Q_CH = R * 128, P_CH = R * 128, P_CHUNKS = (KBP * 16 + 63) / 64;
+  constexpr int KV_BYTES = NCH * KBP * 16 * 128, STAGE = 2 * KV_BYTES;
+  constexpr bool P_IN_K = P_CHUNKS * P_CH <= KV_BYTES;
+  constexpr int OFF_KV = NCH * Q_CH + (P_IN_K ? 0 : P_CHUNKS * P_CH);
+  constexpr int OFF_BAR = OFF_KV + NST * STAGE;
+  constexpr int END = OFF_BAR + 128 + 8 * 32 * (2 * (M / 64)) * 4;
+  return (NCH - 1) * Q_CH + M * 128 <= END &&
+         (P_IN_K ? OFF_KV + (NST - 1) * STAGE : NCH * Q_CH) + (P_CHUNKS - 1) * P_CH + M * 128 <= END &&
+         (2 * R + kMergeMax) * (DH + 4) * 4 <= OFF_BAR;
+}
+
 // Runs F<DH, G, KBP, NST>(args) for the kernel instance serving `splits`.
 template <template <int, int, int, int> class F, typename... A>
-auto dispatch(dflash_ctx* c, int splits, A... args) {
+auto dispatch(dflash_ctx* c, int splits, bool narrow, A... args) {
   const bool short_split = split_pages_bound(c, splits) <= kShortPages;
   const int G = c->cfg.n_q_heads / c->cfg.n_kv_heads;
   const bool d64 = c->cfg.head_dim == 64;
 #define DFLASH_ATTN_CASE(DH_, G_)                                                              \
   if (c->cfg.head_dim == DH_ && G == G_)                                                       \
     return short_split ? F<DH_, G_, kShortPages, 1>::run(c, splits, args...)                   \
-                       : F<DH_, G_, 8, 2>::run(c, splits, args...);
+           : narrow ? F<DH_, G_, narrow_fits<DH_, G_>() ? 4 : 8, 2>::run(c, splits, args...)   \
+                    : F<DH_, G_, 8, 2>::run(c, splits, args...);
   DFLASH_ATTN_CASE(64, 1) DFLASH_ATTN_CASE(64, 2) DFLASH_ATTN_CASE(64, 4) DFLASH_ATTN_CASE(64, 8)
   DFLASH_ATTN_CASE(128, 1) DFLASH_ATTN_CASE(128, 2) DFLASH_ATTN_CASE(128, 4) DFLASH_ATTN_CASE(128, 8)
 #undef DFLASH_ATTN_CASE
@@ -757,7 +778,7 @@ int attention_mma_splits(dflash_ctx* c, int B) {
   const int s0 = std::max(1, std::min({kMergeMax, (2 * c->num_sms + heads - 1) / heads, c->attn_max_splits}));
   for (int S = s0; S > 1; --S) {
     int& n = c->attn_fit[S];
-    if (n == 0) n = std::max(-1, dispatch<ClustersF>(c, S));
+    if (n == 0) n = std::max(-1, dispatch<ClustersF>(c, S, false));
     if (n >= heads) return S;
   }
   return s0;
@@ -765,7 +786,7 @@ int attention_mma_splits(dflash_ctx* c, int B) {
 
 cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
                                  const AttnSrc& src) {
-  return dispatch<LaunchF>(c, splits, layer, B, s, &next, &src);
+  return dispatch<LaunchF>(c, splits, src.narrow, layer, B, s, &next, &src);
 }
 
 }  // namespace dflash
