@@ -419,28 +419,31 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       live = live && mbar_wait(o_full, blk & 1, p.status);
       __syncwarp();
       tc_fence_after();
-      if constexpr (ONE) break;  // O stays in TMEM (a single block: both warps leave here)
-      // O_blk = P V: this warp's half of the head dims, folded with the rescale
+      if constexpr (ONE) {
+        break;  // O stays in TMEM (a single block: both warps leave here)
+      } else {
+        // O_blk = P V: this warp's half of the head dims, folded with the rescale
 #pragma unroll
-      for (int sb = 0; sb < C::SUB; ++sb) {
+        for (int sb = 0; sb < C::SUB; ++sb) {
 #pragma unroll
-        for (int d0 = 0; d0 < DH / 2; d0 += 32) {
-          uint32_t v[16];
-          tc_ld_16x256b_x4(tmem + lanes_of(sb) + hf * (DH / 2) + d0, v);
-          tc_wait_ld();
+          for (int d0 = 0; d0 < DH / 2; d0 += 32) {
+            uint32_t v[16];
+            tc_ld_16x256b_x4(tmem + lanes_of(sb) + hf * (DH / 2) + d0, v);
+            tc_wait_ld();
 #pragma unroll
-          for (int gq = 0; gq < 4; ++gq)
+            for (int gq = 0; gq < 4; ++gq)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+              for (int h = 0; h < 2; ++h)
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int i = 2 * sb + h, d = 2 * (d0 / 8 + gq) + e;
-                if constexpr (!ONE) o_acc[i][d] = o_acc[i][d] * alpha[i] + __uint_as_float(v[4 * gq + 2 * h + e]);
-              }
+                for (int e = 0; e < 2; ++e) {
+                  const int i = 2 * sb + h, d = 2 * (d0 / 8 + gq) + e;
+                  o_acc[i][d] = o_acc[i][d] * alpha[i] + __uint_as_float(v[4 * gq + 2 * h + e]);
+                }
+          }
         }
+        tc_fence_before();
+        mbarrier_arrive_one(o_free);
       }
-      tc_fence_before();
-      mbarrier_arrive_one(o_free);
     }
     // full row sums: over the 4 threads of each row, then the warp pair
 #pragma unroll

@@ -11,16 +11,19 @@
 // hint: each byte is used once per launch.
 //
 // Activations may come as an exact pair of bf16 terms (x = hi + lo, the
-// residual of rounding x to bf16 rounded again): the kernel then issues two
-// MMAs per k-slice into the same accumulator, W.hi + W.lo, so the product
+// residual of rounding x to bf16 rounded again): the two tiles form one
+// K-major operand of 2 BN rows, so one MMA per k-slice yields W.hi and W.lo
+// side by side in the accumulator and the epilogue adds them; the product
 // keeps about 16 significant bits of x while both MMA operands stay bf16.
 //
-// E4M3 weights (W8): TMA brings the 8-bit codes (half the bytes of bf16),
-// four converter warps turn each weight row into exact bf16 values in
-// registers and store them into TMEM (tcgen05.st), and the MMA takes its A
-// operand from TMEM.  The per-row scale multiplies the accumulator row in
-// the epilogue.  The projections are HBM-bound at decode sizes, so halving
-// the weight bytes is the point; the conversion runs beside the stream.
+// E4M3 weights (W8): TMA brings the 8-bit codes (half the bytes of bf16)
+// into a ring of their own; eight converter warps (two per TMEM lane
+// quadrant) turn each weight row into exact bf16 values in registers and
+// store them into TMEM (tcgen05.st); the MMA takes its A operand from TMEM
+// and the activations from a second ring.  The per-row scale multiplies the
+// accumulator row in the epilogue.  The projections are HBM-bound at decode
+// sizes, so halving the weight bytes is the point; the conversion runs
+// beside the stream.
 #pragma once
 
 #include <cudaTypedefs.h>

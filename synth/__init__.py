@@ -152,6 +152,11 @@ MINI_CONFIGS: Dict[str, DraftConfig] = {
                            hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=128,
                            ffn=1328, vocab=5000, n_taps=3, tap_width=448,
                            match_prob=0.8, rounds=3, seed=2005, weight_format="e4m3"),
+    # FP8 projection weights with S = 2 and stochastic acceptance (dh = 64, G = 8)
+    "mini_w8b": DraftConfig("mini_w8b", batch=4, ctx_lo=1, ctx_hi=200, n_layers=2,
+                            hidden=384, n_q_heads=16, n_kv_heads=2, head_dim=64,
+                            ffn=784, vocab=3001, n_taps=3, tap_width=384,
+                            s_passes=2, accept="stochastic", rounds=3, seed=2006, weight_format="e4m3"),
     # fp32 mini: ragged, several pages, G = 2
     "mini_f32": DraftConfig("mini_f32", batch=2, ctx_lo=17, ctx_hi=90, n_layers=2,
                             hidden=192, n_q_heads=6, n_kv_heads=3, head_dim=32,

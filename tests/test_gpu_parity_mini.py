@@ -13,11 +13,11 @@ from harness import Pair
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["c1", "mini_f32", "mini_a", "mini_b", "mini_c", "mini_w8"])
+@pytest.mark.parametrize("name", ["c1", "mini_f32", "mini_a", "mini_b", "mini_c", "mini_w8", "mini_w8b"])
 def test_chain_parity(name):
     import torch
     cfg = synth.get_config(name)
-    if name == "mini_b":
+    if name in ("mini_b", "mini_w8b"):
         cfg = cfg.replace(weight_std=0.06)   # peaked confidences: a well-separated S = 2 commit order
     rounds = 3
     pair = Pair(cfg, rounds)
