@@ -181,14 +181,14 @@ int gemm_blocks_per_sm(int bn, bool split, bool w8) {
 
 // Split-K count for `n_tiles` output tiles of width bn.  A CTA streams its
 // weights at a fraction of the HBM bandwidth an SM can draw, so the grid
-// must keep every SM streaming: aim for about 1.25 CTAs per SM (all
-// resident at once, at most max_ctas when positive), with at most 8 splits
-// (a portable cluster) and at least 4 k-blocks per split; normalised so that
-// every split owns a k-block.
+// must keep every SM streaming: aim for about 1.5 CTAs per SM (all resident
+// at once, at most max_ctas when positive; measured on the c2 round against
+// 1.0, 1.25, 1.75 and 2.0), with at most 8 splits (a portable cluster) and at
+// least 4 k-blocks per split; normalised so that every split owns a k-block.
 int gemm_splits(int n_tiles, int n_kb, int bn, bool split, int num_sms, int max_ctas, bool w8) {
   int cap = gemm_blocks_per_sm(bn, split, w8) * num_sms;
   if (max_ctas > 0) cap = std::min(cap, max_ctas);
-  const int want = std::min(cap, (5 * num_sms + 3) / 4);
+  const int want = std::min(cap, (3 * num_sms + 1) / 2);
   int s = (want + n_tiles - 1) / n_tiles;
   while (s > 1 && n_tiles * s > cap) --s;
   s = std::max(1, std::min({s, 8, n_kb / 4}));

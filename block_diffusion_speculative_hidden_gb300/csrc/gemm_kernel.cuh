@@ -64,10 +64,10 @@ struct TcCfg {
   static constexpr int XPAIR = (SPLIT ? 2 : 1) * X_BOX;            // the hi (and lo) box of one 64-k block
   static constexpr int XS = KB_PER_STAGE * XPAIR;                  // activation bytes per stage
   static constexpr int STAGE_BYTES = W_BYTES + XS;
-  // Shared memory for the rings.  BN = 16 (single-sequence drafting): about
-  // 100 KB, so that a CTA fits beside another one or beside an attention
-  // CTA; BN 32-64: two CTAs per SM; wider tiles: one CTA with deeper rings
-  static constexpr int BUDGET = BN <= 16 ? (W8 ? 104 : 90) * 1024 : BN <= 64 ? 110 * 1024 : 200 * 1024;
+  // Shared memory for the rings.  BN <= 64: about 100-110 KB, two CTAs per
+  // SM (BN = 16, single-sequence drafting: five bf16 stages; measured faster
+  // than four on the c2 round); wider tiles: one CTA with deeper rings
+  static constexpr int BUDGET = BN <= 16 ? (W8 ? 104 : 108) * 1024 : BN <= 64 ? 110 * 1024 : 200 * 1024;
   // One MMA covers both activation terms: their tiles lie back to back in
   // shared memory (hi rows, then lo rows), so they form one K-major operand
   // of 2 BN rows and the accumulator holds W.hi in columns 0 .. BN - 1 and
