@@ -80,9 +80,19 @@ struct MmaAttnCfg {
   static_assert((P_IN_K ? OFF_KV + (NST - 1) * STAGE_BYTES : OFF_P) + (P_CHUNKS - 1) * P_CH + M * 128 <=
                     OFF_BAR + BAR_BYTES,
                 "P padding rows stay inside");
-  // the staged rows [R][DH + 4] and the received split partials [splits][rows
-  // per split][DH + 4] (at most R + kMergeMax rows) reuse Q, P and the ring
-  static_assert((2 * R + kMergeMax) * (DH + 4) * 4 <= OFF_BAR, "split partials must fit");
+  // a split merge stages its rows [R][DH + 4] and receives the partials
+  // [splits][rows per split][DH + 4] in Q, P and the ring: the largest split
+  // count (at most kMergeMax) whose merge fits (one split needs no merge)
+  static constexpr int merge_rows(int S) { return R + S * ((R + S - 1) / S); }
+  static constexpr int max_merge() {
+    int m = 1;
+    for (int S = 2; S <= kMergeMax; ++S)
+      if (merge_rows(S) * (DH + 4) * 4 <= OFF_BAR) m = S;
+    return m;
+  }
+  static constexpr int MAX_MERGE = max_merge();
+  // the 8-page variants merge any split count
+  static_assert(KBP < 8 || MAX_MERGE == kMergeMax, "split partials must fit");
 };
 
 struct MmaAttnParams {
@@ -717,13 +727,16 @@ int max_clusters_t(dflash_ctx* c, int splits) {
 constexpr int kShortPages = 13;
 
 // The streaming variant with 4-page key blocks: half the shared memory and
-// at most 102 registers a thread, so two CTAs share an SM (for long prefixes
-// streamed through one CTA, as in the training-time block attention).  It
-// exists where the split partials still fit its smaller ring.
+// at most 102 registers a thread, so two CTAs share an SM.  It serves grids
+// with more (sequence, kv head) problems than SMs (the serving batches, the
+// training-time block attention), where each CTA streams a long prefix and
+// twice the CTAs an SM hide its latency chain; with few problems and long
+// contexts (c4) the 8-page ring streams faster.  It exists where its layout
+// fits, and serves the split counts whose merge fits its smaller ring.
 template <int DH, int G>
 constexpr bool narrow_fits() {
-  // MmaAttnCfg<DH, G, 4, 2>'s layout and its three static checks, computed
-  // here without instantiating it (its checks would fail to compile)
+  // the Q and P padding checks of MmaAttnCfg<DH, G, 4, 2>, computed here
+  // without instantiating it
   constexpr int KBP = 4, NST = 2, R = G * 16, M = R <= 64 ? 64 : 128, NCH = DH / 64;
   constexpr int Q_CH = R * 128, P_CH = R * 128, P_CHUNKS = (KBP * 16 + 63) / 64;
   constexpr int KV_BYTES = NCH * KBP * 16 * 128, STAGE = 2 * KV_BYTES;
@@ -731,9 +744,15 @@ constexpr bool narrow_fits() {
   constexpr int OFF_KV = NCH * Q_CH + (P_IN_K ? 0 : P_CHUNKS * P_CH);
   constexpr int OFF_BAR = OFF_KV + NST * STAGE;
   constexpr int END = OFF_BAR + 128 + 8 * 32 * (2 * (M / 64)) * 4;
-  return (NCH - 1) * Q_CH + M * 128 <= END &&
-         (P_IN_K ? OFF_KV + (NST - 1) * STAGE : NCH * Q_CH) + (P_CHUNKS - 1) * P_CH + M * 128 <= END &&
-         (2 * R + kMergeMax) * (DH + 4) * 4 <= OFF_BAR;
+  // (128 query rows of 128 dims do not fit 102 registers a thread)
+  return DH * G <= 512 && (NCH - 1) * Q_CH + M * 128 <= END &&
+         (P_IN_K ? OFF_KV + (NST - 1) * STAGE : NCH * Q_CH) + (P_CHUNKS - 1) * P_CH + M * 128 <= END;
+}
+
+template <int DH, int G>
+int narrow_max_merge() {
+  if constexpr (narrow_fits<DH, G>()) return MmaAttnCfg<DH, G, 4, 2>::MAX_MERGE;
+  else return 0;
 }
 
 // Runs F<DH, G, KBP, NST>(args) for the kernel instance serving `splits`.
@@ -745,8 +764,9 @@ auto dispatch(dflash_ctx* c, int splits, bool narrow, A... args) {
 #define DFLASH_ATTN_CASE(DH_, G_)                                                              \
   if (c->cfg.head_dim == DH_ && G == G_)                                                       \
     return short_split ? F<DH_, G_, kShortPages, 1>::run(c, splits, args...)                   \
-           : narrow ? F<DH_, G_, narrow_fits<DH_, G_>() ? 4 : 8, 2>::run(c, splits, args...)   \
-                    : F<DH_, G_, 8, 2>::run(c, splits, args...);
+           : narrow && splits <= narrow_max_merge<DH_, G_>()                                   \
+               ? F<DH_, G_, narrow_fits<DH_, G_>() ? 4 : 8, 2>::run(c, splits, args...)         \
+               : F<DH_, G_, 8, 2>::run(c, splits, args...);
   DFLASH_ATTN_CASE(64, 1) DFLASH_ATTN_CASE(64, 2) DFLASH_ATTN_CASE(64, 4) DFLASH_ATTN_CASE(64, 8)
   DFLASH_ATTN_CASE(128, 1) DFLASH_ATTN_CASE(128, 2) DFLASH_ATTN_CASE(128, 4) DFLASH_ATTN_CASE(128, 8)
 #undef DFLASH_ATTN_CASE
@@ -781,7 +801,7 @@ int attention_mma_splits(dflash_ctx* c, int B) {
   const int s0 = std::max(1, std::min({kMergeMax, (2 * c->num_sms + heads - 1) / heads, c->attn_max_splits}));
   for (int S = s0; S > 1; --S) {
     int& n = c->attn_fit[S];
-    if (n == 0) n = std::max(-1, dispatch<ClustersF>(c, S, false));
+    if (n == 0) n = std::max(-1, dispatch<ClustersF>(c, S, heads > c->num_sms));
     if (n >= heads) return S;
   }
   return s0;
@@ -789,7 +809,7 @@ int attention_mma_splits(dflash_ctx* c, int B) {
 
 cudaError_t launch_attention_mma(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
                                  const AttnSrc& src) {
-  return dispatch<LaunchF>(c, splits, src.narrow, layer, B, s, &next, &src);
+  return dispatch<LaunchF>(c, splits, B * c->cfg.n_kv_heads > c->num_sms, layer, B, s, &next, &src);
 }
 
 }  // namespace dflash

@@ -65,7 +65,6 @@ struct AttnSrc {
   const int32_t* row_of = nullptr;   // page-table row of block b (null: row b)
   const int32_t* seq_len = nullptr;  // context length of block b (null: the context's seq_len)
   bool pdl = true;                   // false: the immediate predecessor wrote row_of / seq_len
-  bool narrow = false;               // long prefixes: the 4-page streaming variant, two CTAs an SM
 };
 
 struct TmapEntry {

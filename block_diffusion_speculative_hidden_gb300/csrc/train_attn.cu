@@ -81,8 +81,7 @@ cudaError_t launch_block_attention(dflash_ctx* c, int layer, int NB, const int32
   AttnSrc src;
   src.row_of = c->blk_row;
   src.seq_len = c->blk_len;
-  src.pdl = false;     // the staging kernel just wrote the rows and lengths
-  src.narrow = true;   // every block streams its whole prefix: two CTAs an SM
+  src.pdl = false;  // the staging kernel just wrote the rows and lengths
   e = launch_attention(c, layer, NB, attn_splits(c, NB), s, NextGemm{}, src);
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(NB) * kBlockK * qd;
