@@ -842,7 +842,7 @@ def main(argv=None):
         "roofline": roof,
         "kernels": per_class,
         "cpu_baseline": cpu,
-        "accepted_tok_per_s": cfg.batch * (res["mean_tau"] + 1) / (res["ms"] / steps / 1e3),
+        "accepted_tok_per_s": world * cfg.batch * (res["mean_tau"] + 1) / (res["ms"] / steps / 1e3),
         "prefill_inject": res["wl"].prefill,
         "e2e": res["e2e"],
         "graph": res["graph"],
