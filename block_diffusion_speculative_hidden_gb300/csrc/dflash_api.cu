@@ -156,6 +156,10 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   const size_t d_tiles = ceil_div(d, kTileN);
   auto ss_x = static_cast<float*>(w.take(sizeof(float) * d_tiles * M));
   auto ss_h = static_cast<float*>(w.take(sizeof(float) * d_tiles * R));
+  const size_t Mc = M / 2;  // S = 2: the uncommitted half of the block rows
+  void* ac = lo ? w.take(Mc * d * e) : nullptr;
+  void* ac_lo = lo ? w.take(Mc * d * e) : nullptr;
+  auto ss_c = lo ? static_cast<float*>(w.take(sizeof(float) * d_tiles * Mc)) : nullptr;
   if (c != nullptr) {
     c->status = status;
     c->scal = status + 4;
@@ -190,6 +194,9 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
     c->commit = commit;
     c->ss_x = ss_x;
     c->ss_h = ss_h;
+    c->ac = ac;
+    c->ac_lo = ac_lo;
+    c->ss_c = ss_c;
   }
   return w.off;
 }
@@ -585,20 +592,28 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         DF_RUN(run_gemm(ctx, ctx->w_down[l], w_row_scale(ctx->s_down, l), d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, e, s));
       }
     }
-    EpiArgs fin = epi_base(ctx, EPI_NONE, M, g.vocab);  // the final norm, folded into the LM head
-    norm_in(ctx, fin, ctx->ss_x, Mmax);
-    const int32_t* skip = pass == 1 ? ctx->commit : nullptr;
+    // the second pass needs the LM head on its uncommitted rows only: without
+    // a logits store (which wants every row in place) they are compacted first
+    const bool compact = pass == 1 && g.dtype != DFLASH_F32 && logits == nullptr;
+    if (compact) {
+      ProfScope pc(ctx, DFLASH_PROF_ROWWISE, 1, s);
+      DF_CHECK(launch_compact_rows(ctx, B, Mmax, s));
+    }
+    const int Mc = g.max_batch * kBlockK / 2;
+    EpiArgs fin = epi_base(ctx, EPI_NONE, compact ? M / 2 : M, g.vocab);  // the final norm, folded into the LM head
+    norm_in(ctx, fin, compact ? ctx->ss_c : ctx->ss_x, compact ? Mc : Mmax);
+    const int32_t* skip = pass == 1 && !compact ? ctx->commit : nullptr;
     ProfScope plm(ctx, DFLASH_PROF_LMHEAD, g.dtype != DFLASH_F32 ? 1 : 2, s);
     if (g.dtype != DFLASH_F32) {
       GemmLaunch lm{};
       lm.W = ctx->w_lm;
       lm.w_scale = ctx->s_lm;
-      lm.X = ctx->a;
-      lm.X_lo = ctx->a_lo;
+      lm.X = compact ? ctx->ac : ctx->a;
+      lm.X_lo = compact ? ctx->ac_lo : ctx->a_lo;
       lm.N = g.vocab;
       lm.K = d;
-      lm.M = M;
-      lm.M_alloc = Mmax;
+      lm.M = compact ? M / 2 : M;
+      lm.M_alloc = compact ? Mc : Mmax;
       lm.splits = 1;
       lm.lm = ctx->lm;
       lm.logits = logits;
@@ -628,7 +643,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
       DF_CHECK(launch_lm_merge(ctx, M, nullptr, ctx->tok1, ctx->conf1, s));
       DF_CHECK(launch_commit(ctx, B, s));
     } else {
-      DF_CHECK(launch_lm_merge(ctx, M, ctx->commit, draft_tokens, conf, s));
+      DF_CHECK(launch_lm_merge(ctx, M, ctx->commit, draft_tokens, conf, s, compact));
     }
   }
   if (committed != nullptr) {

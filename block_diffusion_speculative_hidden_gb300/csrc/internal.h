@@ -127,6 +127,10 @@ struct dflash_ctx {
   // folded RMSNorm: partial sums of squares, [ceil(hidden/128)][rows]
   float* ss_x;   // draft rows (row stride max_batch * 16)
   float* ss_h;   // inject rows (row stride max_inject_rows)
+  // S = 2, second pass: the uncommitted rows compacted for the LM head
+  // (bf16 family): [max_batch * K/2][hidden] twice, partial sums [ceil(hidden/128)][max_batch * K/2]
+  void *ac = nullptr, *ac_lo = nullptr;
+  float* ss_c = nullptr;
   // stream being recorded into a graph (dflash_graph_begin), else null
   cudaStream_t capture = nullptr;
   bool capturing = false;

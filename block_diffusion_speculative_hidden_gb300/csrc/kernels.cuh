@@ -22,7 +22,9 @@ cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, cudaStream_t s)
 cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, const EpiArgs& norm,
                                 cudaStream_t s);
 cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,
-                            cudaStream_t s);
+                            cudaStream_t s, bool compact = false);
+// S = 2, second pass: the uncommitted rows' LM-head inputs into c->ac / ac_lo / ss_c
+cudaError_t launch_compact_rows(dflash_ctx* c, int B, int Mmax, cudaStream_t s);
 cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s);
 
 // attention.cu

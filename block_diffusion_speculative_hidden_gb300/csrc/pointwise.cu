@@ -132,8 +132,12 @@ __device__ __forceinline__ void lm_fold(float& mx, float& se, int& ix, float om,
   se = ns;
 }
 
+// compact (S = 2, second pass): the LM head ran on the uncommitted rows
+// only, sequence b's in position order at rows b * K/2 ...; row m takes its
+// partials from there.
 __global__ void __launch_bounds__(256) k_lm_merge(LmPartials lm, int M, const int32_t* commit, const int32_t* tok1,
-                                                  const float* conf1, int32_t* tok_out, float* conf_out) {
+                                                  const float* conf1, int32_t* tok_out, float* conf_out,
+                                                  int compact) {
   __shared__ float s_mx[8], s_se[8];
   __shared__ int s_ix[8];
   pdl_wait();
@@ -147,7 +151,14 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmPartials lm, int M, const in
     }
     return;
   }
-  const long long base = static_cast<long long>(m) * lm.n_tiles;
+  int prow = m;
+  if (compact) {
+    const int b = m / kBlockK, i = m % kBlockK;
+    int rank = 0;
+    for (int j = 0; j < i; ++j) rank += commit[b * kBlockK + j] == 0 ? 1 : 0;
+    prow = b * (kBlockK / 2) + rank;
+  }
+  const long long base = static_cast<long long>(prow) * lm.n_tiles;
   float mx = -INFINITY, se = 0.f;
   int ix = 0x7fffffff;
   for (int t = threadIdx.x; t < lm.n_tiles; t += blockDim.x) lm_fold(mx, se, ix, lm.mx[base + t], lm.se[base + t], lm.idx[base + t]);
@@ -167,6 +178,38 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmPartials lm, int M, const in
     tok_out[m] = ix;
     if (conf_out != nullptr) conf_out[m] = 1.f / se;
   }
+}
+
+// S = 2, second pass: the K/2 uncommitted rows of each sequence, in position
+// order, into compact rows b * K/2 + r (the two bf16 terms of the LM head's
+// input and their folded-norm partial sums), so that the LM head runs on
+// them alone.  One CTA per compact row.
+__global__ void k_compact_rows(const int32_t* __restrict__ commit, const __nv_bfloat16* __restrict__ a,
+                               const __nv_bfloat16* __restrict__ a_lo, const float* __restrict__ ss, int ss_ld,
+                               int d_tiles, int d, __nv_bfloat16* ac, __nv_bfloat16* ac_lo, float* ssc, int ssc_ld) {
+  __shared__ int s_m;
+  pdl_wait();
+  pdl_trigger();
+  const int j = blockIdx.x, b = j / (kBlockK / 2), r = j % (kBlockK / 2);
+  if (threadIdx.x == 0) {
+    int m = -1;
+    for (int i = 0, cnt = 0; i < kBlockK; ++i)
+      if (commit[b * kBlockK + i] == 0) {
+        if (cnt == r) m = b * kBlockK + i;
+        ++cnt;
+      }
+    s_m = m;
+  }
+  __syncthreads();
+  const int m = s_m;  // exactly K/2 rows of every sequence are uncommitted
+  const long long src = static_cast<long long>(m) * d, dst = static_cast<long long>(j) * d;
+  for (int e = threadIdx.x; e < d / 8; e += blockDim.x) {
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(ac + dst)[e] = m >= 0 ? reinterpret_cast<const uint4*>(a + src)[e] : zero;
+    reinterpret_cast<uint4*>(ac_lo + dst)[e] = m >= 0 ? reinterpret_cast<const uint4*>(a_lo + src)[e] : zero;
+  }
+  for (int t = threadIdx.x; t < d_tiles; t += blockDim.x)
+    ssc[static_cast<long long>(t) * ssc_ld + j] = m >= 0 ? ss[static_cast<long long>(t) * ss_ld + m] : 0.f;
 }
 
 // S = 2: commit the K/2 most confident positions of each block (ties to the
@@ -228,9 +271,17 @@ cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const 
 }
 
 cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool compact) {
   return launch_k(k_lm_merge, dim3(M), dim3(256), 0, s, dim3(1), c->pdl, c->lm, M, commit, c->tok1, c->conf1,
-                  tok_out, conf_out);
+                  tok_out, conf_out, compact ? 1 : 0);
+}
+
+cudaError_t launch_compact_rows(dflash_ctx* c, int B, int Mmax, cudaStream_t s) {
+  const int d = c->cfg.hidden, d_tiles = (d + kTileN - 1) / kTileN;
+  return launch_k(k_compact_rows, dim3(B * kBlockK / 2), dim3(128), 0, s, dim3(1), c->pdl, c->commit,
+                  static_cast<const __nv_bfloat16*>(c->a), static_cast<const __nv_bfloat16*>(c->a_lo), c->ss_x, Mmax,
+                  d_tiles, d, static_cast<__nv_bfloat16*>(c->ac), static_cast<__nv_bfloat16*>(c->ac_lo), c->ss_c,
+                  c->cfg.max_batch * kBlockK / 2);
 }
 
 cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s) {

@@ -89,3 +89,25 @@ def test_pool_exhaustion_changes_nothing():
     dr.reset()
     assert dr.device_status() == 0 and dr.seq_len.tolist() == [0, 0]
     dr.close()
+
+
+@pytest.mark.parametrize("name", ["mini_b", "mini_w8b"])
+def test_second_pass_lm_head_on_uncommitted_rows_only(name):
+    """S = 2: without a logits store the second pass runs the LM head on the
+    K/2 uncommitted rows only (compacted); drafts and confidences equal the
+    path that computes and stores every row's logits, bit for bit (that
+    path is the one checked against the oracle above)."""
+    import torch
+    cfg = synth.get_config(name).replace(weight_std=0.06)
+    pair = Pair(cfg, 2)
+    pair.prefill()
+    dr = pair.gpu
+    B = cfg.batch
+    logits = torch.empty((B, 16, cfg.vocab), dtype=torch.float32, device="cuda")
+    com = torch.empty((B, 16), dtype=torch.int32, device="cuda")
+    tok_full, conf_full, _, _ = dr.draft_block(B, 2, logits=logits, committed=com)
+    tok_c, conf_c, _, _ = dr.draft_block(B, 2)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    assert torch.equal(tok_full, tok_c)
+    assert torch.equal(conf_full, conf_c)
