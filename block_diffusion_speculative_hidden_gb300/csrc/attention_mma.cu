@@ -19,7 +19,9 @@
 //     block's K tile, the A operand of the next MMA) and the running sums;
 //     O_blk = P V reuses the same TMEM columns (V enters as an MN-major
 //     operand); the threads fold O_blk into fp32 registers with the
-//     online-softmax rescale;
+//     online-softmax rescale; in the pipelined variants (4-page blocks,
+//     dh 64: two S and two O buffers in TMEM) S of the next block and P V of
+//     this one run while the softmax works, and O is folded a block late;
 //   - only the real query rows of Q and P are stored: the MMA's padding rows
 //     (G*16 .. 127) read whatever follows in shared memory, and the results
 //     in those rows are never used;
@@ -49,14 +51,29 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9;
 // r in lane r.  The softmax reads 16-lane blocks with the 16x256b shape:
 // thread t of the warp gets rows t/4 and t/4 + 8 of the block, columns
 // 2*(t%4) and 2*(t%4) + 1 of every 8-column group.
+//
+// Columns (256 a CTA, two CTAs an SM): S at column 0 and O = P V over it,
+// folded into registers before the next block's S, except in the pipelined
+// variants (4-page key blocks whose two S and two O buffers fit: dh 64).
+// There S of the next key block is computed while the softmax turns this
+// block's S into P, and O of a block is folded one block late (after the
+// next block's P is written), so the P V product runs under the softmax too.
 template <int DH, int G, int KBP, int NST>
-struct MmaAttnCfg {
+struct MmaAttnLayout {
   static constexpr int R = G * 16;                 // real query rows
   static constexpr int M = R <= 64 ? 64 : 128;     // MMA rows
   static constexpr int SUB = M / 64;               // 16-lane row blocks per TMEM quadrant
   static constexpr int QUADS = R <= 64 ? R / 16 : 4;  // quadrants holding real rows
   static constexpr int RPT = 2 * SUB;              // rows per softmax thread
   static constexpr int NCH = DH / 64;              // 128-byte column chunks of a head
+  static constexpr bool ONE = NST == 1;            // the split is one key block
+  static constexpr int SW = 16 * KBP;              // S columns of a key block
+  static constexpr int TMEM_COLS = 256;
+  static constexpr bool PIPE = !ONE && KBP <= 4 && 2 * SW + 2 * DH <= TMEM_COLS;
+  static constexpr int NSB = PIPE ? 2 : 1;         // S buffers
+  static constexpr int NO = PIPE ? 2 : 1;          // O buffers
+  __host__ __device__ static constexpr int s_col(int j) { return PIPE ? j * SW : 0; }
+  __host__ __device__ static constexpr int o_col(int j) { return PIPE ? 2 * SW + j * DH : 0; }
   static constexpr int Q_CH = R * 128;             // stride of the Q chunks (real rows only)
   static constexpr int Q_BYTES = NCH * Q_CH;
   static constexpr int P_CHUNKS = (KBP * 16 + 63) / 64;
@@ -65,21 +82,25 @@ struct MmaAttnCfg {
   static constexpr int KV_CH = KBP * 16 * 128;     // one 64-column chunk of the K (or V) tile
   static constexpr int KV_BYTES = NCH * KV_CH;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K then V
-  // P overwrites the block's K tile (dead once S is computed) when it fits
+  // P overwrites the block's K tile (dead once S is computed) when it fits;
+  // otherwise it has a buffer per O buffer (P of the next block is written
+  // while the P V product of this one may still read its buffer)
   static constexpr bool P_IN_K = P_BYTES <= KV_BYTES;
+  static constexpr int NPB = P_IN_K ? 0 : NO;
+  __host__ __device__ static constexpr int p_off(int blk) { return NPB > 1 ? (blk % (NPB > 1 ? NPB : 1)) * P_BYTES : 0; }
   static constexpr int OFF_P = Q_BYTES;
-  static constexpr int OFF_KV = OFF_P + (P_IN_K ? 0 : P_BYTES);
+  static constexpr int OFF_KV = OFF_P + NPB * P_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NST * STAGE_BYTES;
-  static constexpr int BAR_BYTES = 128 + 8 * 32 * RPT * 4;  // barriers, then the pair-exchange slots
+  static constexpr int BAR_AREA = 256;             // mbarriers and the TMEM address
+  static constexpr int BAR_BYTES = BAR_AREA + 8 * 32 * RPT * 4;  // then the pair-exchange slots
   static constexpr int SMEM_FIXED = 1024 + OFF_BAR + BAR_BYTES;  // + 4 bytes per page id
-  static constexpr int TMEM_COLS = 256;
-  static_assert(KBP * 16 <= 256 && DH <= 256, "S and O share 256 TMEM columns");
   // the padding rows (R .. M-1) of the last Q / P chunk read into the
   // following buffers, never past the allocation
-  static_assert((NCH - 1) * Q_CH + M * 128 <= OFF_BAR + BAR_BYTES, "Q padding rows stay inside");
-  static_assert((P_IN_K ? OFF_KV + (NST - 1) * STAGE_BYTES : OFF_P) + (P_CHUNKS - 1) * P_CH + M * 128 <=
-                    OFF_BAR + BAR_BYTES,
-                "P padding rows stay inside");
+  static constexpr bool q_padding_inside = (NCH - 1) * Q_CH + M * 128 <= OFF_BAR + BAR_BYTES;
+  static constexpr bool p_padding_inside =
+      (P_IN_K ? OFF_KV + (NST - 1) * STAGE_BYTES : OFF_P + (NPB - 1) * P_BYTES) + (P_CHUNKS - 1) * P_CH +
+          M * 128 <=
+      OFF_BAR + BAR_BYTES;
   // a split merge stages its rows [R][DH + 4] and receives the partials
   // [splits][rows per split][DH + 4] in Q, P and the ring: the largest split
   // count (at most kMergeMax) whose merge fits (one split needs no merge)
@@ -91,8 +112,19 @@ struct MmaAttnCfg {
     return m;
   }
   static constexpr int MAX_MERGE = max_merge();
+};
+
+template <int DH, int G, int KBP, int NST>
+struct MmaAttnCfg : MmaAttnLayout<DH, G, KBP, NST> {
+  using L = MmaAttnLayout<DH, G, KBP, NST>;
+  static_assert(KBP * 16 <= 256 && DH <= 256, "one MMA's N");
+  static_assert(L::PIPE ? 2 * L::SW + 2 * DH <= L::TMEM_COLS : KBP * 16 <= L::TMEM_COLS && DH <= L::TMEM_COLS,
+                "S and O buffers fit the allocation");
+  static_assert((2 * NST + 11) * 8 <= L::BAR_AREA, "barriers fit their area");
+  static_assert(L::q_padding_inside, "Q padding rows stay inside");
+  static_assert(L::p_padding_inside, "P padding rows stay inside");
   // the 8-page variants merge any split count
-  static_assert(KBP < 8 || MAX_MERGE == kMergeMax, "split partials must fit");
+  static_assert(KBP < 8 || L::MAX_MERGE == kMergeMax, "split partials must fit");
 };
 
 struct MmaAttnParams {
@@ -160,13 +192,13 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_empty = kv_full + NST;
   uint64_t* q_full = kv_empty + NST;
-  uint64_t* s_full = q_full + 1;
-  uint64_t* p_full = q_full + 2;
-  uint64_t* o_full = q_full + 3;
-  uint64_t* o_free = q_full + 4;
-  uint64_t* recv_bar = q_full + 5;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 6);
-  float* s_red = reinterpret_cast<float*>(smem + C::OFF_BAR + 128);  // [8 warps][32 lanes][2] pair exchange
+  uint64_t* s_full = q_full + 1;  // [2]: per S buffer
+  uint64_t* p_full = q_full + 3;  // [2]: per S buffer (P of the block in it is written)
+  uint64_t* o_full = q_full + 5;  // [2]: per O buffer
+  uint64_t* o_free = q_full + 7;  // [2]: per O buffer (folded into registers)
+  uint64_t* recv_bar = q_full + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 10);
+  float* s_red = reinterpret_cast<float*>(smem + C::OFF_BAR + C::BAR_AREA);  // [8 warps][32 lanes][RPT] pair exchange
   int* s_pages = reinterpret_cast<int*>(smem + C::OFF_BAR + C::BAR_BYTES);
 
   const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -187,10 +219,12 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(q_full, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, SOFT);
-    mbar_init(o_full, 1);
-    mbar_init(o_free, SOFT);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&s_full[j], 1);
+      mbar_init(&p_full[j], SOFT);
+      mbar_init(&o_full[j], 1);
+      mbar_init(&o_free[j], SOFT);
+    }
     mbar_init(recv_bar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -217,7 +251,8 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
   // dims of O).  Thread state: RPT rows x (2 of every 8 of its head dims).
   // With a single stage the split is one key block (np <= page_slots <= KBP)
   // and O stays in TMEM until the output; otherwise it is folded into
-  // registers with the online-softmax rescale.
+  // registers with the online-softmax rescale (one block late where there
+  // are two O buffers).
   constexpr int RPT = C::RPT, OG = DH / 16;  // 8-column groups per half of the head dims
   constexpr bool ONE = NST == 1;
   const int qd = warp & 3, hf = warp >> 2;
@@ -302,33 +337,47 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer.  Serial variants: S(j) (over the columns
+    // of O(j - 1), once the softmax has folded it), PV(j) once P(j) is
+    // written.  Pipelined: tensor-pipe order S(0), S(1), PV(0), S(2), PV(1),
+    // ...; S(j) reuses the buffer of S(j - 2), whose P was waited for before
+    // PV(j - 2), and PV(j) the O buffer of PV(j - 2), once the softmax has
+    // folded that.
     if (lane == 0) {
-      bool ok = nblk == 0 || mbar_wait(q_full, 0, p.status);
-      for (int blk = 0; ok && blk < nblk; ++blk) {
-        const int s = blk % NST;
-        const int npb = min(KBP, np - blk * KBP);
-        if (!mbar_wait(&kv_full[s], (blk / NST) & 1, p.status)) break;
-        if (blk > 0 && !mbar_wait(o_free, (blk - 1) & 1, p.status)) break;
+      const uint32_t aq = smem_u32(sQ);
+      auto issue_s = [&](int j) {
+        const int s = j % NST, npb = min(KBP, np - j * KBP);
+        if (!mbar_wait(&kv_full[s], (j / NST) & 1, p.status)) return false;
+        if (!C::PIPE && j > 0 && !mbar_wait(&o_free[0], (j - 1) & 1, p.status)) return false;
         tc_fence_after();
-        const uint32_t aq = smem_u32(sQ), ak = smem_u32(sKV + s * C::STAGE_BYTES);
-        const uint32_t av = ak + C::KV_BYTES, ap = C::P_IN_K ? ak : smem_u32(sP);
+        const uint32_t ak = smem_u32(sKV + s * C::STAGE_BYTES);
         const uint32_t id_s = mma_idesc_f16_f32(C::M, 16 * npb, false);
 #pragma unroll
         for (int ks = 0; ks < DH / 16; ++ks) {
           const uint32_t off = (ks & 3) * 32;
-          tc_mma_bf16(tmem, sw128_desc(aq + (ks >> 2) * C::Q_CH + off, 16, 1024),
+          tc_mma_bf16(tmem + C::s_col(j % C::NSB), sw128_desc(aq + (ks >> 2) * C::Q_CH + off, 16, 1024),
                       sw128_desc(ak + (ks >> 2) * C::KV_CH + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
         }
-        tc_commit(s_full);
-        if (!mbar_wait(p_full, blk & 1, p.status)) break;
+        tc_commit(&s_full[j % C::NSB]);
+        return true;
+      };
+      bool ok = nblk == 0 || (mbar_wait(q_full, 0, p.status) && issue_s(0));
+      for (int blk = 0; ok && blk < nblk; ++blk) {
+        if (C::PIPE && blk + 1 < nblk && !issue_s(blk + 1)) break;
+        const int s = blk % NST, npb = min(KBP, np - blk * KBP), ob = blk % C::NO;
+        if (!mbar_wait(&p_full[blk % C::NSB], (blk / C::NSB) & 1, p.status)) break;
+        if (C::PIPE && blk >= 2 && !mbar_wait(&o_free[ob], ((blk - 2) / 2) & 1, p.status)) break;
         tc_fence_after();
+        const uint32_t ak = smem_u32(sKV + s * C::STAGE_BYTES);
+        const uint32_t av = ak + C::KV_BYTES;
+        const uint32_t ap = C::P_IN_K ? ak : smem_u32(sP + C::p_off(blk));
         const uint32_t id_o = mma_idesc_f16_f32(C::M, DH, true);
         for (int k16 = 0; k16 < npb; ++k16)
-          tc_mma_bf16(tmem, sw128_desc(ap + (k16 >> 2) * C::P_CH + (k16 & 3) * 32, 16, 1024),
+          tc_mma_bf16(tmem + C::o_col(ob), sw128_desc(ap + (k16 >> 2) * C::P_CH + (k16 & 3) * 32, 16, 1024),
                       sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, k16 > 0 ? 1u : 0u);
-        tc_commit(o_full);
+        tc_commit(&o_full[ob]);
         tc_commit(&kv_empty[s]);
+        if (!C::PIPE && blk + 1 < nblk && !issue_s(blk + 1)) break;
       }
     }
     __syncwarp();
@@ -337,13 +386,46 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     // barriers, so both always run every block: a wait that gives up only
     // marks the work as failed (status word) and later waits are skipped.
     bool live = true;
+    // O of block f into the registers.  One O buffer: o = o al + O_f with
+    // the rescale al of block f.  Two: O_f is folded one block late, after
+    // the next block's rescale al is known, as o = (o + O_f) al (o then
+    // refers to that block's running max); the last block adds O_f alone.
+    auto fold = [&](int f, const float (&al)[RPT], bool last) {
+      const int ob = f % C::NO;
+      live = live && mbar_wait(&o_full[ob], (f / C::NO) & 1, p.status);
+      __syncwarp();
+      tc_fence_after();
+      // this warp's half of the head dims
+#pragma unroll
+      for (int sb = 0; sb < C::SUB; ++sb) {
+#pragma unroll
+        for (int d0 = 0; d0 < DH / 2; d0 += 32) {
+          uint32_t v[16];
+          tc_ld_16x256b_x4(tmem + lanes_of(sb) + C::o_col(ob) + hf * (DH / 2) + d0, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int i = 2 * sb + h, d = 2 * (d0 / 8 + gq) + e;
+                float& o = o_acc[ONE ? 0 : i][ONE ? 0 : d];
+                const float x = __uint_as_float(v[4 * gq + 2 * h + e]);
+                o = last ? o + x : C::NO == 1 ? o * al[i] + x : (o + x) * al[i];
+              }
+        }
+      }
+      tc_fence_before();
+      mbarrier_arrive_one(&o_free[ob]);
+    };
     for (int blk = 0; blk < nblk; ++blk) {
       const int npb = min(KBP, np - blk * KBP);
       const int vp0 = vp_begin + blk * KBP;
       // this warp's pages of the block: [pg_lo, pg_hi)
       const int pg_split = (npb + 1) >> 1;
       const int pg_lo = hf == 0 ? 0 : pg_split, pg_hi = hf == 0 ? pg_split : npb;
-      live = live && mbar_wait(s_full, blk & 1, p.status);
+      live = live && mbar_wait(&s_full[blk % C::NSB], (blk / C::NSB) & 1, p.status);
       __syncwarp();
       tc_fence_after();
       constexpr int HP = (KBP + 1) / 2;  // pages per warp at most
@@ -356,7 +438,8 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       for (int sb = 0; sb < C::SUB; ++sb)
 #pragma unroll
         for (int j = 0; j < HP; ++j)
-          if (pg_lo + j < pg_hi) tc_ld_16x256b_x2(tmem + lanes_of(sb) + (pg_lo + j) * 16, sv[sb][j]);
+          if (pg_lo + j < pg_hi)
+            tc_ld_16x256b_x2(tmem + lanes_of(sb) + C::s_col(blk % C::NSB) + (pg_lo + j) * 16, sv[sb][j]);
       tc_wait_ld();
       // pass 1: row max over the valid keys
 #pragma unroll
@@ -391,7 +474,7 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         lsum[i] = 0.f;
       }
       // pass 2: P = 2^(S scale - m) in fp16 into the swizzled A operand
-      uint8_t* pbase = C::P_IN_K ? sKV + (blk % NST) * C::STAGE_BYTES : sP;
+      uint8_t* pbase = C::P_IN_K ? sKV + (blk % NST) * C::STAGE_BYTES : sP + C::p_off(blk);
 #pragma unroll
       for (int j = 0; j < HP; ++j) {
         const int pg = pg_lo + j;
@@ -425,35 +508,22 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       for (int i = 0; i < RPT; ++i) l_run[i] = l_run[i] * alpha[i] + lsum[i];
       fence_proxy_async_smem();  // P is read by the tensor cores
       tc_fence_before();
-      mbarrier_arrive_one(p_full);
-      live = live && mbar_wait(o_full, blk & 1, p.status);
-      __syncwarp();
-      tc_fence_after();
+      mbarrier_arrive_one(&p_full[blk % C::NSB]);
       if constexpr (ONE) {
-        break;  // O stays in TMEM (a single block: both warps leave here)
-      } else {
-        // O_blk = P V: this warp's half of the head dims, folded with the rescale
-#pragma unroll
-        for (int sb = 0; sb < C::SUB; ++sb) {
-#pragma unroll
-          for (int d0 = 0; d0 < DH / 2; d0 += 32) {
-            uint32_t v[16];
-            tc_ld_16x256b_x4(tmem + lanes_of(sb) + hf * (DH / 2) + d0, v);
-            tc_wait_ld();
-#pragma unroll
-            for (int gq = 0; gq < 4; ++gq)
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const int i = 2 * sb + h, d = 2 * (d0 / 8 + gq) + e;
-                  o_acc[i][d] = o_acc[i][d] * alpha[i] + __uint_as_float(v[4 * gq + 2 * h + e]);
-                }
-          }
-        }
-        tc_fence_before();
-        mbarrier_arrive_one(o_free);
+        // O stays in TMEM (a single block: both warps leave here)
+        live = live && mbar_wait(&o_full[0], 0, p.status);
+        __syncwarp();
+        tc_fence_after();
+        break;
+      } else if constexpr (C::NO == 1) {
+        fold(blk, alpha, false);
+      } else if (blk > 0) {
+        // O of the previous block: its P V product ran while this block's P was formed
+        fold(blk - 1, alpha, false);
       }
+    }
+    if constexpr (!ONE && C::NO == 2) {
+      if (nblk > 0) fold(nblk - 1, l_run, true);  // (no rescale: al unused)
     }
     // full row sums: over the 4 threads of each row, then the warp pair
 #pragma unroll
@@ -625,9 +695,28 @@ bool q_map(const void* base, int rows, int cols, CUtensorMap* out) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Shared memory of a launch: the layout plus the page ids, raised where
+// needed so that the CTAs one SM can hold never ask for more than its 512
+// TMEM columns.  (An allocation that does not fit waits for another CTA on
+// the SM to free its columns; if that CTA belonged to the same cluster and
+// waited at the split merge, neither would finish.)
 template <int DH, int G, int KBP, int NST>
 int smem_bytes(int page_slots) {
-  return MmaAttnCfg<DH, G, KBP, NST>::SMEM_FIXED + 4 * page_slots;
+  using C = MmaAttnCfg<DH, G, KBP, NST>;
+  static int sm_smem = -1, reserved = 0;
+  if (sm_smem < 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+      cudaGetLastError();
+      sm_smem = 233472;  // 228 KB, the sm_100 family's figure
+      reserved = 1024;
+    }
+  }
+  constexpr int per_sm = 512 / C::TMEM_COLS;  // CTAs whose allocations fit at once
+  const int floor = sm_smem / (per_sm + 1) - reserved + 128;  // (per_sm + 1) CTAs exceed the SM
+  return std::max(C::SMEM_FIXED + 4 * page_slots, (floor + 127) & ~127);
 }
 
 template <int DH, int G, int KBP, int NST>
@@ -735,23 +824,24 @@ constexpr int kShortPages = 13;
 // fits, and serves the split counts whose merge fits its smaller ring.
 template <int DH, int G>
 constexpr bool narrow_fits() {
-  // the Q and P padding checks of MmaAttnCfg<DH, G, 4, 2>, computed here
-  // without instantiating it
-  constexpr int KBP = 4, NST = 2, R = G * 16, M = R <= 64 ? 64 : 128, NCH = DH / 64;
-  constexpr int Q_CH = R * 128, P_CH = R * 128, P_CHUNKS = (KBP * 16 + 63) / 64;
-  constexpr int KV_BYTES = NCH * KBP * 16 * 128, STAGE = 2 * KV_BYTES;
-  constexpr bool P_IN_K = P_CHUNKS * P_CH <= KV_BYTES;
-  constexpr int OFF_KV = NCH * Q_CH + (P_IN_K ? 0 : P_CHUNKS * P_CH);
-  constexpr int OFF_BAR = OFF_KV + NST * STAGE;
-  constexpr int END = OFF_BAR + 128 + 8 * 32 * (2 * (M / 64)) * 4;
   // (128 query rows of 128 dims do not fit 102 registers a thread)
-  return DH * G <= 512 && (NCH - 1) * Q_CH + M * 128 <= END &&
-         (P_IN_K ? OFF_KV + (NST - 1) * STAGE : NCH * Q_CH) + (P_CHUNKS - 1) * P_CH + M * 128 <= END;
+  using L = MmaAttnLayout<DH, G, 4, 2>;
+  return DH * G <= 512 && L::q_padding_inside && L::p_padding_inside;
+}
+
+// Ring depth of the 4-page variant: three stages where it is pipelined and
+// two CTAs still share an SM with room for the page ids (on 128 sequences of
+// 1-8k keys, dh 64, it measured the same as two stages: the loads are not
+// what the softmax waits for), two otherwise.
+template <int DH, int G>
+constexpr int narrow_stages() {
+  using L3 = MmaAttnLayout<DH, G, 4, 3>;
+  return L3::PIPE && L3::q_padding_inside && L3::p_padding_inside && L3::SMEM_FIXED <= 104 * 1024 ? 3 : 2;
 }
 
 template <int DH, int G>
 int narrow_max_merge() {
-  if constexpr (narrow_fits<DH, G>()) return MmaAttnCfg<DH, G, 4, 2>::MAX_MERGE;
+  if constexpr (narrow_fits<DH, G>()) return MmaAttnCfg<DH, G, 4, narrow_stages<DH, G>()>::MAX_MERGE;
   else return 0;
 }
 
@@ -765,7 +855,8 @@ auto dispatch(dflash_ctx* c, int splits, bool narrow, A... args) {
   if (c->cfg.head_dim == DH_ && G == G_)                                                       \
     return short_split ? F<DH_, G_, kShortPages, 1>::run(c, splits, args...)                   \
            : narrow && splits <= narrow_max_merge<DH_, G_>()                                   \
-               ? F<DH_, G_, narrow_fits<DH_, G_>() ? 4 : 8, 2>::run(c, splits, args...)         \
+               ? F<DH_, G_, narrow_fits<DH_, G_>() ? 4 : 8,                                    \
+                   narrow_fits<DH_, G_>() ? narrow_stages<DH_, G_>() : 2>::run(c, splits, args...)  \
                : F<DH_, G_, 8, 2>::run(c, splits, args...);
   DFLASH_ATTN_CASE(64, 1) DFLASH_ATTN_CASE(64, 2) DFLASH_ATTN_CASE(64, 4) DFLASH_ATTN_CASE(64, 8)
   DFLASH_ATTN_CASE(128, 1) DFLASH_ATTN_CASE(128, 2) DFLASH_ATTN_CASE(128, 4) DFLASH_ATTN_CASE(128, 8)

@@ -63,10 +63,13 @@ def _setup(name, S, NB, seed):
     return dr, layer, ctx_k, ctx_v, seq, ctx_len, q, kb, vb, T
 
 
+# 40 blocks x 2 kv heads: fewer problems than SMs, the 8-page key blocks;
+# 80 blocks: more problems than SMs (152 on a GB300), the 4-page key blocks
+@pytest.mark.parametrize("NB", [40, 80])
 @pytest.mark.parametrize("name", ["mini_a", "mini_b"])
-def test_block_attention_matches_oracle(name):
+def test_block_attention_matches_oracle(name, NB):
     import torch
-    dr, layer, ctx_k, ctx_v, seq, ctx_len, q, kb, vb, T = _setup(name, S=5, NB=40, seed=31)
+    dr, layer, ctx_k, ctx_v, seq, ctx_len, q, kb, vb, T = _setup(name, S=5, NB=NB, seed=31)
     c = lambda a: torch.from_numpy(a).cuda()
     out = dr.block_attention(layer, c(seq), c(ctx_len), c(q), c(kb), c(vb))
     torch.cuda.synchronize()
