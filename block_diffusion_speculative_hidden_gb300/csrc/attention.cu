@@ -214,7 +214,8 @@ static cudaError_t launch_attn_ty(dflash_ctx* c, int layer, int B, int splits, c
 cudaError_t launch_attention(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s, const NextGemm& next,
                              const AttnSrc& src) {
   if (c->cfg.dtype != DFLASH_F32) return launch_attention_mma(c, layer, B, splits, s, next, src);
-  if (src.row_of != nullptr || src.seq_len != nullptr) return cudaErrorInvalidValue;  // bf16 family only
+  if (src.row_of != nullptr || src.seq_len != nullptr || src.order != nullptr)
+    return cudaErrorInvalidValue;  // bf16 family only
   return launch_attn_ty<float>(c, layer, B, splits, s);
 }
 

@@ -131,6 +131,7 @@ struct MmaAttnParams {
   const int32_t* page_table;
   const int32_t* seq_len;  // context length of block b
   const int32_t* row_of;   // page-table row of block b (null: row b)
+  const int32_t* order;    // block served by grid slot z (null: z)
   int max_pages, block_page0, pool_pages, layer;
   int Hkv, splits;
   int page_slots;     // capacity of the shared-memory page-id list
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
   float* s_red = reinterpret_cast<float*>(smem + C::OFF_BAR + C::BAR_AREA);  // [8 warps][32 lanes][RPT] pair exchange
   int* s_pages = reinterpret_cast<int*>(smem + C::OFF_BAR + C::BAR_BYTES);
 
-  const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int sp = blockIdx.x, kvh = blockIdx.y, b = p.order != nullptr ? p.order[blockIdx.z] : blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.seq_len[b];
   const int prow = p.row_of != nullptr ? p.row_of[b] : b;
@@ -762,6 +763,7 @@ cudaError_t launch_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s
   p.page_table = c->page_table;
   p.seq_len = src.seq_len != nullptr ? src.seq_len : c->seq_len;
   p.row_of = src.row_of;
+  p.order = src.order;
   p.max_pages = g.max_pages_per_seq;
   p.block_page0 = g.n_pages;
   p.pool_pages = c->pool_pages;

@@ -129,6 +129,7 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   auto row_src = static_cast<int32_t*>(w.take(sizeof(int32_t) * R));
   auto blk_row = static_cast<int32_t*>(w.take(sizeof(int32_t) * g.max_batch));
   auto blk_len = static_cast<int32_t*>(w.take(sizeof(int32_t) * g.max_batch));
+  auto attn_order = static_cast<int32_t*>(w.take(sizeof(int32_t) * g.max_batch));
   auto rcos = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
   auto rsin = static_cast<float*>(w.take(sizeof(float) * rope_rows * (g.head_dim / 2)));
   const bool lo = g.dtype != DFLASH_F32;  // GEMM inputs carry a second bf16 term
@@ -169,6 +170,7 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
     c->row_src = row_src;
     c->blk_row = blk_row;
     c->blk_len = blk_len;
+    c->attn_order = attn_order;
     c->rope_cos = rcos;
     c->rope_sin = rsin;
     c->rope_rows = rope_rows;
@@ -543,10 +545,15 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
   const int s_gu = draft_splits(g, M, Ngu, d, sms);
   const int s_dn = draft_splits(g, M, d, F, sms);
   const int a_sp = attn_splits(ctx, B);
+  // with more attention CTAs than SMs, the sequences start longest context
+  // first (the order is written by the embedding kernel of each pass)
+  int32_t* order = g.dtype != DFLASH_F32 && B * g.n_kv_heads * a_sp > sms ? ctx->attn_order : nullptr;
+  AttnSrc asrc;
+  asrc.order = order;
   for (int pass = 0; pass < S; ++pass) {
     {
       ProfScope p(ctx, DFLASH_PROF_ROWWISE, 1, s);
-      DF_CHECK(launch_embed(ctx, M, pass == 1, s));
+      DF_CHECK(launch_embed(ctx, M, pass == 1, order, s));
     }
     // every pre-norm runs folded: the producing epilogue writes g . x and the
     // sums of squares of x (ss_x), the consuming projection scales its rows
@@ -566,7 +573,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         ProfScope p(ctx, DFLASH_PROF_ATTN, g.dtype != DFLASH_F32 ? 1 : 2, s);
         // attention is latency-bound: it streams all of the O projection's
         // weights beyond that kernel's ring into L2
-        DF_CHECK(launch_attention(ctx, l, B, a_sp, s, next_gemm(ctx->w_o[l], d, qd, M, s_o, 1ll << 40)));
+        DF_CHECK(launch_attention(ctx, l, B, a_sp, s, next_gemm(ctx->w_o[l], d, qd, M, s_o, 1ll << 40), asrc));
       }
       {
         ProfScope p(ctx, DFLASH_PROF_PROJ, 1, s);

@@ -65,6 +65,9 @@ struct AttnSrc {
   const int32_t* row_of = nullptr;   // page-table row of block b (null: row b)
   const int32_t* seq_len = nullptr;  // context length of block b (null: the context's seq_len)
   bool pdl = true;                   // false: the immediate predecessor wrote row_of / seq_len
+  // launch order: grid slot z serves block order[z] (null: block z); written
+  // at least two kernels earlier, or by the immediate predecessor with pdl off
+  const int32_t* order = nullptr;
 };
 
 struct TmapEntry {
@@ -100,6 +103,7 @@ struct dflash_ctx {
   int* scal;  // [0] rows of the current inject, [1] free-list head, [2] free count
   int32_t *free_ring, *row_seq, *row_pos, *row_src;
   int32_t *blk_row, *blk_len;  // training-time block attention: page-table row and context length per block
+  int32_t* attn_order;          // [max_batch] attention launch order, longest context first
   float *rope_cos, *rope_sin;
   int rope_rows;
   int pool_pages;  // pages per layer in the pool: n_pages context pages + max_batch block pages

@@ -18,7 +18,8 @@ cudaError_t launch_rope_table(dflash_ctx* c, cudaStream_t s);
 
 // pointwise.cu (T = the config element type, chosen by c->cfg.dtype)
 cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, cudaStream_t s);
-cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, cudaStream_t s);
+// order (null: none): also writes the attention launch order of the M / 16 sequences
+cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, int32_t* order, cudaStream_t s);
 cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, const EpiArgs& norm,
                                 cudaStream_t s);
 cudaError_t launch_lm_merge(dflash_ctx* c, int M, const int32_t* commit, int32_t* tok_out, float* conf_out,

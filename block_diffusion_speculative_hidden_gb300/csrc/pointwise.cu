@@ -42,11 +42,25 @@ template <typename T>
 __global__ void __launch_bounds__(128) k_embed(const T* __restrict__ embed, const T* __restrict__ gain,
                                                float* __restrict__ x, ActOut<T> a, float* __restrict__ ss, int ss_ld,
                                                int d, int mask_id, int vocab, const int32_t* commit,
-                                               const int32_t* tok1, int* status) {
+                                               const int32_t* tok1, int* status, const int32_t* seq_len,
+                                               int32_t* order, int B) {
   __shared__ float red[4];
   pdl_wait();
   pdl_trigger();
   const int tile = blockIdx.x, m = blockIdx.y, n = tile * 128 + threadIdx.x;
+  if (order != nullptr && tile == 0 && m == 0) {
+    // the attention's launch order: sequences by context length, longest
+    // first (ties by index), so that the long ones do not start last
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      const int lb = seq_len[b];
+      int rank = 0;
+      for (int u = 0; u < B; ++u) {
+        const int lu = seq_len[u];
+        rank += lu > lb || (lu == lb && u < b);
+      }
+      order[rank] = b;
+    }
+  }
   int tok = mask_id;
   if (commit != nullptr && commit[m] != 0) tok = tok1[m];
   if (tok < 0 || tok >= vocab) {
@@ -254,13 +268,14 @@ cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, cudaS
                                      F));
 }
 
-cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, cudaStream_t s) {
+cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, int32_t* order, cudaStream_t s) {
   const auto& g = c->cfg;
   const dim3 grid((g.hidden + 127) / 128, M);
   DFLASH_DISPATCH(c, return launch_k(k_embed<T>, grid, dim3(128), 0, s, dim3(1), c->pdl,
                                      static_cast<const T*>(c->embed), static_cast<const T*>(c->g_in[0]), c->x,
                                      act_out<T>(c->a, c->a_lo), c->ss_x, g.max_batch * kBlockK, g.hidden,
-                                     g.mask_id, g.vocab, second_pass ? c->commit : nullptr, c->tok1, c->status));
+                                     g.mask_id, g.vocab, second_pass ? c->commit : nullptr, c->tok1, c->status,
+                                     c->seq_len, order, M / kBlockK));
 }
 
 cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, const EpiArgs& norm,

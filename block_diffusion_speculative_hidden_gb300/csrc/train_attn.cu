@@ -13,32 +13,54 @@
 
 namespace dflash {
 
-// One CTA per block v: the page-table row and prefix length (checked against
-// the sequence: an out-of-range sequence or a prefix longer than it sets
-// ST_BAD_BLOCK and is clamped), the block's queries into the query buffer
+// The sequence and prefix length of block v, checked against the sequence
+// (an out-of-range sequence or a prefix longer than it is clamped; *bad set).
+__device__ __forceinline__ int2 block_src(int v, int max_batch, const int32_t* seq, const int32_t* ctx_len,
+                                          const int32_t* seq_len, bool* bad) {
+  int s = seq[v], c = ctx_len[v];
+  *bad = s < 0 || s >= max_batch;
+  if (*bad) s = 0;
+  const int L = seq_len[s];
+  if (c < 0 || c > L) {
+    *bad = true;
+    c = c < 0 ? 0 : L;
+  }
+  return make_int2(s, c);
+}
+
+// One CTA per block v: the page-table row and prefix length (checked, see
+// block_src; a bad block sets ST_BAD_BLOCK), the block's place in the
+// attention's launch order (longest prefix first, ties by index: the rank of
+// v among all blocks), the block's queries into the query buffer
 // ([v*16 + i][Hq*dh], fp16, the layout they arrive in), and its keys and
 // values from [16][Hkv][dh] (token-major) into the pool's block page
 // [Hkv][16][dh] of the layer.
 __global__ void k_blockattn_stage(int NB, int max_batch, const int32_t* __restrict__ seq,
                                   const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ seq_len,
-                                  int32_t* blk_row, int32_t* blk_len, const __half* __restrict__ q,
+                                  int32_t* blk_row, int32_t* blk_len, int32_t* order, const __half* __restrict__ q,
                                   const __half* __restrict__ kb, const __half* __restrict__ vb, __half* q_buf,
                                   __half* pool_k_layer, __half* pool_v_layer, int block_page0, int qd, int Hkv,
                                   int dh, int* status) {
   const int v = blockIdx.x;
   if (v >= NB) return;
-  if (threadIdx.x == 0) {
-    int s = seq[v], c = ctx_len[v];
-    bool bad = s < 0 || s >= max_batch;
-    if (bad) s = 0;
-    const int L = seq_len[s];
-    if (c < 0 || c > L) {
-      bad = true;
-      c = c < 0 ? 0 : L;
+  bool bad;
+  const int2 src = block_src(v, max_batch, seq, ctx_len, seq_len, &bad);
+  int rank = 0;
+  for (int u0 = 0; u0 < NB; u0 += blockDim.x) {
+    const int u = u0 + threadIdx.x;
+    bool before = false;
+    if (u < NB) {
+      bool bad_u;
+      const int lu = block_src(u, max_batch, seq, ctx_len, seq_len, &bad_u).y;
+      before = lu > src.y || (lu == src.y && u < v);
     }
+    rank += __syncthreads_count(before);
+  }
+  if (threadIdx.x == 0) {
     if (bad) atomicOr(status, ST_BAD_BLOCK);
-    blk_row[v] = s;
-    blk_len[v] = c;
+    blk_row[v] = src.x;
+    blk_len[v] = src.y;
+    order[rank] = v;
   }
   // queries: 16 rows of qd halves, copied 8 halves (16 bytes) at a time
   const long long q0 = static_cast<long long>(v) * kBlockK * qd;
@@ -73,7 +95,7 @@ cudaError_t launch_block_attention(dflash_ctx* c, int layer, int NB, const int32
   __half* pk = static_cast<__half*>(c->pool_k) + per_layer * layer;
   __half* pv = static_cast<__half*>(c->pool_v) + per_layer * layer;
   k_blockattn_stage<<<NB, 256, 0, s>>>(NB, g.max_batch, seq, ctx_len, c->seq_len, c->blk_row, c->blk_len,
-                                       static_cast<const __half*>(q), static_cast<const __half*>(k_blk),
+                                       c->attn_order, static_cast<const __half*>(q), static_cast<const __half*>(k_blk),
                                        static_cast<const __half*>(v_blk), static_cast<__half*>(c->q), pk, pv,
                                        g.n_pages, qd, g.n_kv_heads, g.head_dim, c->status);
   cudaError_t e = cudaGetLastError();
@@ -81,7 +103,8 @@ cudaError_t launch_block_attention(dflash_ctx* c, int layer, int NB, const int32
   AttnSrc src;
   src.row_of = c->blk_row;
   src.seq_len = c->blk_len;
-  src.pdl = false;  // the staging kernel just wrote the rows and lengths
+  src.order = c->attn_order;
+  src.pdl = false;  // the staging kernel just wrote the rows, lengths and order
   e = launch_attention(c, layer, NB, attn_splits(c, NB), s, NextGemm{}, src);
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(NB) * kBlockK * qd;
