@@ -30,7 +30,10 @@
 //     wait; q and the block page come after it;
 //   - with several splits, the splits of one (sequence, kv head) form a
 //     cluster and merge (o, m, l) with bulk copies between the CTAs' shared
-//     memories.
+//     memories;
+//   - grid slot z serves sequence order[z] when an order is given (longest
+//     context first, so that in a grid of several waves the long streams
+//     start early).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
