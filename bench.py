@@ -540,13 +540,15 @@ def run_reference(args, cfg, world, rank):
         return
     w = synth.make_weights(cfg)
     lens = synth.make_ctx_lens(cfg)
-    # bounded sample: about a minute of timed oracle work
-    dt1, cores, _ = oracle_rounds(cfg, w, 1, lens)
+    # untimed warm-up rounds, which also size the bounded sample: about a
+    # minute of timed oracle work
+    warmup = max(1, args.warmup)
+    dt1, cores, _ = oracle_rounds(cfg, w, warmup, lens)
     steps = max(1, min(args.steps, int(60.0 / max(dt1, 1e-3))))
     dt, cores, mean_tau = oracle_rounds(cfg, w, steps, lens)
     value = cfg.batch * K_BLOCK / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": steps, "warmup": 1, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "steps": steps, "warmup": warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_block(cfg, lens),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -556,7 +558,7 @@ def run_reference(args, cfg, world, rank):
 
 
 def config_block(cfg, lens):
-    return {"workload": cfg.name, "weights": "e4m3 codes + fp32 row scales" if cfg.weight_format == "e4m3" else "bf16",
+    return {"workload": cfg.name, "weights": "e4m3 codes + fp32 row scales" if cfg.weight_format == "e4m3" else cfg.dtype,
             "batch": cfg.batch, "context": int(lens.max()), "block_k": K_BLOCK,
             "s_passes": cfg.s_passes, "draft_layers": cfg.n_layers, "hidden": cfg.hidden,
             "heads": f"{cfg.n_q_heads}/{cfg.n_kv_heads}x{cfg.head_dim}", "ffn": cfg.ffn, "vocab": cfg.vocab,
