@@ -314,6 +314,47 @@ def test_mask_semantics_logits_depend_only_on_context():
     np.testing.assert_array_equal(z_direct, z)
 
 
+def test_argmax_confidence_closed_forms_and_library():
+    # two logits: the confidence is the logistic of their gap
+    for a, b in [(2.0, -1.0), (0.3, 0.1), (-5.0, -7.5)]:
+        tok, conf, _ = O.argmax_conf(np.array([[a, b]]))
+        assert tok[0] == 0 and math.isclose(conf[0], 1.0 / (1.0 + math.exp(b - a)), rel_tol=1e-14)
+    # uniform row: 1 / V, the lowest index wins the tie
+    tok, conf, lse = O.argmax_conf(np.full((1, 37), 0.25))
+    assert tok[0] == 0 and math.isclose(conf[0], 1.0 / 37, rel_tol=1e-14)
+    assert math.isclose(lse[0], 0.25 + math.log(37), rel_tol=1e-14)
+    z = np.zeros((1, 10))
+    z[0, 3] = z[0, 7] = 1.5
+    assert O.argmax_conf(z)[0][0] == 3
+    # against the library, including magnitudes that overflow a naive exp
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((6, 501)) * 4.0
+    z[2] += 1000.0
+    z[4] -= 800.0
+    tok, conf, lse = O.argmax_conf(z)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(z, axis=-1), rtol=1e-13)
+    np.testing.assert_allclose(conf, scipy.special.softmax(z, axis=-1).max(axis=-1), rtol=1e-12)
+    np.testing.assert_array_equal(tok, np.argmax(scipy.special.softmax(z, axis=-1), axis=-1))
+    # shifting a row changes neither the token nor the confidence
+    t2, c2, l2 = O.argmax_conf(z + 123.0)
+    np.testing.assert_array_equal(t2, tok)
+    np.testing.assert_allclose(c2, conf, rtol=1e-12)
+    np.testing.assert_allclose(l2, lse + 123.0, rtol=1e-13)
+
+
+def test_lm_head_normalises_then_projects_rows():
+    # W_lm = [I; 2I] (V = 2d, so a transposed operand cannot even multiply),
+    # unit final gain: z = [x / rms(x), 2 x / rms(x)] per row
+    cfg = tiny_cfg()
+    d = cfg.hidden
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((3, d))
+    w = {"g_final": np.ones(d), "w_lm": np.vstack([np.eye(d), 2.0 * np.eye(d)])}
+    z = O.lm_head(x, w, cfg)
+    xh = x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + cfg.rms_eps)
+    np.testing.assert_allclose(z, np.hstack([xh, 2.0 * xh]), rtol=1e-13, atol=1e-13)
+
+
 def test_two_pass_commit_rule():
     rng = np.random.default_rng(10)
     conf = rng.random(16)
