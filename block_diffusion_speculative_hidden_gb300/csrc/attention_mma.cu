@@ -855,7 +855,6 @@ template <template <int, int, int, int> class F, typename... A>
 auto dispatch(dflash_ctx* c, int splits, bool narrow, A... args) {
   const bool short_split = split_pages_bound(c, splits) <= kShortPages;
   const int G = c->cfg.n_q_heads / c->cfg.n_kv_heads;
-  const bool d64 = c->cfg.head_dim == 64;
 #define DFLASH_ATTN_CASE(DH_, G_)                                                              \
   if (c->cfg.head_dim == DH_ && G == G_)                                                       \
     return short_split ? F<DH_, G_, kShortPages, 1>::run(c, splits, args...)                   \
@@ -866,7 +865,6 @@ auto dispatch(dflash_ctx* c, int splits, bool narrow, A... args) {
   DFLASH_ATTN_CASE(64, 1) DFLASH_ATTN_CASE(64, 2) DFLASH_ATTN_CASE(64, 4) DFLASH_ATTN_CASE(64, 8)
   DFLASH_ATTN_CASE(128, 1) DFLASH_ATTN_CASE(128, 2) DFLASH_ATTN_CASE(128, 4) DFLASH_ATTN_CASE(128, 8)
 #undef DFLASH_ATTN_CASE
-  (void)d64;
   return F<64, 1, 8, 2>::invalid();
 }
 
