@@ -254,10 +254,9 @@ dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* dra
                             uint64_t round, int32_t* accept_len, int32_t* emitted, int32_t* n_emit,
                             dflash_stream stream);
 
-/* Training-time block attention.  [Paper] Figure 4 (DFlash training
- * attention: within a masked block the positions attend to each other; the
- * mask keeps "causal consistency" with the target context and prevents
- * "inter-block information leakage").
+/* Training-time block attention.  [Paper] Figure 4 (the training mask: the
+ * positions of a masked block see each other and the target context before
+ * the block, and nothing of any other block).
  *
  * For NB blocks of K = 16 positions (NB <= max_batch): block j belongs to
  * sequence seq[j] (device int32 [NB]) and sees that sequence's injected
