@@ -36,11 +36,12 @@ Readings taken where the pages are silent (each repeated at its function):
   R15 optional shared pre-RoPE key offset on the injected keys (workload knob)
   R17 training-time block attention (P2 Fig. 4): a block of K positions
       that starts at response position c sees the target context at
-      positions [0, c) ("causal consistency") and all K positions of its own
-      block (bidirectional, as at inference), and nothing of any other block
-      ("no inter-block leakage"); anchors (clean tokens inside a block)
-      change only the block's input embeddings, not the mask
-  R16 FP8 weights (the Guide's "FP4/FP8 mixed execution" on Blackwell): a
+      positions [0, c) (nothing later than its own start) and all K
+      positions of its own block (bidirectional, as at inference), and
+      nothing of any other block (no leakage between blocks); anchors (clean
+      tokens inside a block) change only the block's input embeddings, not
+      the mask
+  R16 FP8 weights (the Guide mentions mixed FP4/FP8 execution on Blackwell): a
       projection weight is an e4m3 code per entry and an fp32 scale per
       output row, W = diag(s) . decode(codes); the drafter's arithmetic is
       otherwise that of the bf16 workload
@@ -110,7 +111,7 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
 
     q [n_q, Hq, dh], k/v [n_k, Hkv, dh] -> o [n_q, Hq, dh].  Query head h reads
     kv head h // G.  No causal mask: block positions see every context key and
-    every block key (P1 "bidirectional self-attention"; P3 the [MASK]
+    every block key (P1: attention inside the block is bidirectional; P3 the [MASK]
     placeholders of both neighbours are visible).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -341,7 +342,7 @@ def block_forward(w: Dict[str, np.ndarray], ctx_kv: Sequence[Tuple[np.ndarray, n
 
 def commit_order(conf: np.ndarray, n_commit: int) -> np.ndarray:
     """Boolean mask of the n_commit most confident positions, ties to the lower
-    position (R9; P3 "committing positions in confidence order")."""
+    position (R9; P3: positions are committed most confident first)."""
     K = conf.shape[0]
     order = sorted(range(K), key=lambda i: (-float(conf[i]), i))
     mask = np.zeros(K, bool)
