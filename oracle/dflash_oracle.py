@@ -46,8 +46,11 @@ Readings taken where the pages are silent (each repeated at its function):
       output row, W = diag(s) . decode(codes); the drafter's arithmetic is
       otherwise that of the bf16 workload
 
-Pins (tests/test_oracle_pins.py): closed forms, textbook special cases,
-invariants, brute force and exact enumeration.  There is no worked numeric
+Pins (tests/test_oracle_pins.py, tests/test_oracle_accept_pins.py): closed
+forms, textbook special cases, invariants, brute force and exact
+enumeration; the stochastic acceptance (accept_stochastic, race_sample)
+against an exact enumeration of the lossless rule, the rule's closed-form
+per-round outcome probabilities and the race's defining frequencies.  There is no worked numeric
 example on any page, so the block's logit VALUES are pinned only through
 those invariants and special cases (two independent formulations of KV
 injection, RoPE shift invariance, special weights that reduce a layer to the
