@@ -3,11 +3,16 @@
 
 One step = one speculative round on the GPU: KV-inject the tau+1 rows the
 previous round accepted, draft a K = 16 block (S passes), and accept against
-the synthetic target.  Default workload: the Qwen3-8B-shaped drafter (5
-layers, hidden 4096, 32/8 heads of 128, SwiGLU 12288, vocab 151936, 5 taps
-of 4096), batch 1, context 2048, S = 1, greedy accept with per-position
-match probability 0.85; random-init N(0, 0.02) bf16 weights, N(0, 1)
-features (seeded, synthetic).
+the synthetic target.  Default workload (the largest that fits one GPU): the
+gpt-oss-120b-shaped drafter (3 layers, hidden 2880, 64/8 heads of 64, SwiGLU
+2880, vocab 201088, 3 taps of 2880), 128 sequences with contexts uniform in
+[1024, 8192], S = 2 confidence-ordered commits, stochastic rejection-sampling
+accept at temperature 1 against target logits = the committing pass's draft
+logits + N(0, 1) noise; random-init N(0, 0.02) bf16 weights, N(0, 1)
+features (seeded, synthetic).  The other workloads (tiny fp32, Qwen3-8B-
+shaped at batch 1 with bf16 and FP8 weights, the 32-sequence serving batch,
+4 x 32k long context) are timed in the same run and reported under
+"per_config".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs its own replica (the path shards by
@@ -41,16 +46,19 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c2")
+    ap.add_argument("--config", default="c5")
+    ap.add_argument("--per-config", default="c1,c2,c2w8,c3,c4",
+                    help="workloads timed after the headline one (comma list; empty: none)")
+    ap.add_argument("--per-config-steps", type=int, default=100)
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-rounds", type=int, default=4, help="oracle rounds timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay leg")
-    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight leg of the default workload")
     ap.add_argument("--sweep", action="store_true",
                     help="draft-cost sweeps (1/3/5 draft layers; projections on 1 vs 16 rows), JSON line per item")
-    ap.add_argument("--reset-every", type=int, default=16,
-                    help="roll each sequence back to its prompt length every N rounds")
+    ap.add_argument("--reset-every", type=int, default=0,
+                    help="roll each sequence back to its prompt length every N rounds "
+                         "(0: the workload's stated round count)")
     ap.add_argument("--kernel", choices=["gemm", "train_attn"], default=None,
                     help="time one kernel alone on the workload's shapes (small case for profilers)")
     ap.add_argument("--small", action="store_true",
@@ -212,7 +220,8 @@ def algorithmic_bytes(cfg):
     Fp = 64 * -(-F // 64)                     # gate/up rows are packed in groups of 64
     per_layer = proj(qd + 2 * kvd, d) + proj(d, qd) + proj(2 * Fp, d) + proj(d, F)
     return {"proj": L * per_layer * cfg.s_passes,
-            "lm_head": (wbytes(V, d) + M * d * 4) * cfg.s_passes,
+            # S = 2: the second LM head reads the K/2 uncommitted rows of each block
+            "lm_head": wbytes(V, d) * cfg.s_passes + (M + (cfg.s_passes - 1) * (M // 2)) * d * 4,
             "inject_weights": wbytes(d, cfg.feat_dim) + wbytes(2 * L * kvd, d)}
 
 
@@ -224,11 +233,23 @@ def kv_bytes(cfg, ctx_len):
 
 # --------------------------------------------------------------------------- GPU arm
 
+def reset_period(cfg, reset_every: int) -> int:
+    """Rounds between roll-backs to the prompt: the workload's stated round
+    count (c3: 32, c4: 64, the others 8) unless given."""
+    return reset_every if reset_every > 0 else cfg.rounds
+
+
 class Workload:
     """The drafter on the GPU with its prompt injected and every round's
-    inputs (new feature rows, synthetic target coins) already in HBM."""
+    inputs (new feature rows, synthetic target coins or noise) already in HBM.
 
-    def __init__(self, cfg, rounds: int, rank: int, device, reset_every: int = 16):
+    Stochastic workloads: the synthetic target's logits are the committing
+    pass's draft logits (the draft call's logits output: pass-1 rows on the
+    committed positions, pass-2 rows elsewhere) plus N(0, 1) noise, and the
+    bonus row is noise alone; the noise comes from n_noise device-resident
+    draws (torch's seeded generator, used cyclically)."""
+
+    def __init__(self, cfg, rounds: int, rank: int, device, reset_every: int = 0, n_noise: int = 4):
         import torch
         from block_diffusion_speculative_hidden_gb300 import Drafter, weights_to_device
         self.torch = torch
@@ -240,7 +261,8 @@ class Workload:
         self.t_gen = time.time() - t0
         self.lens = synth.make_ctx_lens(cfg)
         chunk = min(1024, int(self.lens.max()))
-        max_ctx = int(self.lens.max()) + 17 * (max(reset_every, 1) + 2)
+        self.period = reset_period(cfg, reset_every)
+        max_ctx = int(self.lens.max()) + 17 * (self.period + 2)
         self.mpps = -(-max_ctx // 16) + 2
         n_pages = B * self.mpps + 8
         koff = synth.make_key_offsets(cfg)
@@ -272,6 +294,13 @@ class Workload:
         assert self.dr.device_status() == 0
         # per-round inputs, resident
         self.rounds = rounds
+        self.stochastic = cfg.accept == "stochastic"
+        if self.stochastic:
+            V = cfg.vocab
+            self.zd = torch.empty((B, K_BLOCK, V), dtype=torch.float32, device=device)
+            self.zt = torch.empty((B, K_BLOCK + 1, V), dtype=torch.float32, device=device)
+            gen = torch.Generator(device=device).manual_seed(cfg.seed * 1000 + rank)
+            self.noise = [torch.randn((B, K_BLOCK + 1, V), generator=gen, device=device) for _ in range(n_noise)]
         feats = np.zeros((rounds, B, 17, F), np.float32)
         match = np.zeros((rounds, B, 17), bool)
         rand = np.zeros((rounds, B, 17), np.int32)
@@ -291,6 +320,7 @@ class Workload:
                     torch.empty((B, 17), dtype=torch.int32, device=device),
                     torch.empty(B, dtype=torch.int32, device=device))
         self.tau_sum = torch.zeros(B, dtype=torch.int64, device=device)
+        self.target_events = None    # list of event pairs while the target's ops are timed
 
     def step(self, r: int, feats=None, y=None, match=None):
         """One round: inject tau+1 rows, draft, synthetic target, accept."""
@@ -298,26 +328,61 @@ class Workload:
         cfg = self.cfg
         r %= self.rounds
         self.dr.inject_kv(self.feats[r] if feats is None else feats, self.n_rows)
+        if self.stochastic:
+            self.dr.draft_block(cfg.batch, cfg.s_passes, tokens=self.tok, conf=self.conf, logits=self.zd)
+            # synthetic target verify: its logits are the draft logits plus noise
+            nz = self.noise[r % len(self.noise)]
+            ev = None
+            if self.target_events is not None:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record()
+            torch.add(self.zd, nz[:, :K_BLOCK], out=self.zt[:, :K_BLOCK])
+            self.zt[:, K_BLOCK].copy_(nz[:, K_BLOCK])
+            if ev is not None:
+                ev[1].record()
+                self.target_events.append(ev)
+            tau, em, n = self.dr.accept(1, self.tok, target_logits=self.zt, temperature=cfg.temperature,
+                                        seed=cfg.seed, round=r, out=self.acc)
+            self.n_rows.copy_(n)
+            self.tau_sum += tau
+            return
         self.dr.draft_block(cfg.batch, cfg.s_passes, tokens=self.tok, conf=self.conf)
         yy = self.y[r] if y is None else y
         mm = self.match[r] if match is None else match
         # synthetic target verify: y_i = d_i where the round's coin matched
+        ev = None
+        if self.target_events is not None:
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record()
         torch.where(mm[:, :K_BLOCK], self.tok, yy[:, :K_BLOCK], out=yy[:, :K_BLOCK])
+        if ev is not None:
+            ev[1].record()
+            self.target_events.append(ev)
         tau, em, n = self.dr.accept(0, self.tok, target_tokens=yy, out=self.acc)
         self.n_rows.copy_(n)
         self.tau_sum += tau
 
-    def maybe_reset(self, r: int, every: int):
-        if every > 0 and r % every == every - 1:
+    def maybe_reset(self, r: int):
+        """After round r: roll every sequence back to its prompt at the end of
+        each period of the workload's stated round count."""
+        every = self.period
+        if r % every == every - 1:
             for b in range(self.cfg.batch):
                 self.dr.truncate(b, int(self.lens[b]))
 
 
-def run_ours(args, cfg, world, rank, local):
+def run_ours(args, cfg, world, rank, local, steps=None, legs=True):
+    """Warm-up, then timed region A (the number: one CUDA-event pair around
+    `steps` rounds, clocks sampled meanwhile) and timed region B (the same
+    rounds with per-launch events per kernel class, and the synthetic
+    target's ops timed on their own); with legs, the end-to-end and graph
+    replay legs.  Returns the figures and the workload."""
     import torch
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    rounds = 64
+    steps = args.steps if steps is None else steps
+    period = reset_period(cfg, args.reset_every)
+    rounds = min(64, max(16, 2 * period))
     wl = Workload(cfg, rounds, rank, device, reset_every=args.reset_every)
     stream = torch.cuda.current_stream(device)
     B = cfg.batch
@@ -325,7 +390,7 @@ def run_ours(args, cfg, world, rank, local):
     def loop(n, start):
         for i in range(n):
             wl.step(start + i)
-            wl.maybe_reset(start + i, args.reset_every)
+            wl.maybe_reset(start + i)
 
     # warm-up
     loop(args.warmup, 0)
@@ -341,34 +406,38 @@ def run_ours(args, cfg, world, rank, local):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        loop(args.steps, args.warmup)
+        loop(steps, args.warmup)
         e1.record(stream)
         torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1)
     barrier(world)
-    mean_tau = float(wl.tau_sum.sum().item()) / (args.steps * B)
-    tokens, ms_max = aggregate(float(args.steps * B * K_BLOCK), ms, world)
+    mean_tau = float(wl.tau_sum.sum().item()) / (steps * B)
+    tokens, ms_max = aggregate(float(steps * B * K_BLOCK), ms, world)
     value = tokens / (ms_max / 1e3)
     clocks = clk.summary()
     # ---- timed region B: same loop with per-launch events (kernel classes)
     wl.dr.profile(True)
     wl.dr.profile_read()
+    wl.target_events = []
     torch.cuda.synchronize(device)
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    loop(args.steps, args.warmup + args.steps)
+    loop(steps, args.warmup + steps)
     f1.record(stream)
     prof = wl.dr.profile_read()
     ms_b = f0.elapsed_time(f1)
     wl.dr.profile(False)
+    target_ms = sum(a.elapsed_time(b) for a, b in wl.target_events)
+    wl.target_events = None
     assert wl.dr.device_status() == 0
-    launches_per_step = sum(v[1] for v in prof.values()) / args.steps
+    launches_per_step = sum(v[1] for v in prof.values()) / steps
     # ---- e2e: host buffers through the public API, copies inside the region
-    e2e = run_e2e(wl, args, device) if args.e2e_steps > 0 else None
-    graph = None if args.no_graph else run_graph(wl, args, device)
+    e2e = run_e2e(wl, args, device) if legs and args.e2e_steps > 0 else None
+    graph = None if (args.no_graph or not legs) else run_graph(wl, args, device)
     return dict(value=value, ms=ms_max, tokens=tokens, mean_tau=mean_tau, clocks=clocks, prof=prof, ms_b=ms_b,
-                launches_per_step=launches_per_step, e2e=e2e, graph=graph, wl=wl)
+                target_ms=target_ms, launches_per_step=launches_per_step, e2e=e2e, graph=graph, wl=wl,
+                lens=wl.lens, steps=steps, period=wl.period)
 
 
 def run_graph(wl, args, device):
@@ -384,7 +453,7 @@ def run_graph(wl, args, device):
         for r in range(wl.rounds):
             wl.dr.graph_begin(stream=gs)
             wl.step(r)
-            wl.maybe_reset(r, args.reset_every)
+            wl.maybe_reset(r)
             graphs.append(wl.dr.graph_end(stream=gs))
     n = wl.rounds
     # start from the prompts, so that the rollback schedule of the recorded
@@ -414,8 +483,9 @@ def run_graph(wl, args, device):
 
 
 def run_e2e(wl, args, device):
-    """Per step: pinned host feature rows and target coins -> device, the
-    three library calls, drafts + emitted tokens + counts -> pinned host,
+    """Per step: pinned host feature rows and target coins (greedy
+    workloads) -> device, the three library calls, drafts + emitted tokens +
+    counts -> pinned host,
     then a stream sync (the caller reads its result).  Timed twice: each
     step's calls issued one by one, and each step as one replay of a CUDA
     graph recorded from the same calls, copies included (dflash_graph_*);
@@ -433,16 +503,19 @@ def run_e2e(wl, args, device):
     o_tok = torch.empty((B, K_BLOCK), dtype=torch.int32).pin_memory()
     o_em = torch.empty((B, 17), dtype=torch.int32).pin_memory()
     o_n = torch.empty((B,), dtype=torch.int32).pin_memory()
-    h2d = d_feats.numel() * d_feats.element_size() + d_match.numel() + d_y.numel() * 4
+    # stochastic workloads: the synthetic target's noise stays on the device
+    # (target-side state); the host supplies the round's feature rows
+    h2d = d_feats.numel() * d_feats.element_size() + (0 if wl.stochastic else d_match.numel() + d_y.numel() * 4)
     d2h = o_tok.numel() * 4 + o_em.numel() * 4 + o_n.numel() * 4
     gs = torch.cuda.Stream(device)
 
     def one_step(r):
         d_feats.copy_(h_feats[r], non_blocking=True)
-        d_match.copy_(h_match[r], non_blocking=True)
-        d_y.copy_(h_y[r], non_blocking=True)
+        if not wl.stochastic:
+            d_match.copy_(h_match[r], non_blocking=True)
+            d_y.copy_(h_y[r], non_blocking=True)
         wl.step(r, feats=d_feats, y=d_y, match=d_match)
-        wl.maybe_reset(r, args.reset_every)
+        wl.maybe_reset(r)
         o_tok.copy_(wl.tok, non_blocking=True)
         o_em.copy_(wl.acc[1], non_blocking=True)
         o_n.copy_(wl.acc[2], non_blocking=True)
@@ -503,35 +576,64 @@ def run_e2e(wl, args, device):
 
 # --------------------------------------------------------------------------- oracle (CPU)
 
-def oracle_rounds(cfg, weights, n_rounds: int, lens):
-    """Time the oracle on rounds of the same workload: inject tau+1 rows,
-    draft, greedy accept.  Returns (seconds per round, threads, mean tau)."""
+ORACLE_SEQS = 4  # sequences of a batch the CPU oracle times (sequences are independent)
+
+
+def oracle_seqs(cfg):
+    """The sequences the oracle times: all of a small batch, else a seeded
+    sample of ORACLE_SEQS (per-sequence work is independent of the others,
+    so the batch's token rate is the sample's)."""
+    if cfg.batch <= ORACLE_SEQS:
+        return list(range(cfg.batch))
+    rng = np.random.default_rng(cfg.seed)
+    return sorted(rng.choice(cfg.batch, size=ORACLE_SEQS, replace=False).tolist())
+
+
+def oracle_rounds(cfg, weights, n_rounds: int, lens, seqs):
+    """Time the oracle on rounds of the same workload for sequences `seqs`:
+    inject tau+1 rows, draft (S passes), accept (greedy against the synthetic
+    target's tokens, or stochastic against its logits = the committing
+    pass's draft logits + N(0, 1) noise).  Returns (seconds per round,
+    threads, mean tau)."""
     from oracle import dflash_oracle as O
-    B = cfg.batch
-    mpps = -(-(int(lens.max()) + 17 * (n_rounds + 2)) // 16) + 1
-    dr = O.OracleDrafter(cfg, weights, B * mpps + 4, mpps, key_offsets=synth.make_key_offsets(cfg))
-    assert dr.inject([synth.make_prefill_features(cfg, b, int(lens[b])) for b in range(B)])
-    n_rows = np.ones(B, np.int64)
+    nb = len(seqs)
+    ln = lens[seqs]
+    mpps = -(-(int(ln.max()) + 17 * (n_rounds + 2)) // 16) + 1
+    dr = O.OracleDrafter(cfg, weights, nb * mpps + 4, mpps, key_offsets=synth.make_key_offsets(cfg), seqs=seqs)
+    assert dr.inject([synth.make_prefill_features(cfg, b, int(lens[b])) for b in seqs])
+    n_rows = np.ones(nb, np.int64)
     taus = []
     t0 = time.perf_counter()
     for r in range(n_rounds):
-        assert dr.inject([synth.make_round_features(cfg, r, b, int(n_rows[b])) for b in range(B)])
-        d = np.stack([dr.draft(b)["tokens"] for b in range(B)]).astype(np.int64)
-        y = synth.make_target_tokens(cfg, r, d)
-        tau, _, n = O.accept_greedy(d, y)
+        assert dr.inject([synth.make_round_features(cfg, r, b, int(n_rows[j])) for j, b in enumerate(seqs)])
+        res = [dr.draft(j) for j in range(nb)]
+        d = np.stack([x["tokens"] for x in res]).astype(np.int64)
+        if cfg.accept == "stochastic":
+            z = np.stack([x["logits"] for x in res])
+            zt = np.concatenate([z, np.zeros((nb, 1, cfg.vocab))], 1)
+            zt += synth.make_target_logits(cfg, 100 + r, d, cfg.vocab, noise_std=1.0)
+            tau, _, n = O.accept_stochastic(zt, d, None, cfg.temperature, cfg.seed, r)
+        else:
+            y = synth.make_target_tokens(cfg, r, d)
+            tau, _, n = O.accept_greedy(d, y)
         n_rows = n
         taus.append(tau.mean())
     dt = (time.perf_counter() - t0) / n_rounds
     return dt, os.cpu_count(), float(np.mean(taus))
 
 
+def oracle_sample_text(cfg, seqs, rounds):
+    part = "all" if len(seqs) == cfg.batch else f"{len(seqs)} seeded of {cfg.batch} (tok/s extrapolated: the per-sequence rate)"
+    return (f"{rounds} rounds of {cfg.name}, sequences {part}, NumPy fp64, after an untimed prompt injection")
+
+
 def cpu_baseline(cfg, args, weights=None):
     w = weights if weights is not None else synth.make_weights(cfg)
     lens = synth.make_ctx_lens(cfg)
-    dt, cores, _ = oracle_rounds(cfg, w, args.cpu_rounds, lens)
-    return {"value": cfg.batch * K_BLOCK / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{args.cpu_rounds} rounds of {cfg.name} (batch {cfg.batch}, context {int(lens[0])}), "
-                      "NumPy fp64, after an untimed prompt injection"}
+    seqs = oracle_seqs(cfg)
+    dt, cores, _ = oracle_rounds(cfg, w, args.cpu_rounds, lens, seqs)
+    return {"value": len(seqs) * K_BLOCK / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": oracle_sample_text(cfg, seqs, args.cpu_rounds)}
 
 
 def run_reference(args, cfg, world, rank):
@@ -540,31 +642,37 @@ def run_reference(args, cfg, world, rank):
         return
     w = synth.make_weights(cfg)
     lens = synth.make_ctx_lens(cfg)
+    seqs = oracle_seqs(cfg)
     # untimed warm-up rounds, which also size the bounded sample: about a
     # minute of timed oracle work
     warmup = max(1, args.warmup)
-    dt1, cores, _ = oracle_rounds(cfg, w, warmup, lens)
+    dt1, cores, _ = oracle_rounds(cfg, w, warmup, lens, seqs)
     steps = max(1, min(args.steps, int(60.0 / max(dt1, 1e-3))))
-    dt, cores, mean_tau = oracle_rounds(cfg, w, steps, lens)
-    value = cfg.batch * K_BLOCK / dt
+    dt, cores, mean_tau = oracle_rounds(cfg, w, steps, lens, seqs)
+    value = len(seqs) * K_BLOCK / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": steps, "warmup": warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_block(cfg, lens),
+            "steps": steps, "warmup": warmup, "ms_per_step": dt * 1e3 * cfg.batch / len(seqs),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(cfg, lens), "mean_tau": mean_tau,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{steps} rounds (of {args.steps} requested) of {cfg.name}, NumPy fp64"},
+                             "sample": oracle_sample_text(cfg, seqs, steps) + f" ({args.steps} requested)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def config_block(cfg, lens):
+    """The workload, identical in both arms' lines."""
+    ab = algorithmic_bytes(cfg)
     return {"workload": cfg.name, "weights": "e4m3 codes + fp32 row scales" if cfg.weight_format == "e4m3" else cfg.dtype,
-            "batch": cfg.batch, "context": int(lens.max()), "block_k": K_BLOCK,
+            "batch": cfg.batch, "context": [int(lens.min()), int(lens.max())], "block_k": K_BLOCK,
             "s_passes": cfg.s_passes, "draft_layers": cfg.n_layers, "hidden": cfg.hidden,
             "heads": f"{cfg.n_q_heads}/{cfg.n_kv_heads}x{cfg.head_dim}", "ffn": cfg.ffn, "vocab": cfg.vocab,
-            "taps": f"{cfg.n_taps}x{cfg.tap_width}", "accept": cfg.accept, "match_prob": cfg.match_prob,
+            "taps": f"{cfg.n_taps}x{cfg.tap_width}", "accept": cfg.accept,
+            "temperature": cfg.temperature if cfg.accept == "stochastic" else None,
+            "match_prob": cfg.match_prob if cfg.accept == "greedy" else None,
+            "rounds_per_prompt": cfg.rounds,
             "l2": "inputs larger than L2: every step streams all drafter weights "
-                  f"({(algorithmic_bytes(cfg)['proj'] + algorithmic_bytes(cfg)['lm_head']) / 1e9:.2f} GB) from HBM"}
+                  f"({(ab['proj'] + ab['lm_head']) / 1e9:.2f} GB) from HBM"}
 
 
 # --------------------------------------------------------------------------- single kernels
@@ -637,13 +745,13 @@ def run_sweep(args, cfg):
         wl = Workload(c, 64, 0, device, reset_every=args.reset_every)
         for i in range(args.warmup):
             wl.step(i)
-            wl.maybe_reset(i, args.reset_every)
+            wl.maybe_reset(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(steps):
             wl.step(args.warmup + i)
-            wl.maybe_reset(args.warmup + i, args.reset_every)
+            wl.maybe_reset(args.warmup + i)
         e1.record()
         torch.cuda.synchronize()
         round_ms = e0.elapsed_time(e1) / steps
@@ -683,54 +791,114 @@ def run_sweep(args, cfg):
                       "ms_1_row": tot[1], "ms_16_rows": tot[16], "ratio_16_over_1": tot[16] / tot[1]}), flush=True)
 
 
-def roofline_block(cfg, res, args, hbm, peak_kind):
+def gemm_flops(cfg):
+    """Multiply-add flops (x2) of the projections and the LM head per round:
+    the method's (one product per weight and activation row) and the issued
+    ones (bf16 workloads multiply the hi and the lo activation terms).  S = 2
+    runs the layers twice and the second LM head on the K/2 uncommitted rows
+    of each block only."""
+    M, d, F, V, L = cfg.batch * K_BLOCK, cfg.hidden, cfg.ffn, cfg.vocab, cfg.n_layers
+    qd, kvd = cfg.q_dim, cfg.kv_dim
+    per_layer = 2 * M * d * (qd + 2 * kvd) + 2 * M * qd * d + 2 * M * d * 2 * F + 2 * M * F * d
+    proj = L * per_layer * cfg.s_passes
+    lm = 2 * M * d * V + (cfg.s_passes - 1) * 2 * (M // 2) * d * V
+    terms = 2 if cfg.dtype == "bf16" else 1
+    return {"proj": proj, "lm_head": lm, "issued_factor": terms}
+
+
+def tensor_bound(cfg) -> bool:
+    """The projections are tensor-bound from M = 512 activation rows up
+    (weights streamed at M rows have ~M flop per byte, above GB300's ridge)."""
+    return cfg.dtype == "bf16" and cfg.batch * K_BLOCK >= 512
+
+
+def mean_context(res) -> float:
+    """The context grows by tau + 1 per round and is rolled back to the
+    prompt every `period` rounds: mean over the period."""
+    return float(res["lens"].mean()) + 0.5 * res["period"] * (res["mean_tau"] + 1)
+
+
+def roofline_block(cfg, res, hbm, tc, peak_kind):
     """The dominant kernel's roofline (k_gemm_tc: projections + LM head) and
     the per-class figures, from the profiled (second) timed region."""
     ab = algorithmic_bytes(cfg)
-    lens = res["wl"].lens
+    fl = gemm_flops(cfg)
     prof = res["prof"]
-    steps = args.steps
+    steps = res["steps"]
+    B = cfg.batch
     gemm_ms = prof["proj"][0] + prof["lm_head"][0]
     gemm_launches = prof["proj"][1] + prof["lm_head"][1]
-    gemm_bytes = (ab["proj"] + ab["lm_head"]) * steps
-    achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
     per_class = {k: {"ms_per_step": v[0] / steps, "launches_per_step": v[1] / steps} for k, v in prof.items()}
-    # the context grows by tau+1 per round and is rolled back every reset_every rounds
-    mean_ctx = float(lens.mean()) + 0.5 * max(args.reset_every, 1) * (res["mean_tau"] + 1)
-    attn_bytes = kv_bytes(cfg, int(mean_ctx)) * steps
+    attn_bytes = kv_bytes(cfg, int(mean_context(res))) * steps
     if prof["attention"][0] > 0:
         per_class["attention"]["GB_per_s"] = attn_bytes / (prof["attention"][0] / 1e3) / 1e9
-    per_class["proj"]["GB_per_s"] = ab["proj"] * steps / (prof["proj"][0] / 1e3) / 1e9
-    per_class["lm_head"]["GB_per_s"] = ab["lm_head"] * steps / (prof["lm_head"][0] / 1e3) / 1e9
-    inj_bytes = ab["inject_weights"] * steps
+        per_class["attention"]["frac_hbm"] = per_class["attention"]["GB_per_s"] / hbm
+    for k in ("proj", "lm_head"):
+        per_class[k]["GB_per_s"] = ab[k] * steps / (prof[k][0] / 1e3) / 1e9
+        per_class[k]["TFLOP_per_s_method"] = fl[k] * steps / (prof[k][0] / 1e3) / 1e12
+        per_class[k]["TFLOP_per_s_issued"] = fl[k] * fl["issued_factor"] * steps / (prof[k][0] / 1e3) / 1e12
     if prof["inject"][0] > 0:
-        per_class["inject"]["GB_per_s"] = inj_bytes / (prof["inject"][0] / 1e3) / 1e9
-    roof = {"kernel": "k_gemm_tc (tcgen05 projections + LM head)", "bound": "hbm",
-            "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "peak_kind": f"{peak_kind} hbm_gbs", "traffic": gemm_traffic(cfg),
-            "traffic_unit": "bytes per launch (ncu dram read+write; profiles/k_gemm_tc_c2_layer.md)",
-            "algorithmic_bytes_per_launch": (ab["proj"] + ab["lm_head"]) * steps / max(gemm_launches, 1),
-            "bytes_per_step": ab["proj"] + ab["lm_head"], "launches_per_step": gemm_launches / steps,
-            "timed_in": "second timed region of the same loop, per-launch CUDA events"}
+        per_class["inject"]["GB_per_s"] = ab["inject_weights"] * steps / (prof["inject"][0] / 1e3) / 1e9
+        per_class["inject"]["frac_hbm"] = per_class["inject"]["GB_per_s"] / hbm
+    if cfg.accept == "stochastic" and prof["accept"][0] > 0:
+        # each of the tau + 1 target rows read: one pass for its softmax
+        # normaliser, one for the race (fp32 logits)
+        acc_bytes = B * (res["mean_tau"] + 1) * cfg.vocab * 4 * 2 * steps
+        per_class["accept"]["GB_per_s"] = acc_bytes / (prof["accept"][0] / 1e3) / 1e9
+        per_class["accept"]["frac_hbm"] = per_class["accept"]["GB_per_s"] / hbm
+    per_class["synthetic_target"] = {"ms_per_step": res["target_ms"] / steps,
+                                     "what": "torch ops that form the target's verify output; not this library's"}
+    common = {"kernel": "k_gemm_tc (tcgen05 projections + LM head)",
+              "launches_per_step": gemm_launches / steps,
+              "timed_in": "second timed region of the same loop, per-launch CUDA events"}
+    if tensor_bound(cfg):
+        flops = (fl["proj"] + fl["lm_head"]) * steps
+        achieved = flops / (gemm_ms / 1e3) / 1e12
+        roof = dict(common, bound="tensor", achieved=achieved, peak=tc, unit="TFLOP/s", frac=achieved / tc,
+                    peak_kind=f"{peak_kind} bf16_tflops_sustained (kernels timed inside a seconds-long loop)",
+                    flops_per_step=fl["proj"] + fl["lm_head"], traffic=None,
+                    issued={"achieved": achieved * fl["issued_factor"], "frac": achieved * fl["issued_factor"] / tc,
+                            "what": "both bf16 activation terms (hi + lo) multiplied: twice the method's flops"})
+        return roof, per_class
+    gemm_bytes = (ab["proj"] + ab["lm_head"]) * steps
+    achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
+    roof = dict(common, bound="hbm", achieved=achieved, peak=hbm, unit="GB/s", frac=achieved / hbm,
+                peak_kind=f"{peak_kind} hbm_gbs", traffic=gemm_traffic(cfg),
+                traffic_unit="bytes per launch (ncu dram read+write; profiles/k_gemm_tc_c2_layer.md)",
+                algorithmic_bytes_per_launch=(ab["proj"] + ab["lm_head"]) * steps / max(gemm_launches, 1),
+                bytes_per_step=ab["proj"] + ab["lm_head"])
     return roof, per_class
 
 
-def run_fp8_leg(args, world, rank, local, hbm, peak_kind):
-    """The same workload with FP8 (E4M3, per-row scale) projection weights:
-    its own rounds, timed the same way (no e2e or graph legs)."""
+def run_per_config(args, names, world, rank, local, hbm, tc, peak_kind):
+    """The other workloads, each timed like the headline one (its own
+    warm-up, region A with clocks, region B per kernel class), without the
+    end-to-end and graph legs."""
     import torch
-    cfg8 = synth.CONFIGS["c2w8"]
-    a8 = argparse.Namespace(**vars(args))
-    a8.no_graph = True
-    a8.e2e_steps = 0
+    out = {}
+    for name in names:
+        c = synth.get_config(name)
+        torch.cuda.empty_cache()
+        res = run_ours(args, c, world, rank, local, steps=args.per_config_steps, legs=False)
+        roof, per_class = roofline_block(c, res, hbm, tc, peak_kind)
+        out[name] = {"workload": c.name, "value": res["value"], "unit": UNIT,
+                     "ms_per_step": res["ms"] / res["steps"], "steps": res["steps"], "warmup": args.warmup,
+                     "dtype": line_dtype(c), "mean_tau": res["mean_tau"], "accept": c.accept,
+                     "rounds_per_prompt": res["period"], "mean_context": mean_context(res),
+                     "roofline": roof, "kernels": per_class, "clocks": res["clocks"],
+                     "gpu_launches_per_step": res["launches_per_step"]}
+        del res
     torch.cuda.empty_cache()
-    res = run_ours(a8, cfg8, world, rank, local)
-    roof, per_class = roofline_block(cfg8, res, a8, hbm, peak_kind)
-    roof.pop("traffic_unit")
-    roof["traffic"] = None
-    return {"workload": cfg8.name, "value": res["value"], "unit": UNIT, "ms_per_step": res["ms"] / args.steps,
-            "mean_tau": res["mean_tau"], "roofline": roof,
-            "kernels": {k: v for k, v in per_class.items() if k in ("proj", "lm_head", "inject")}}
+    return out
+
+
+def line_dtype(cfg) -> str:
+    """The arithmetic the path computes in: fp32 SIMT for fp32 workloads,
+    bf16 tensor-core products (fp32 accumulation) otherwise, with E4M3
+    weights widened to bf16 for the FP8-weight workloads."""
+    if cfg.dtype == "f32":
+        return "f32"
+    return "bf16 (e4m3 weights)" if cfg.weight_format == "e4m3" else "bf16"
 
 
 def run_kernel_train_attn(args, cfg):
@@ -827,28 +995,38 @@ def main(argv=None):
         return
     hbm, tc, peak_kind = load_peaks()
     steps = args.steps
-    lens = res["wl"].lens
-    roof, per_class = roofline_block(cfg, res, args, hbm, peak_kind)
-    fp8 = None
-    if not args.no_fp8 and cfg.name == synth.CONFIGS["c2"].name and world == 1:
-        fp8 = run_fp8_leg(args, world, rank, local, hbm, peak_kind)
+    lens = res["lens"]
+    roof, per_class = roofline_block(cfg, res, hbm, tc, peak_kind)
+    wl = res.pop("wl")
+    w_np, prefill, stoch = wl.w_np, wl.prefill, wl.stochastic
+    del wl
+    per_config = None
+    names = [n for n in args.per_config.split(",") if n and n != args.config]
+    if names and world == 1:
+        per_config = run_per_config(args, names, world, rank, local, hbm, tc, peak_kind)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(cfg, args, res["wl"].w_np)
+        cpu = cpu_baseline(cfg, args, w_np)
+    target = ("per step, torch forms the target's logits: the draft call's logits output (pass-1 rows on the "
+              "committed positions, pass-2 rows elsewhere) + N(0,1) noise from 4 device-resident draws, the bonus "
+              "row noise alone; inside the region, timed as kernels.synthetic_target" if stoch else
+              "per step, one torch elementwise op forms y from the drafts and the round's coins; inside the region")
     line = {
         "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": res["ms"] / steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights, N(0,1) features)",
-        "config": dict(config_block(cfg, lens), mean_tau=res["mean_tau"], parallelism=f"replicas x{world}",
-                       synthetic_target="one torch elementwise op per step forms y from the drafts; inside the region"),
+        "vs_baseline": None, "dtype": line_dtype(cfg),
+        "data": "synthetic (seeded random-init weights, N(0,1) features)",
+        "config": config_block(cfg, lens),
+        "mean_tau": res["mean_tau"], "mean_context": mean_context(res), "parallelism": f"replicas x{world}",
+        "synthetic_target": target,
         "roofline": roof,
         "kernels": per_class,
         "cpu_baseline": cpu,
         "accepted_tok_per_s": world * cfg.batch * (res["mean_tau"] + 1) / (res["ms"] / steps / 1e3),
-        "prefill_inject": res["wl"].prefill,
+        "prefill_inject": prefill,
         "e2e": res["e2e"],
         "graph": res["graph"],
-        "fp8_weights": fp8,
+        "per_config": per_config,
         "gpu_launches": int(round(res["launches_per_step"] * steps)),
         "clocks": res["clocks"],
     }

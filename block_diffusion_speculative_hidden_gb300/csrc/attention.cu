@@ -166,13 +166,11 @@ template <typename T, int DH, int G>
 static cudaError_t launch_attn_t(dflash_ctx* c, int layer, int B, int splits, cudaStream_t s) {
   using C = AttnCfg<DH, G>;
   using KT = typename std::conditional<std::is_same<T, float>::value, float, __half>::type;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_attn_split<KT, DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static FuncAttr smem_attr;
+  cudaError_t ae = smem_attr.ensure(C::SMEM, [](int v) {
+    return cudaFuncSetAttribute(k_attn_split<KT, DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  });
+  if (ae != cudaSuccess) return ae;
   const auto& g = c->cfg;
   const long long layer_off = static_cast<long long>(layer) * c->pool_pages * g.n_kv_heads * kPage * DH;
   dim3 grid(splits, g.n_kv_heads, B);

@@ -725,19 +725,14 @@ int smem_bytes(int page_slots) {
 
 template <int DH, int G, int KBP, int NST>
 cudaError_t set_attrs(int smem) {
-  static int attr_smem = 0;
-  static bool np = false;
-  if (!np) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<DH, G, KBP, NST>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    np = true;
-  }
-  if (smem > attr_smem) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<DH, G, KBP, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_smem = smem;
-  }
-  return cudaSuccess;
+  static FuncAttr cluster_attr, smem_attr;
+  cudaError_t e = cluster_attr.ensure(1, [](int v) {
+    return cudaFuncSetAttribute(k_attn_mma<DH, G, KBP, NST>, cudaFuncAttributeNonPortableClusterSizeAllowed, v);
+  });
+  if (e != cudaSuccess) return e;
+  return smem_attr.ensure(smem, [](int v) {
+    return cudaFuncSetAttribute(k_attn_mma<DH, G, KBP, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  });
 }
 
 // Pages one split can hold at most (the split's share of the longest

@@ -16,17 +16,25 @@ using namespace dflash;
 namespace dflash {
 
 bool prefer_max_smem(const void* kernel) {
-  // a fixed table (no host heap): the library has a few dozen kernel instances
+  // a fixed table (no host heap) of (kernel, device) pairs already set: the
+  // attribute belongs to the kernel on one device; the library has a few
+  // dozen kernel instances
   static std::mutex mu;
-  static const void* done[256];
+  static const void* done[512];
+  static int done_dev[512];
   static int n_done = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_done; ++i)
-    if (done[i] == kernel) return true;
+    if (done[i] == kernel && done_dev[i] == dev) return true;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
       cudaSuccess)
     return false;
-  if (n_done < 256) done[n_done++] = kernel;
+  if (n_done < 512) {
+    done[n_done] = kernel;
+    done_dev[n_done++] = dev;
+  }
   return true;
 }
 
@@ -161,6 +169,7 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   void* ac = lo ? w.take(Mc * d * e) : nullptr;
   void* ac_lo = lo ? w.take(Mc * d * e) : nullptr;
   auto ss_c = lo ? static_cast<float*>(w.take(sizeof(float) * d_tiles * Mc)) : nullptr;
+  auto crow = lo ? static_cast<int32_t*>(w.take(sizeof(int32_t) * Mc)) : nullptr;
   if (c != nullptr) {
     c->status = status;
     c->scal = status + 4;
@@ -199,6 +208,7 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
     c->ac = ac;
     c->ac_lo = ac_lo;
     c->ss_c = ss_c;
+    c->crow = crow;
   }
   return w.off;
 }
@@ -599,9 +609,9 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
         DF_RUN(run_gemm(ctx, ctx->w_down[l], w_row_scale(ctx->s_down, l), d, F, ctx->act, ctx->act_lo, M, Mmax, s_dn, nullptr, e, s));
       }
     }
-    // the second pass needs the LM head on its uncommitted rows only: without
-    // a logits store (which wants every row in place) they are compacted first
-    const bool compact = pass == 1 && g.dtype != DFLASH_F32 && logits == nullptr;
+    // the second pass needs the LM head on its uncommitted rows only: they
+    // are compacted first (a logits store puts each row back in its place)
+    const bool compact = pass == 1 && g.dtype != DFLASH_F32;
     if (compact) {
       ProfScope pc(ctx, DFLASH_PROF_ROWWISE, 1, s);
       DF_CHECK(launch_compact_rows(ctx, B, Mmax, s));
@@ -626,6 +636,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int B, int S, int32_t* draft_t
       lm.logits = logits;
       lm.ld_logits = g.vocab;
       lm.skip_rows = skip;
+      lm.logits_rows = compact ? ctx->crow : nullptr;
       lm.epi = fin;
       DF_CHECK(gemm_launch(ctx, lm, s));
     } else {

@@ -123,6 +123,7 @@ struct TcParams {
   float* logits;
   long long ld_logits;
   const int* skip_rows;
+  const int* logits_rows;  // nullable: row m's logits are stored at row logits_rows[m]
   const float* w_scale;  // W8: fp32 scale of every weight row [N]
   L2Plan l2;  // the next projection's weights, prefetched into L2 after this CTA's last load
 };
@@ -361,8 +362,11 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT, W8>::THREADS, TcCfg<BN, SPLIT
       const int m = m0 + j;
       const bool ok = m < mv;
       if (p.epi.ss_in != nullptr) s_rs[j] = ok ? norm_row_scale(p.epi, m) : 0.f;
-      if (LMHEAD)
-        s_ri[j] = make_int4(0, 0, 0, ok && (p.skip_rows == nullptr || p.skip_rows[m] == 0) ? 1 : 0);
+      if (LMHEAD) {
+        // x: the logits row this row is stored at; w: whether it is stored
+        const int orow = ok ? (p.logits_rows != nullptr ? p.logits_rows[m] : m) : -1;
+        s_ri[j] = make_int4(orow, 0, 0, orow >= 0 && (p.skip_rows == nullptr || p.skip_rows[m] == 0) ? 1 : 0);
+      }
       else
         s_ri[j] = ok ? epi_row_info(p.epi, m) : make_int4(0, 0, 0, 0);
     }
@@ -521,11 +525,10 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT, W8>::THREADS, TcCfg<BN, SPLIT
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int m = m0 + c + j;
         const float z = W8 ? v[j] * wsc : v[j];
         const float val = nv ? (p.epi.ss_in != nullptr ? z * s_rs[c + j] : z) : -INFINITY;
         tile[(c + j) * kLmLd + quad * 32 + lane] = val;
-        if (p.logits != nullptr && nv && s_ri[c + j].w != 0) p.logits[m * p.ld_logits + n] = val;
+        if (p.logits != nullptr && nv && s_ri[c + j].w != 0) p.logits[s_ri[c + j].x * p.ld_logits + n] = val;
       }
     }
     tc_fence_before();
@@ -588,13 +591,11 @@ template <int BN, bool LM, bool SPLIT, bool W8>
 cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& tw, const CUtensorMap& tx,
                              const CUtensorMap& txlo, cudaStream_t s) {
   using C = TcCfg<BN, SPLIT, W8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_gemm_tc<BN, LM, SPLIT, W8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static FuncAttr smem_attr;
+  cudaError_t ae = smem_attr.ensure(C::SMEM, [](int v) {
+    return cudaFuncSetAttribute(k_gemm_tc<BN, LM, SPLIT, W8>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  });
+  if (ae != cudaSuccess) return ae;
   TcParams p;
   const int n_kb = gemm_kb(g.K);
   p.M = g.M;
@@ -613,6 +614,7 @@ cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& tw,
   p.logits = g.logits;
   p.ld_logits = g.ld_logits;
   p.skip_rows = g.skip_rows;
+  p.logits_rows = g.logits_rows;
   p.w_scale = g.w_scale;
   CUtensorMap tn = tw;  // the next projection's weights (a placeholder when there is no plan)
   if (!gemm_l2_plan(c, g.next, &p.l2, &tn)) p.l2 = L2Plan{};

@@ -5,12 +5,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <vector>
 
 #include "../../include/dflash.h"
 #include "epilogue.cuh"
 
 namespace dflash {
+
+// A kernel attribute (the dynamic shared-memory limit, a cluster flag) is
+// a property of the kernel on one device: it must be set on every device a
+// kernel runs on, and calls may come from several host threads.  FuncAttr
+// remembers, per device, the largest value set so far; ensure() sets it
+// (through set(value)) only when a launch needs more.
+struct FuncAttr {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  int value[kMaxDevices] = {};
+  template <class Set>
+  cudaError_t ensure(int need, Set&& set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (value[dev] >= need) return cudaSuccess;
+    e = set(need);
+    if (e == cudaSuccess) value[dev] = need;
+    return e;
+  }
+};
 
 constexpr int kTileN = 128;   // weight rows per GEMM tile (MMA M)
 constexpr int kTileK = 64;    // reduction depth per pipeline stage (one 128-byte swizzle row)
@@ -54,6 +78,7 @@ struct GemmLaunch {
   float* logits;       // nullable: raw logits [M][ld_logits]
   long long ld_logits;
   const int* skip_rows;  // nullable: rows whose logits are not stored
+  const int* logits_rows;  // nullable: row m's logits go to row logits_rows[m] (compacted rows)
   NextGemm next;         // the projection after this one (L2 prefetch of its weights)
   const float* w_scale;  // E4M3 weights (DFLASH_BF16_W8): fp32 scale of every weight row [N]
 };
@@ -135,6 +160,7 @@ struct dflash_ctx {
   // (bf16 family): [max_batch * K/2][hidden] twice, partial sums [ceil(hidden/128)][max_batch * K/2]
   void *ac = nullptr, *ac_lo = nullptr;
   float* ss_c = nullptr;
+  int32_t* crow = nullptr;  // compact row -> block row ([max_batch * K/2])
   // stream being recorded into a graph (dflash_graph_begin), else null
   cudaStream_t capture = nullptr;
   bool capturing = false;

@@ -63,6 +63,9 @@ extern "C" dflash_status dflash_gemm_bf16_noalloc(const void* W, int N, int K, c
     g_scratch_addr[dev] = static_cast<float*>(p);
   }
   float* scratch = g_scratch_addr[dev];
+  // with no caller status word, the kernel's flags go to the array's
+  // reserved slot, which nothing reads back: such a call does not report a
+  // device-side failure (the header says so)
   int* st = status != nullptr ? status : reinterpret_cast<int*>(scratch);
   if (status == nullptr && cudaMemsetAsync(st, 0, sizeof(int), stream) != cudaSuccess) return DFLASH_ERR_CUDA;
   if (splits_used != nullptr) *splits_used = s_used;

@@ -197,10 +197,12 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmPartials lm, int M, const in
 // S = 2, second pass: the K/2 uncommitted rows of each sequence, in position
 // order, into compact rows b * K/2 + r (the two bf16 terms of the LM head's
 // input and their folded-norm partial sums), so that the LM head runs on
-// them alone.  One CTA per compact row.
+// them alone; crow[j] records the block row of compact row j (where a logits
+// store puts it back).  One CTA per compact row.
 __global__ void k_compact_rows(const int32_t* __restrict__ commit, const __nv_bfloat16* __restrict__ a,
                                const __nv_bfloat16* __restrict__ a_lo, const float* __restrict__ ss, int ss_ld,
-                               int d_tiles, int d, __nv_bfloat16* ac, __nv_bfloat16* ac_lo, float* ssc, int ssc_ld) {
+                               int d_tiles, int d, __nv_bfloat16* ac, __nv_bfloat16* ac_lo, float* ssc, int ssc_ld,
+                               int32_t* crow) {
   __shared__ int s_m;
   pdl_wait();
   pdl_trigger();
@@ -213,6 +215,7 @@ __global__ void k_compact_rows(const int32_t* __restrict__ commit, const __nv_bf
         ++cnt;
       }
     s_m = m;
+    crow[j] = m;
   }
   __syncthreads();
   const int m = s_m;  // exactly K/2 rows of every sequence are uncommitted
@@ -296,7 +299,7 @@ cudaError_t launch_compact_rows(dflash_ctx* c, int B, int Mmax, cudaStream_t s) 
   return launch_k(k_compact_rows, dim3(B * kBlockK / 2), dim3(128), 0, s, dim3(1), c->pdl, c->commit,
                   static_cast<const __nv_bfloat16*>(c->a), static_cast<const __nv_bfloat16*>(c->a_lo), c->ss_x, Mmax,
                   d_tiles, d, static_cast<__nv_bfloat16*>(c->ac), static_cast<__nv_bfloat16*>(c->ac_lo), c->ss_c,
-                  c->cfg.max_batch * kBlockK / 2);
+                  c->cfg.max_batch * kBlockK / 2, c->crow);
 }
 
 cudaError_t launch_commit(dflash_ctx* c, int B, cudaStream_t s) {

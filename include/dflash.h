@@ -355,7 +355,12 @@ dflash_status dflash_gemm_w8(const void* W, const float* w_scale, int N, int K, 
  * the library (a __device__ object that every GPU loading the library holds
  * until exit): splits_used * M * N must not exceed 2^21 - 64 floats, else
  * DFLASH_ERR_TOO_LARGE and nothing is enqueued.  status: device int32
- * (caller-owned) or NULL to use a slot in that array, cleared by each call.
+ * (caller-owned), where a bounded device wait that gives up sets
+ * DFLASH_DEV_WAIT_TIMEOUT (out then holds partial sums); the word is only
+ * ever OR-ed into, so clear it before the call.  With status NULL the call
+ * uses a slot of the library's array, cleared by each call, that no entry
+ * point reads back: a device-side failure is then not reported, so callers
+ * that need to know of one pass a status word.
  * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating
  * library routine).  Its first call on a device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current); make that first

@@ -93,10 +93,11 @@ def test_pool_exhaustion_changes_nothing():
 
 @pytest.mark.parametrize("name", ["mini_b", "mini_w8b"])
 def test_second_pass_lm_head_on_uncommitted_rows_only(name):
-    """S = 2: without a logits store the second pass runs the LM head on the
-    K/2 uncommitted rows only (compacted); drafts and confidences equal the
-    path that computes and stores every row's logits, bit for bit (that
-    path is the one checked against the oracle above)."""
+    """S = 2: the second pass runs the LM head on the K/2 uncommitted rows
+    only (compacted), and a logits store puts each of them back at its block
+    row; asking for the logits changes neither the drafts nor the
+    confidences, bit for bit, and the stored logits of the uncommitted rows
+    are the ones checked against the oracle above."""
     import torch
     cfg = synth.get_config(name).replace(weight_std=0.06)
     pair = Pair(cfg, 2)

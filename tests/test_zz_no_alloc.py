@@ -64,16 +64,21 @@ def test_noalloc_matches_regular_entry_on_two_calls_in_a_row():
     import torch
     from block_diffusion_speculative_hidden_gb300 import _lib
     L = _lib.lib()
-    cases = [(16, 640, 1024, 4, True), (33, 200, 520, 3, False)]
-    for i, (M, N, K, splits, with_lo) in enumerate(cases):   # the second call reuses the shared array
+    # the second call reuses the shared array; the third reports device
+    # errors through a status word of its own, which must stay clear
+    cases = [(16, 640, 1024, 4, True, False), (33, 200, 520, 3, False, False), (64, 384, 768, 2, True, True)]
+    for i, (M, N, K, splits, with_lo, own_status) in enumerate(cases):
         W, X, X_lo = _inputs(M, N, K, 100 + i, with_lo)
         ref, used = _regular(L, W, X, X_lo, splits)
         out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda") if own_status else None
         got = ctypes.c_int(0)
         rc = L.dflash_gemm_bf16_noalloc(_ptr(W), N, K, _ptr(X), _ptr(X_lo), M, _ptr(out), splits,
-                                        ctypes.byref(got), None, _stream())
+                                        ctypes.byref(got), _ptr(status), _stream())
         torch.cuda.synchronize()
         assert rc == 0 and got.value == used
+        if own_status:
+            assert int(status.item()) == 0
         # the tolerance of the projection tests (fp32 accumulation of K products)
         np.testing.assert_allclose(out.cpu().numpy(), ref.cpu().numpy(), atol=4e-5 * np.sqrt(K), rtol=1e-5)
 
