@@ -103,6 +103,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
 // Every thread of every CTA in the cluster arrives and waits (release /
 // acquire): shared-memory writes before it are visible to the whole cluster.
 __device__ __forceinline__ void cluster_sync_all() {
@@ -146,6 +151,17 @@ __device__ __forceinline__ void bulk_copy_smem_to_rank(uint32_t dst_local, uint3
       "r"(src_local), "r"(bytes), "r"(dsmem_map(smem_u32(bar), rank))
       : "memory");
 }
+// Bulk copy shared memory -> global memory (the copy engine reads the
+// source asynchronously; 16-byte aligned addresses, a multiple of 16 bytes),
+// with an L2 cache policy; completes in this thread's bulk async-group.
+__device__ __forceinline__ void bulk_store_global(void* dst, uint32_t src_local, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+               "r"(src_local), "r"(bytes), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the copy engine has read the sources of this thread's bulk copies.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }

@@ -691,7 +691,8 @@ dflash_status dflash_accept(dflash_ctx* ctx, int mode, int B, const int32_t* dra
   ProfScope p(ctx, DFLASH_PROF_ACCEPT, 1, s);
   int* round_ctr = round == DFLASH_ROUND_DEVICE ? ctx->status + 2 : nullptr;
   DF_CHECK(launch_accept_stochastic(B, kBlockK, ctx->cfg.vocab, draft_tokens, target_logits, draft_probs,
-                                    temperature, seed, round, round_ctr, accept_len, emitted, n_emit, ctx->pdl, s));
+                                    temperature, seed, round, round_ctr, accept_len, emitted, n_emit, ctx->num_sms,
+                                    ctx->pdl, s));
   return DFLASH_OK;
 }
 
@@ -724,6 +725,7 @@ dflash_status dflash_gemm_bf16(const void* W, int N, int K, const void* X, const
   tmp.cfg = dflash_config{};
   tmp.cfg.dtype = DFLASH_BF16;
   tmp.status = status;
+  tmp.num_sms = device_sms();
   const int n_kb = gemm_kb(K);
   const int want = std::min(splits, n_kb);
   const int per = (n_kb + want - 1) / want;

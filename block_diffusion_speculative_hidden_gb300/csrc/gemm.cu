@@ -8,7 +8,7 @@
 #include <cstdio>
 #include <cudaTypedefs.h>
 
-#include "gemm_kernel.cuh"
+#include "gemm_persist.cuh"
 
 namespace dflash {
 
@@ -234,6 +234,18 @@ bool gemm_l2_plan(dflash_ctx* c, const NextGemm& nx, L2Plan* pl, CUtensorMap* ma
   return true;
 }
 
+int pers_bn(int M, int N, int num_sms) {
+  // the persistent kernel serves the tensor-bound sizes (at least 256
+  // activation rows) with 128-row activation tiles, where the tiles fill the
+  // SMs in waves that are at least 75 % full on average (measured: 64-row
+  // tiles, and fewer tiles, ran slower than the split-K kernel)
+  if (M < 256 || num_sms < 1) return 0;
+  const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + 127) / 128);
+  if (tiles < num_sms) return 0;
+  const long long waves = (tiles + num_sms - 1) / num_sms;
+  return 4 * tiles >= 3 * waves * num_sms ? 128 : 0;
+}
+
 int gemm_bn(int M, bool split, bool w8) {
   const int cap = split || w8 ? 128 : 256;  // E4M3: the 256-row tile's stages would not hold its epilogue
   int bn = 16;
@@ -253,6 +265,17 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s) {
     return cudaGetLastError();
   }
   const bool split = g.X_lo != nullptr, w8 = c->cfg.dtype == DFLASH_BF16_W8;
+  const int pbn = (!w8 && split && (g.splits == 1 || g.epi.kind != EPI_NONE)) ? pers_bn(g.M, g.N, c->num_sms) : 0;
+  if (pbn > 0) {
+    // many activation rows: the persistent kernel (every tile owns its whole
+    // reduction, so the caller's split count does not apply)
+    CUtensorMap tw, tx, txlo;
+    if (!get_tmap(c, g.W, g.N, g.K, kTileN, &tw) || !get_tmap(c, g.X, g.M_alloc, g.K, pbn, &tx) ||
+        !get_tmap(c, g.X_lo, g.M_alloc, g.K, pbn, &txlo))
+      return cudaErrorInvalidValue;
+    const bool lm = g.lm.mx != nullptr;
+    return lm ? launch_pers<128, true>(c, g, tw, tx, txlo, s) : launch_pers<128, false>(c, g, tw, tx, txlo, s);
+  }
   const int bn = gemm_bn(g.M, split, w8);
   CUtensorMap tw, tx, txlo;
   if (!get_tmap(c, g.W, g.N, g.K, kTileN, &tw, w8 ? 1 : 0) || !get_tmap(c, g.X, g.M_alloc, g.K, bn, &tx))

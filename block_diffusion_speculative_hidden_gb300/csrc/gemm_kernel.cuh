@@ -124,6 +124,7 @@ struct TcParams {
   long long ld_logits;
   const int* skip_rows;
   const int* logits_rows;  // nullable: row m's logits are stored at row logits_rows[m]
+  int logits_bulk;         // logits rows 16-byte aligned: whole tiles leave by bulk copies
   const float* w_scale;  // W8: fp32 scale of every weight row [N]
   L2Plan l2;  // the next projection's weights, prefetched into L2 after this CTA's last load
 };
@@ -508,10 +509,15 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT, W8>::THREADS, TcCfg<BN, SPLIT
       }
     }
   } else {
-    // LM head: the scaled logits go to a padded [BN][kLmLd] tile (and, when
-    // asked for, to global memory); then 8 threads per row reduce it to the
-    // tile's (max, lowest argmax, sum of exp(z - max)), 16 rows at a time.
+    // LM head: the scaled logits go to a padded [BN][kLmLd] tile; then 8
+    // threads per row reduce it to the tile's (max, lowest argmax, sum of
+    // exp(z - max)), 16 rows at a time.  When the logits are asked for, a
+    // whole 128-column tile leaves by bulk copies, one 512-byte row each
+    // (issued by warp 0 once the tile is complete, evict-first in L2, read
+    // from shared memory while the reduction runs); a ragged tile, or rows
+    // that are not 16-byte aligned, by streaming stores.
     float* tile = reinterpret_cast<float*>(smem);
+    const bool bulk_out = p.logits != nullptr && p.logits_bulk && n0 + kTileN <= p.N;
     epi_sync();
 #pragma unroll 1
     for (int c = 16 * wg; c < BN; c += 16 * (kGemmThreads / 128)) {
@@ -528,11 +534,20 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT, W8>::THREADS, TcCfg<BN, SPLIT
         const float z = W8 ? v[j] * wsc : v[j];
         const float val = nv ? (p.epi.ss_in != nullptr ? z * s_rs[c + j] : z) : -INFINITY;
         tile[(c + j) * kLmLd + quad * 32 + lane] = val;
-        if (p.logits != nullptr && nv && s_ri[c + j].w != 0) p.logits[s_ri[c + j].x * p.ld_logits + n] = val;
+        if (!bulk_out && p.logits != nullptr && nv && s_ri[c + j].w != 0)
+          __stcs(p.logits + s_ri[c + j].x * p.ld_logits + n, val);
       }
     }
     tc_fence_before();
+    if (bulk_out) fence_proxy_async_smem();  // the tile, as the copy engine will read it
     epi_sync();
+    if (bulk_out && warp == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      for (int j = lane; j < BN; j += 32)
+        if (s_ri[j].w != 0)
+          bulk_store_global(p.logits + s_ri[j].x * p.ld_logits + n0, smem_u32(tile + j * kLmLd), kTileN * 4, pol);
+      bulk_commit();
+    }
     const int seg = threadIdx.x & 7;
 #pragma unroll 1
     for (int rb = 0; rb < BN; rb += kGemmThreads >> 3) {
@@ -576,6 +591,7 @@ __global__ void __launch_bounds__(TcCfg<BN, SPLIT, W8>::THREADS, TcCfg<BN, SPLIT
       }
     }
     tc_fence_before();
+    if (bulk_out && warp == 0) bulk_wait_read_all();  // the tile stays put until the copies have read it
   }
   epi_sync();
   if (warp == ALLOC_WARP) {
@@ -615,6 +631,7 @@ cudaError_t launch_tc(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& tw,
   p.ld_logits = g.ld_logits;
   p.skip_rows = g.skip_rows;
   p.logits_rows = g.logits_rows;
+  p.logits_bulk = g.logits != nullptr && (reinterpret_cast<uintptr_t>(g.logits) & 15) == 0 && g.ld_logits % 4 == 0;
   p.w_scale = g.w_scale;
   CUtensorMap tn = tw;  // the next projection's weights (a placeholder when there is no plan)
   if (!gemm_l2_plan(c, g.next, &p.l2, &tn)) p.l2 = L2Plan{};

@@ -1,0 +1,437 @@
+// The persistent tcgen05 projection kernel for many activation rows (the
+// serving batches: 512 and more block rows), bf16 weights with the hi + lo
+// activation pair.
+//
+// At these sizes the projections are tensor-bound, and a kernel that gives
+// each CTA one output tile leaves the tensor pipe idle while the CTA starts
+// (barriers, TMEM, the first loads) and while it finishes (accumulator
+// readout, fused epilogue).  Here one CTA per SM walks a list of output
+// tiles (128 weight rows x BN activation rows, activation tile fastest so
+// that CTAs running at the same time share weight tiles in L2):
+//
+//   - warp 4, one thread: TMA loads of the weight tile and both activation
+//     terms, 64 k a stage, into an STAGES-deep ring that runs across tile
+//     boundaries;
+//   - warp 5, one thread: one MMA of N = 2 BN per 16-k slice (the hi and lo
+//     activation tiles lie back to back, so one MMA yields W.hi and W.lo
+//     side by side) into one of two TMEM accumulators, alternating by tile;
+//     warp 5 owns the TMEM allocation;
+//   - warps 0-3 (TMEM lane quadrants 0-3): read an accumulator out into a
+//     shared-memory tile of their own, release the accumulator (so the MMAs
+//     of the tile after next may start), then run the same fused epilogue
+//     as the single-tile kernel while the MMAs of the next tile proceed.
+//
+// Every wait is bounded; after a wait gives up the CTA marks the status
+// word, the roles stop waiting on one another (a shared abort flag) and the
+// epilogue warps still meet at every named barrier.
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace dflash {
+
+template <int BN, bool LMHEAD>
+struct PersCfg {
+  static constexpr int W_BYTES = kTileN * kTileK * 2;          // 16 KB
+  static constexpr int X_BOX = BN * kTileK * 2;                 // one activation term, 64 k
+  static constexpr int STAGE_BYTES = W_BYTES + 2 * X_BOX;       // weights, hi, lo
+  static constexpr int NMMA = 2 * BN;                           // MMA N: hi and lo rows
+  static constexpr int ACC_COLS = NMMA;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;                // two accumulators
+  static constexpr int LD = LMHEAD ? kLmLd : 128;               // epilogue tile row stride (floats)
+  static constexpr int EPI_BYTES = BN * LD * 4;
+  static constexpr int AUX_BYTES = 256 /*barriers*/ + BN * 4 * 4 /*red*/ + BN * 4 /*row scales*/ + BN * 16;
+  static constexpr int SMEM_MAX = 232448;                       // 227 KB a CTA
+  static constexpr int STAGES_RAW = (SMEM_MAX - 1024 - EPI_BYTES - AUX_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW < 6 ? STAGES_RAW : 6;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = 1024 + RING_BYTES + EPI_BYTES + AUX_BYTES;
+  static constexpr int THREADS = 192;
+  static constexpr int PRODUCER = 4, MMA_WARP = 5;
+  static_assert(STAGES >= 3, "ring too shallow");
+  static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(SMEM <= SMEM_MAX, "shared memory");
+};
+
+struct PersParams {
+  int M, N, n_kb;
+  int n_tiles, m_tiles;  // weight tiles (128 rows) and activation tiles (BN rows), host bounds
+  float* out;            // EPI_NONE: the result [M][ldo]
+  int ldo;
+  const int* m_valid;
+  int* status;
+  EpiArgs epi;
+  LmPartials lm;
+  float* logits;
+  long long ld_logits;
+  const int* skip_rows;
+  const int* logits_rows;
+  int logits_bulk;
+};
+
+// STORE / RESIDUAL epilogue of one tile, row-major: warp w finishes rows
+// w, w + 4, ... and lane l the columns n0 + 4l .. n0 + 4l + 3 (128-bit loads
+// and stores), eight rows a batch with their loads in flight together; the
+// sum of z^2 of a row over the tile's columns is one warp reduction.  The
+// same function as apply_epilogue's STORE / RESIDUAL branch (e.N a multiple
+// of 4, bf16 next input).
+__device__ __forceinline__ void epilogue_rows_vec(const EpiArgs& e, const float* tile, int m0, int rows, int n0,
+                                                  const float* rs) {
+  constexpr int B = 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = n0 + 4 * lane;
+  const bool nv = n < e.N;  // N % 4 == 0: the four columns are valid together
+  float4 gn = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (e.nx_hi != nullptr && nv) {
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(e.nx_gain) + n);
+    const float2 a = __bfloat1622float2(g2[0]), b = __bfloat1622float2(g2[1]);
+    gn = make_float4(a.x, a.y, b.x, b.y);
+  }
+  for (int j0 = warp; j0 < rows; j0 += 4 * B) {
+    float4 z[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int j = j0 + 4 * u;
+      z[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (nv && j < rows && e.kind == EPI_RESIDUAL)
+        z[u] = *reinterpret_cast<const float4*>(e.out + static_cast<long long>(m0 + j) * e.N + n);
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int j = j0 + 4 * u;
+      float sq = 0.f;
+      if (nv && j < rows) {
+        const float sc = rs != nullptr ? rs[j] : 1.f;
+        const float4 t = *reinterpret_cast<const float4*>(tile + j * 128 + 4 * lane);
+        float4 v = z[u];
+        v.x += t.x * sc;
+        v.y += t.y * sc;
+        v.z += t.z * sc;
+        v.w += t.w * sc;
+        const long long o = static_cast<long long>(m0 + j) * e.N + n;
+        if (e.out != nullptr) *reinterpret_cast<float4*>(e.out + o) = v;
+        if (e.nx_hi != nullptr) {
+          const float a0 = gn.x * v.x, a1 = gn.y * v.y, a2 = gn.z * v.z, a3 = gn.w * v.w;
+          const __nv_bfloat162 h01 = __floats2bfloat162_rn(a0, a1), h23 = __floats2bfloat162_rn(a2, a3);
+          const __nv_bfloat162 l01 = __floats2bfloat162_rn(a0 - __low2float(h01), a1 - __high2float(h01));
+          const __nv_bfloat162 l23 = __floats2bfloat162_rn(a2 - __low2float(h23), a3 - __high2float(h23));
+          uint2 hv, lv;
+          hv.x = *reinterpret_cast<const uint32_t*>(&h01);
+          hv.y = *reinterpret_cast<const uint32_t*>(&h23);
+          lv.x = *reinterpret_cast<const uint32_t*>(&l01);
+          lv.y = *reinterpret_cast<const uint32_t*>(&l23);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(e.nx_hi) + o) = hv;
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(e.nx_lo) + o) = lv;
+        }
+        sq = (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+      }
+      if (e.ss_out != nullptr && j < rows) {  // uniform per warp
+        sq = warp_sum(sq);
+        if (lane == 0) e.ss_out[static_cast<long long>(n0 >> 7) * e.ss_ld + m0 + j] = sq;
+      }
+    }
+  }
+}
+
+template <int BN, bool LMHEAD>
+__global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
+    k_gemm_pers(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ CUtensorMap tmXlo, const __grid_constant__ PersParams p) {
+  using C = PersCfg<BN, LMHEAD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;                                         // [STAGES][W | X hi | X lo]
+  float* tile = reinterpret_cast<float*>(smem + C::RING_BYTES);  // [BN][LD] epilogue tile
+  uint8_t* aux = smem + C::RING_BYTES + C::EPI_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(aux);            // [STAGES] stage landed
+  uint64_t* empty = full + C::STAGES;                           // [STAGES] stage consumed by the MMAs
+  uint64_t* accf = empty + C::STAGES;                           // [2] accumulator complete
+  uint64_t* acce = accf + 2;                                    // [2] accumulator read out
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  static_assert((2 * C::STAGES + 4) * 8 + 8 <= 256, "barrier area");
+  float* red = reinterpret_cast<float*>(aux + 256);             // [BN][4]
+  float* s_rs = red + 4 * BN;                                   // folded-RMSNorm row scales
+  int4* s_ri = reinterpret_cast<int4*>(s_rs + BN);              // per-row epilogue facts
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // m_valid is written two kernels upstream (page allocation), never by the
+  // predecessor, so every role may size the work list before pdl_wait
+  const int mv = p.m_valid != nullptr ? min(p.M, __ldg(p.m_valid)) : p.M;
+  const int m_tiles = min(p.m_tiles, (mv + BN - 1) / BN);
+  const int n_work = p.n_tiles * m_tiles;
+  const int my_tiles = static_cast<int>(blockIdx.x) < n_work
+                           ? (n_work - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                 static_cast<int>(gridDim.x)
+                           : 0;
+  auto tile_of = [&](int tl, int& n0, int& m0) {
+    const int t = static_cast<int>(blockIdx.x) + tl * static_cast<int>(gridDim.x);
+    n0 = (t / m_tiles) * kTileN;
+    m0 = (t % m_tiles) * BN;
+  };
+
+  if (warp == C::PRODUCER && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmXlo);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&accf[a], 1);
+      mbar_init(&acce[a], 4);  // one arrival per epilogue warp
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::PRODUCER) {
+    if (lane == 0) {
+      const int total = my_tiles * p.n_kb;
+      auto coords = [&](int it, int& n0, int& m0, int& kx) {
+        tile_of(it / p.n_kb, n0, m0);
+        kx = (it % p.n_kb) * kTileK;
+      };
+      // the weights do not depend on the predecessor: the first stages'
+      // weight tiles go out before its completion, their activations after
+      const int pre = min(total, C::STAGES);
+      for (int it = 0; it < pre; ++it) {
+        int n0, m0, kx;
+        coords(it, n0, m0, kx);
+        mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
+        tma_load_2d(ring + it * C::STAGE_BYTES, &tmW, &full[it], kx, n0);
+      }
+      pdl_wait();
+      pdl_trigger();
+      for (int it = 0; it < pre; ++it) {
+        int n0, m0, kx;
+        coords(it, n0, m0, kx);
+        uint8_t* st = ring + it * C::STAGE_BYTES;
+        tma_load_2d(st + C::W_BYTES, &tmX, &full[it], kx, m0);
+        tma_load_2d(st + C::W_BYTES + C::X_BOX, &tmXlo, &full[it], kx, m0);
+      }
+      int issued = pre;
+      for (int it = pre; it < total; ++it) {
+        const int s = it % C::STAGES;
+        if (*s_abort || !mbar_wait(&empty[s], ((it / C::STAGES) & 1) ^ 1, p.status)) {
+          *s_abort = 1;
+          break;
+        }
+        int n0, m0, kx;
+        coords(it, n0, m0, kx);
+        uint8_t* st = ring + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        tma_load_2d(st, &tmW, &full[s], kx, n0);
+        tma_load_2d(st + C::W_BYTES, &tmX, &full[s], kx, m0);
+        tma_load_2d(st + C::W_BYTES + C::X_BOX, &tmXlo, &full[s], kx, m0);
+        issued = it + 1;
+      }
+      // leave only once every copy this thread issued has landed
+      for (int it = max(0, issued - C::STAGES); it < issued; ++it)
+        mbar_wait(&full[it % C::STAGES], (it / C::STAGES) & 1, p.status);
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = mma_idesc_bf16_f32(kTileN, C::NMMA);
+      int it = 0;
+      bool ok = true;
+      for (int tl = 0; ok && tl < my_tiles; ++tl) {
+        const int a = tl & 1;
+        // the epilogue has read accumulator a out (its use two tiles ago)
+        if (tl >= 2 && (*s_abort || !mbar_wait(&acce[a], ((tl >> 1) & 1) ^ 1, p.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + static_cast<uint32_t>(a * C::ACC_COLS);
+        for (int kb = 0; kb < p.n_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          if (*s_abort || !mbar_wait(&full[s], (it / C::STAGES) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aW = smem_u32(ring + s * C::STAGE_BYTES);
+          const uint32_t aX = aW + C::W_BYTES;
+#pragma unroll
+          for (int k = 0; k < kTileK / 16; ++k)
+            tc_mma_bf16(acc, sw128_kmajor_desc(aW + 32 * k), sw128_kmajor_desc(aX + 32 * k), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&accf[a]);
+      }
+      if (!ok) *s_abort = 1;
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue warps 0-3: TMEM lane quadrant = warp
+    pdl_wait();  // the row facts below read the predecessor's output
+    bool live = true;
+    const uint32_t tquad = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int tl = 0; tl < my_tiles; ++tl) {
+      int n0, m0;
+      tile_of(tl, n0, m0);
+      const int n = n0 + warp * 32 + lane;
+      const bool nv = n < p.N;
+      for (int j = threadIdx.x; j < BN; j += kEpiThreads) {
+        const int m = m0 + j;
+        const bool ok = m < mv;
+        if (p.epi.ss_in != nullptr) s_rs[j] = ok ? norm_row_scale(p.epi, m) : 0.f;
+        if constexpr (LMHEAD) {
+          const int orow = ok ? (p.logits_rows != nullptr ? p.logits_rows[m] : m) : -1;
+          s_ri[j] = make_int4(orow, 0, 0, orow >= 0 && (p.skip_rows == nullptr || p.skip_rows[m] == 0) ? 1 : 0);
+        } else {
+          s_ri[j] = ok ? epi_row_info(p.epi, m) : make_int4(0, 0, 0, 0);
+        }
+      }
+      const int a = tl & 1;
+      live = live && !*s_abort && mbar_wait(&accf[a], (tl >> 1) & 1, p.status);
+      if (!live) *s_abort = 1;
+      __syncwarp();
+      tc_fence_after();
+      epi_sync();  // the row facts are complete
+      const uint32_t tacc = tquad + static_cast<uint32_t>(a * C::ACC_COLS);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        float v[16], v2[16];
+        if (live) {
+          tc_ld_32x32b_x16(tacc + c, v);
+          tc_ld_32x32b_x16(tacc + BN + c, v2);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float z = live ? v[j] + v2[j] : 0.f;
+          if constexpr (LMHEAD) z = nv ? (p.epi.ss_in != nullptr ? z * s_rs[c + j] : z) : -INFINITY;
+          tile[(c + j) * C::LD + warp * 32 + lane] = z;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbarrier_arrive_one(&acce[a]);  // accumulator a may take the tile after next
+      if constexpr (LMHEAD) {
+        const bool bulk_out = p.logits != nullptr && p.logits_bulk && n0 + kTileN <= p.N;
+        if (!bulk_out && p.logits != nullptr && nv)
+          for (int j = 0; j < BN; ++j)
+            if (s_ri[j].w != 0) __stcs(p.logits + s_ri[j].x * p.ld_logits + n, tile[j * C::LD + warp * 32 + lane]);
+        if (bulk_out) fence_proxy_async_smem();
+        epi_sync();
+        if (bulk_out && warp == 0) {
+          const uint64_t pol = l2_policy_evict_first();
+          for (int j = lane; j < BN; j += 32)
+            if (s_ri[j].w != 0)
+              bulk_store_global(p.logits + s_ri[j].x * p.ld_logits + n0, smem_u32(tile + j * C::LD), kTileN * 4, pol);
+          bulk_commit();
+        }
+        // (max, lowest argmax, sum of exp(z - max)) of each row over the
+        // tile's 128 columns: 8 threads a row, 16 rows at a time
+        const int seg = threadIdx.x & 7;
+        const int ntile = n0 / kTileN;
+#pragma unroll 1
+        for (int rb = 0; rb < BN; rb += kEpiThreads >> 3) {
+          const int j = rb + (threadIdx.x >> 3);
+          const float* row = tile + j * C::LD;
+          float z[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) z[k] = row[seg + 8 * k];
+          float mx = z[0];
+          int ix = seg;
+#pragma unroll
+          for (int k = 1; k < 16; ++k)
+            if (z[k] > mx) {
+              mx = z[k];
+              ix = seg + 8 * k;
+            }
+#pragma unroll
+          for (int o = 4; o > 0; o >>= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+            if (om > mx || (om == mx && oi < ix)) {
+              mx = om;
+              ix = oi;
+            }
+          }
+          float se = 0.f;
+          if (mx > -INFINITY)
+#pragma unroll
+            for (int k = 0; k < 16; ++k) se += expf(z[k] - mx);
+#pragma unroll
+          for (int o = 4; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+          const int m = m0 + j;
+          if (seg == 0 && m < mv) {
+            const long long o = static_cast<long long>(m) * p.lm.n_tiles + ntile;
+            p.lm.mx[o] = mx;
+            p.lm.se[o] = se;
+            p.lm.idx[o] = n0 + ix;
+          }
+        }
+        if (bulk_out && warp == 0) bulk_wait_read_all();  // the copies have read the tile
+      } else {
+        epi_sync();  // the tile is complete
+        if (p.epi.kind == EPI_NONE) {
+          const int t = threadIdx.x;
+          for (int j = 0; j < BN && m0 + j < mv; ++j)
+            if (n0 + t < p.N) p.out[static_cast<long long>(m0 + j) * p.ldo + n0 + t] = tile[j * 128 + t];
+        } else if ((p.epi.kind == EPI_STORE || p.epi.kind == EPI_RESIDUAL) && p.N % 4 == 0) {
+          epilogue_rows_vec(p.epi, tile, m0, min(BN, mv - m0), n0, p.epi.ss_in != nullptr ? s_rs : nullptr);
+        } else {
+          EpiPre pre;
+          epilogue_preload<__nv_bfloat16>(p.epi, m0, BN, n0, s_ri, pre);
+          apply_epilogue<__nv_bfloat16, __half>(p.epi, tile, m0, BN, n0, p.epi.ss_in != nullptr ? s_rs : nullptr,
+                                                s_ri, red, &pre);
+        }
+      }
+      epi_sync();  // the tile, the row facts and the scratch are free again
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int BN, bool LM>
+cudaError_t launch_pers(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& tw, const CUtensorMap& tx,
+                        const CUtensorMap& txlo, cudaStream_t s) {
+  using C = PersCfg<BN, LM>;
+  static FuncAttr smem_attr;
+  cudaError_t ae = smem_attr.ensure(C::SMEM, [](int v) {
+    return cudaFuncSetAttribute(k_gemm_pers<BN, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  });
+  if (ae != cudaSuccess) return ae;
+  PersParams p{};
+  p.M = g.M;
+  p.N = g.N;
+  p.n_kb = gemm_kb(g.K);
+  p.n_tiles = (g.N + kTileN - 1) / kTileN;
+  p.m_tiles = (g.M + BN - 1) / BN;
+  p.out = g.out;
+  p.ldo = g.ldo;
+  p.m_valid = g.m_valid;
+  p.status = c->status;
+  p.epi = g.epi;
+  p.lm = g.lm;
+  p.logits = g.logits;
+  p.ld_logits = g.ld_logits;
+  p.skip_rows = g.skip_rows;
+  p.logits_rows = g.logits_rows;
+  p.logits_bulk = g.logits != nullptr && (reinterpret_cast<uintptr_t>(g.logits) & 15) == 0 && g.ld_logits % 4 == 0;
+  const int work = p.n_tiles * p.m_tiles;
+  const int grid = std::max(1, std::min(work, c->num_sms));
+  return launch_k(k_gemm_pers<BN, LM>, dim3(grid), dim3(C::THREADS), C::SMEM, s, dim3(1), c->pdl, tw, tx, txlo, p);
+}
+
+}  // namespace dflash

@@ -112,7 +112,7 @@ struct dflash_graph {
 struct dflash_ctx {
   dflash_config cfg;
   int elem;  // bytes per element of the config dtype
-  int num_sms;
+  int num_sms = 0;  // 0: unknown (the persistent projection kernel is not used)
   // weights
   const void *w_fc, *g_fc, *embed, *g_final, *w_lm, *w_kv_inj;
   const float* key_offset;
@@ -218,6 +218,9 @@ cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
 int gemm_kb(int K);
 int gemm_bn(int M, bool split, bool w8 = false);
+// tile width (activation rows) of the persistent projection kernel for an
+// M x N projection with hi + lo activations, 0 where it does not apply
+int pers_bn(int M, int N, int num_sms);
 int gemm_kb_per_split(int n_kb, int splits, bool w8);
 int gemm_normalize_splits(int n_kb, int splits, bool w8);
 int gemm_blocks_per_sm(int bn, bool split, bool w8);

@@ -45,6 +45,7 @@ cudaError_t launch_accept_greedy(int B, int K, const int32_t* d, const int32_t* 
                                  int32_t* n_emit, bool pdl, cudaStream_t s);
 cudaError_t launch_accept_stochastic(int B, int K, int V, const int32_t* d, const float* z, const float* q,
                                      float temperature, uint64_t seed, uint64_t round, int* round_ctr,
-                                     int32_t* tau, int32_t* emitted, int32_t* n_emit, bool pdl, cudaStream_t s);
+                                     int32_t* tau, int32_t* emitted, int32_t* n_emit, int num_sms, bool pdl,
+                                     cudaStream_t s);
 
 }  // namespace dflash

@@ -30,7 +30,9 @@ Readings taken where the pages are silent (each repeated at its function):
       embedded, take the other K/2 tokens from pass 2
   R10 greedy target y has K+1 entries so that tau = K emits the bonus y_K
   R11 stochastic accept with argmax drafts uses the point-mass q = delta(d_i)
-  R12 randomness: Philox4x32-10, key = seed, counter = (v, i | stream<<16, b, round)
+  R12 randomness: Philox4x32-10, key = seed, counter = (v >> 2, i | stream<<16,
+      b, round), the uniform of index v taken from output word v & 3 (four
+      consecutive indices share one counter)
   R13 residual / bonus sampling by an exponential race, ties to lowest v
   R14 page allocation: FIFO free list, sequences served in index order
   R15 optional shared pre-RoPE key offset on the injected keys (workload knob)
@@ -483,14 +485,17 @@ STREAM_ACCEPT, STREAM_RACE = 0, 1
 
 
 def rng_uniform(seed: int, rnd: int, b, i, stream: int, v) -> np.ndarray:
-    """The uniform of R12: Philox4x32-10 word 0 at key (seed lo, seed hi) and
-    counter (v, i | stream << 16, b, round lo), broadcast over b, i, v."""
+    """The uniform of R12: Philox4x32-10 at key (seed lo, seed hi) and
+    counter (v >> 2, i | stream << 16, b, round lo), output word v & 3,
+    broadcast over b, i, v."""
     b, i, v = np.broadcast_arrays(np.asarray(b, np.uint64), np.asarray(i, np.uint64),
                                   np.asarray(v, np.uint64))
-    ctr = np.stack([v, i | np.uint64(stream << 16), b,
+    ctr = np.stack([v >> np.uint64(2), i | np.uint64(stream << 16), b,
                     np.full(b.shape, rnd & _M32, np.uint64)], axis=-1)
     key = np.broadcast_to(np.array([seed & _M32, (seed >> 32) & _M32], np.uint64), ctr.shape[:-1] + (2,))
-    return uniform_from_u32(philox4x32_10(ctr, key)[..., 0])
+    words = philox4x32_10(ctr, key)
+    word = np.take_along_axis(words, (v & np.uint64(3)).astype(np.int64)[..., None], axis=-1)[..., 0]
+    return uniform_from_u32(word)
 
 
 def race_sample(r: np.ndarray, seed: int, rnd: int, b: int, i: int) -> int:

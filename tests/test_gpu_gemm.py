@@ -42,9 +42,16 @@ def test_gemm_bf16_matches_fp64(M, N, K, splits):
 
 
 @pytest.mark.parametrize("M,N,K,splits", [(16, 256, 512, 2), (17, 300, 1000, 1), (100, 384, 264, 3), (128, 128, 64, 1),
-                                          (200, 640, 4096, 1)])
+                                          (200, 640, 4096, 1),
+                                          # many rows: the persistent kernel, 128-row activation tiles
+                                          (2048, 5760, 2880, 1),
+                                          # persistent, ragged rows, columns and depth
+                                          (1000, 20000, 1000, 1), (512, 4000, 520, 1)])
 def test_gemm_bf16_hi_lo_pair(M, N, K, splits):
-    """Activations as an exact hi + lo pair: the product keeps ~16 bits of x."""
+    """Activations as an exact hi + lo pair: the product keeps ~16 bits of x.
+    From 256 rows with at least a full wave of output tiles the projection
+    runs on the persistent kernel (one CTA an SM over many tiles, two TMEM
+    accumulators); the same check holds there."""
     import torch
     from block_diffusion_speculative_hidden_gb300 import gemm_bf16
     rng = np.random.default_rng(M + 3 * N + K)

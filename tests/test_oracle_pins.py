@@ -438,6 +438,22 @@ def test_philox_known_answer_vectors():
         assert out.tolist() == w[6:10]
 
 
+def test_uniforms_take_the_four_words_of_one_philox_block():
+    """R12's index mapping: the uniforms of v = 4g .. 4g + 3 (seed, round, b,
+    i, stream) are the four output words of the Philox block at counter
+    (g, i | stream << 16, b, round), key (seed lo, seed hi): checked on the
+    published known-answer vectors."""
+    for line in open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        w = [int(t, 16) for t in line.split()]
+        c0, c1, c2, c3, k0, k1 = w[:6]
+        seed = k0 | (k1 << 32)
+        v = 4 * c0 + np.arange(4, dtype=np.uint64)
+        u = O.rng_uniform(seed, c3, c2, c1 & 0xFFFF, c1 >> 16, v)
+        np.testing.assert_array_equal(u, O.uniform_from_u32(np.array(w[6:10], np.uint64)))
+
+
 def test_uniform_is_open_interval_and_fp32_exact():
     x = np.array([0, 1, 511, 512, 0xFFFFFFFF], np.uint64)
     u = O.uniform_from_u32(x)
