@@ -171,6 +171,14 @@ __device__ __forceinline__ void tc_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[1
       : "memory");
 }
 
+// 2^x for the softmax: one ex2.approx (results below 2^-126 flush to zero;
+// P is stored in fp16, where they are zero anyway)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -445,22 +453,34 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
           if (pg_lo + j < pg_hi)
             tc_ld_16x256b_x2(tmem + lanes_of(sb) + C::s_col(blk % C::NSB) + (pg_lo + j) * 16, sv[sb][j]);
       tc_wait_ld();
-      // pass 1: row max over the valid keys
+      // pass 1: row max over the valid keys (a full page needs no mask:
+      // only the sequence's last context page is partial)
 #pragma unroll
       for (int j = 0; j < HP; ++j) {
         const int pg = pg_lo + j;
         if (pg >= pg_hi) break;
         const int vp = vp0 + pg;
         const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
+        if (nvalid == kPage) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // keys 2c4, 2c4+1, 8+2c4, 9+2c4
-          const int key = (q >> 1) * 8 + 2 * c4 + (q & 1);
-          if (key < nvalid)
+          for (int sb = 0; sb < C::SUB; ++sb) {
+            const uint32_t* w = sv[sb][j];
+            mx[2 * sb] = fmaxf(mx[2 * sb], fmaxf(fmaxf(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                                 fmaxf(__uint_as_float(w[4]), __uint_as_float(w[5]))));
+            mx[2 * sb + 1] = fmaxf(mx[2 * sb + 1], fmaxf(fmaxf(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                                         fmaxf(__uint_as_float(w[6]), __uint_as_float(w[7]))));
+          }
+        } else {
 #pragma unroll
-            for (int sb = 0; sb < C::SUB; ++sb) {
-              mx[2 * sb] = fmaxf(mx[2 * sb], __uint_as_float(sv[sb][j][(q >> 1) * 4 + (q & 1)]));
-              mx[2 * sb + 1] = fmaxf(mx[2 * sb + 1], __uint_as_float(sv[sb][j][(q >> 1) * 4 + 2 + (q & 1)]));
-            }
+          for (int q = 0; q < 4; ++q) {  // keys 2c4, 2c4+1, 8+2c4, 9+2c4
+            const int key = (q >> 1) * 8 + 2 * c4 + (q & 1);
+            if (key < nvalid)
+#pragma unroll
+              for (int sb = 0; sb < C::SUB; ++sb) {
+                mx[2 * sb] = fmaxf(mx[2 * sb], __uint_as_float(sv[sb][j][(q >> 1) * 4 + (q & 1)]));
+                mx[2 * sb + 1] = fmaxf(mx[2 * sb + 1], __uint_as_float(sv[sb][j][(q >> 1) * 4 + 2 + (q & 1)]));
+              }
+          }
         }
       }
 #pragma unroll
@@ -473,7 +493,7 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         m_new[i] = fmaxf(m_run[i], mx[i] * p.scale_log2);
-        alpha[i] = m_run[i] == -INFINITY ? 0.f : exp2f(m_run[i] - m_new[i]);
+        alpha[i] = m_run[i] == -INFINITY ? 0.f : ex2_ftz(m_run[i] - m_new[i]);
         m_run[i] = m_new[i];
         lsum[i] = 0.f;
       }
@@ -487,24 +507,27 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
         uint8_t* pch = pbase + (pg >> 2) * C::P_CH;
         const int u0 = 2 * (pg & 3);
+        const bool full = nvalid == kPage;
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
           const int sb = i >> 1, h = i & 1;
+          const float mneg = -m_new[i];
           float e[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int key = (q >> 1) * 8 + 2 * c4 + (q & 1);
-            e[q] = key < nvalid ? exp2f(__uint_as_float(sv[sb][j][(q >> 1) * 4 + 2 * h + (q & 1)]) * p.scale_log2 -
-                                        m_new[i])
-                                : 0.f;
+            const float x = ex2_ftz(fmaf(__uint_as_float(sv[sb][j][(q >> 1) * 4 + 2 * h + (q & 1)]), p.scale_log2, mneg));
+            e[q] = full || key < nvalid ? x : 0.f;
           }
           lsum[i] += (e[0] + e[1]) + (e[2] + e[3]);
           const int r = row_of(i);
           if (r < R) {
             // keys 2*c4, 2*c4+1 of the page's first / second 8-key unit
+            // (16-byte units u0 and u0 + 1 of the 128-byte row, swizzled)
             uint8_t* prow = pch + r * 128 + 4 * c4;
-            *reinterpret_cast<uint32_t*>(prow + ((u0 ^ (r & 7)) << 4)) = pack_half2(e[0], e[1]);
-            *reinterpret_cast<uint32_t*>(prow + (((u0 + 1) ^ (r & 7)) << 4)) = pack_half2(e[2], e[3]);
+            const int sw = (u0 ^ (r & 7)) << 4;
+            *reinterpret_cast<uint32_t*>(prow + sw) = pack_half2(e[0], e[1]);
+            *reinterpret_cast<uint32_t*>(prow + (sw ^ 16)) = pack_half2(e[2], e[3]);
           }
         }
       }
