@@ -133,6 +133,79 @@ __device__ __forceinline__ void epilogue_rows_vec(const EpiArgs& e, const float*
   }
 }
 
+// QKV epilogue of one tile, row-major like epilogue_rows_vec: lane l takes
+// columns n0 + 4l .. n0 + 4l + 3, which lie in one head (4 divides dh) and
+// are all q, all k or all v.  q and k are rotated (rotate-half RoPE at the
+// row's position: the partner columns i +- dh/2 and the cos / sin of the
+// four frequencies come as 128-bit loads), then q goes to the query buffer
+// and k, v to the sequence's block page, four fp16 values a store.  The same
+// function as apply_epilogue's QKV branch (e.N and dh multiples of 4).
+__device__ __forceinline__ void epilogue_qkv_vec(const EpiArgs& e, const float* tile, int m0, int rows, int n0,
+                                                 const float* rs, const int4* ri) {
+  constexpr int B = 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = 4 * lane, n = n0 + t;
+  if (n >= e.N) return;  // per lane; no collective operations below
+  const int qd = e.Hq * e.dh, kvd = e.Hkv * e.dh, half = e.dh / 2;
+  const int kind = n < qd ? 0 : n < qd + kvd ? 1 : 2;
+  const int w = kind == 0 ? n : kind == 1 ? n - qd : n - qd - kvd;
+  const int head = w / e.dh, i = w % e.dh;
+  const int jr = i < half ? i : i - half;  // first of the four RoPE frequencies
+  const int base = t - i;                  // tile column of the head's element 0
+  __half* q = static_cast<__half*>(e.q);
+  __half* pk = static_cast<__half*>(e.pool_k);
+  __half* pv = static_cast<__half*>(e.pool_v);
+  for (int j0 = warp; j0 < rows; j0 += 4 * B) {
+    float4 cs[B], sn[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int j = j0 + 4 * u;
+      cs[u] = sn[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kind != 2 && j < rows) {
+        const long long o = static_cast<long long>(ri[j].x) * half + jr;
+        cs[u] = *reinterpret_cast<const float4*>(e.rope_cos + o);
+        sn[u] = *reinterpret_cast<const float4*>(e.rope_sin + o);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int j = j0 + 4 * u;
+      if (j >= rows) break;
+      const float* row = tile + j * 128;
+      const float sc = rs != nullptr ? rs[j] : 1.f;
+      float4 v;
+      if (kind == 2) {
+        v = *reinterpret_cast<const float4*>(row + t);
+        v.x *= sc;
+        v.y *= sc;
+        v.z *= sc;
+        v.w *= sc;
+      } else {
+        const float4 x1 = *reinterpret_cast<const float4*>(row + base + jr);
+        const float4 x2 = *reinterpret_cast<const float4*>(row + base + jr + half);
+        const float a1[4] = {x1.x * sc, x1.y * sc, x1.z * sc, x1.w * sc};
+        const float a2[4] = {x2.x * sc, x2.y * sc, x2.z * sc, x2.w * sc};
+        const float c[4] = {cs[u].x, cs[u].y, cs[u].z, cs[u].w};
+        const float s[4] = {sn[u].x, sn[u].y, sn[u].z, sn[u].w};
+        float r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = i < half ? a1[k] * c[k] - a2[k] * s[k] : a2[k] * c[k] + a1[k] * s[k];
+        v = make_float4(r[0], r[1], r[2], r[3]);
+      }
+      const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+      uint2 pkd;
+      pkd.x = *reinterpret_cast<const uint32_t*>(&h01);
+      pkd.y = *reinterpret_cast<const uint32_t*>(&h23);
+      if (kind == 0) {
+        *reinterpret_cast<uint2*>(q + static_cast<long long>(m0 + j) * qd + n) = pkd;
+      } else {
+        const long long idx = pool_index(ri[j].y, head, ri[j].z, i, e.Hkv, e.dh);
+        *reinterpret_cast<uint2*>((kind == 1 ? pk : pv) + idx) = pkd;
+      }
+    }
+  }
+}
+
 template <int BN, bool LMHEAD>
 __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
     k_gemm_pers(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -385,6 +458,8 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
             if (n0 + t < p.N) p.out[static_cast<long long>(m0 + j) * p.ldo + n0 + t] = tile[j * 128 + t];
         } else if ((p.epi.kind == EPI_STORE || p.epi.kind == EPI_RESIDUAL) && p.N % 4 == 0) {
           epilogue_rows_vec(p.epi, tile, m0, min(BN, mv - m0), n0, p.epi.ss_in != nullptr ? s_rs : nullptr);
+        } else if (p.epi.kind == EPI_QKV && p.N % 4 == 0 && p.epi.dh % 8 == 0) {
+          epilogue_qkv_vec(p.epi, tile, m0, min(BN, mv - m0), n0, p.epi.ss_in != nullptr ? s_rs : nullptr, s_ri);
         } else {
           EpiPre pre;
           epilogue_preload<__nv_bfloat16>(p.epi, m0, BN, n0, s_ri, pre);
