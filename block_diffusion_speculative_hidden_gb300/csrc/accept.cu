@@ -190,10 +190,15 @@ __global__ void __launch_bounds__(kAccThreads) k_accept_stochastic(int K, int V,
     if (s_dec) continue;
     // the first reject, or the bonus position: exponential race over
     // r(v) = max(0, p(v) - q(v)) (point mass: p with d zeroed), falling
-    // back to p when r has no mass
+    // back to p when r has no mass.  With the point-mass q (and at the bonus
+    // position) r is p off d, so the keys drop the common factor 1/S (an
+    // argmax does not see it), no second race over p is run (it could only
+    // differ from the first at d) and r has no mass only when no entry but d
+    // has any probability, when the fallback draws d itself.
     const float M = s_M, invS = 1.f / s_S;
     const int dv = i < K ? d[b * K + i] : -1;
     const float* qrow = q != nullptr && i < K ? q + (static_cast<long long>(b) * K + i) * V : nullptr;
+    const bool pmass = qrow == nullptr;
     float kr = -INFINITY, kp = -INFINITY, rsum = 0.f;
     int vr = 0x7fffffff, vp = 0x7fffffff;
     // two groups a step: their loads and their Philox blocks are independent
@@ -223,13 +228,17 @@ __global__ void __launch_bounds__(kAccThreads) k_accept_stochastic(int K, int V,
         for (int j = 0; j < 4; ++j) {
           const int v = 4 * gu + j;
           if (v >= V) break;
-          const float pv = expf(x[u][j] - M) * invS;
-          float r = pv;
-          if (i < K) r = qrow != nullptr ? fmaxf(0.f, pv - __ldg(qrow + v)) : (v == dv ? 0.f : pv);
-          const float e = -logf(uniform_u32(wv[j]));
-          if (r > 0.f) better(kr, vr, r / e, v);
-          if (pv > 0.f) better(kp, vp, pv / e, v);
-          rsum += r;
+          const float inv_e = __frcp_rn(-logf(uniform_u32(wv[j])));  // 1 / E_v
+          if (pmass) {
+            const float pv = expf(x[u][j] - M);  // p(v) S
+            if (pv > 0.f && v != dv) better(kr, vr, pv * inv_e, v);
+          } else {
+            const float pv = expf(x[u][j] - M) * invS;
+            const float r = fmaxf(0.f, pv - __ldg(qrow + v));
+            if (r > 0.f) better(kr, vr, r * inv_e, v);
+            if (pv > 0.f) better(kp, vp, pv * inv_e, v);
+            rsum += r;
+          }
         }
       }
     }
@@ -270,7 +279,8 @@ __global__ void __launch_bounds__(kAccThreads) k_accept_stochastic(int K, int V,
                static_cast<int>(__float_as_uint(ld_dsmem_f32(dsmem_map(smem_u32(&s_race_v[1]), r)))));
         RS += ld_dsmem_f32(dsmem_map(smem_u32(&s_race_sum), r));
       }
-      emitted[b * (K + 1) + i] = RS > 0.f ? VR : VP;
+      // point mass: r has mass iff some entry other than d won a key
+      emitted[b * (K + 1) + i] = pmass ? (KR > -INFINITY ? VR : dv) : (RS > 0.f ? VR : VP);
     }
     tau = i < K ? i : K;
     break;

@@ -234,16 +234,28 @@ bool gemm_l2_plan(dflash_ctx* c, const NextGemm& nx, L2Plan* pl, CUtensorMap* ma
   return true;
 }
 
-int pers_bn(int M, int N, int num_sms) {
+int pers_plan(int M, int N, int K, int num_sms, int split_slots) {
   // the persistent kernel serves the tensor-bound sizes (at least 256
-  // activation rows) with 128-row activation tiles, where the tiles fill the
-  // SMs in waves that are at least 75 % full on average (measured: 64-row
-  // tiles, and fewer tiles, ran slower than the split-K kernel)
+  // activation rows) with 128 x 128 tiles, one CTA a tile or a cluster pair
+  // splitting K (each half a tile's time, a small price for the exchange);
+  // it applies where its waves are at least 75 % full on average (measured:
+  // 64-row activation tiles, and fewer tiles, ran slower than the split-K
+  // kernel)
   if (M < 256 || num_sms < 1) return 0;
   const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + 127) / 128);
-  if (tiles < num_sms) return 0;
-  const long long waves = (tiles + num_sms - 1) / num_sms;
-  return 4 * tiles >= 3 * waves * num_sms ? 128 : 0;
+  const double ideal = static_cast<double>(tiles) / num_sms;  // in full-K tile times
+  const double t1 = static_cast<double>((tiles + num_sms - 1) / num_sms);
+  double best_eff = tiles >= num_sms ? ideal / t1 : 0.0;
+  int best = 1;
+  if (split_slots > 0 && gemm_kb(K) >= 2) {
+    const double t2 = 0.5 * static_cast<double>((tiles + split_slots - 1) / split_slots) * 1.05;
+    const double eff2 = ideal / t2;
+    if (eff2 > best_eff) {
+      best_eff = eff2;
+      best = 2;
+    }
+  }
+  return best_eff >= 0.75 ? best : 0;
 }
 
 int gemm_bn(int M, bool split, bool w8) {
@@ -265,16 +277,22 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s) {
     return cudaGetLastError();
   }
   const bool split = g.X_lo != nullptr, w8 = c->cfg.dtype == DFLASH_BF16_W8;
-  const int pbn = (!w8 && split && (g.splits == 1 || g.epi.kind != EPI_NONE)) ? pers_bn(g.M, g.N, c->num_sms) : 0;
-  if (pbn > 0) {
-    // many activation rows: the persistent kernel (every tile owns its whole
-    // reduction, so the caller's split count does not apply)
+  const bool lm = g.lm.mx != nullptr;
+  int plan = 0;
+  if (!w8 && split && (g.splits == 1 || g.epi.kind != EPI_NONE) && g.M >= 256 && c->num_sms > 0) {
+    if (!lm && c->pers_split_clusters < 0) c->pers_split_clusters = pers_split_clusters(PersCfg<128, false>::SMEM);
+    plan = pers_plan(g.M, g.N, g.K, c->num_sms, lm ? 0 : std::max(0, c->pers_split_clusters));
+  }
+  if (plan > 0) {
+    // many activation rows: the persistent kernel (a tile's reduction stays
+    // within its CTA or CTA pair, so the caller's split count does not apply)
     CUtensorMap tw, tx, txlo;
-    if (!get_tmap(c, g.W, g.N, g.K, kTileN, &tw) || !get_tmap(c, g.X, g.M_alloc, g.K, pbn, &tx) ||
-        !get_tmap(c, g.X_lo, g.M_alloc, g.K, pbn, &txlo))
+    if (!get_tmap(c, g.W, g.N, g.K, kTileN, &tw) || !get_tmap(c, g.X, g.M_alloc, g.K, 128, &tx) ||
+        !get_tmap(c, g.X_lo, g.M_alloc, g.K, 128, &txlo))
       return cudaErrorInvalidValue;
-    const bool lm = g.lm.mx != nullptr;
-    return lm ? launch_pers<128, true>(c, g, tw, tx, txlo, s) : launch_pers<128, false>(c, g, tw, tx, txlo, s);
+    if (lm) return launch_pers<128, true, 1>(c, g, tw, tx, txlo, s);
+    return plan == 2 ? launch_pers<128, false, 2>(c, g, tw, tx, txlo, s)
+                     : launch_pers<128, false, 1>(c, g, tw, tx, txlo, s);
   }
   const int bn = gemm_bn(g.M, split, w8);
   CUtensorMap tw, tx, txlo;

@@ -206,11 +206,20 @@ __device__ __forceinline__ void epilogue_qkv_vec(const EpiArgs& e, const float* 
   }
 }
 
-template <int BN, bool LMHEAD>
+// KSPLIT = 2: the two CTAs of a cluster share each tile, CTA r multiplying
+// the k-blocks of half r (rank 0 takes the larger half).  Both read their
+// accumulator out into their own tile, then CTA r sums rows 64 r .. 64 r + 63
+// of its tile and of its peer's (distributed shared memory, rank 0's term
+// first) and finishes those 64 rows.  The pair meets through mbarriers
+// rather than cluster barriers, so the TMA and MMA threads never stop:
+// `ready` (the peer's tile is complete), `cons` (the peer has read this
+// CTA's tile, which may then take the next one).
+template <int BN, bool LMHEAD, int KSPLIT>
 __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
     k_gemm_pers(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ CUtensorMap tmXlo, const __grid_constant__ PersParams p) {
   using C = PersCfg<BN, LMHEAD>;
+  static_assert(KSPLIT == 1 || (KSPLIT == 2 && !LMHEAD && BN == 128), "split tiles: 128-row projections");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;                                         // [STAGES][W | X hi | X lo]
@@ -220,25 +229,34 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
   uint64_t* empty = full + C::STAGES;                           // [STAGES] stage consumed by the MMAs
   uint64_t* accf = empty + C::STAGES;                           // [2] accumulator complete
   uint64_t* acce = accf + 2;                                    // [2] accumulator read out
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  uint64_t* ready = acce + 2;                                   // KSPLIT 2: the peer's tile is complete
+  uint64_t* cons = ready + 1;                                   // KSPLIT 2: the peer has read this tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cons + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  static_assert((2 * C::STAGES + 4) * 8 + 8 <= 256, "barrier area");
+  static_assert((2 * C::STAGES + 6) * 8 + 8 <= 256, "barrier area");
   float* red = reinterpret_cast<float*>(aux + 256);             // [BN][4]
   float* s_rs = red + 4 * BN;                                   // folded-RMSNorm row scales
   int4* s_ri = reinterpret_cast<int4*>(s_rs + BN);              // per-row epilogue facts
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = KSPLIT == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit = static_cast<int>(blockIdx.x) / KSPLIT, n_units = static_cast<int>(gridDim.x) / KSPLIT;
+  // this CTA's k-blocks of every tile
+  const int kb_half = (p.n_kb + 1) / 2;
+  const int kb0 = KSPLIT == 2 && rank == 1 ? kb_half : 0;
+  const int kb1 = KSPLIT == 2 && rank == 0 ? kb_half : p.n_kb;
+  const int nkb = kb1 - kb0;
+  // the rows this CTA finishes: all of a tile, or its half
+  constexpr int ROWS = BN / KSPLIT;
+  const int r0 = rank * ROWS;
   // m_valid is written two kernels upstream (page allocation), never by the
   // predecessor, so every role may size the work list before pdl_wait
   const int mv = p.m_valid != nullptr ? min(p.M, __ldg(p.m_valid)) : p.M;
   const int m_tiles = min(p.m_tiles, (mv + BN - 1) / BN);
   const int n_work = p.n_tiles * m_tiles;
-  const int my_tiles = static_cast<int>(blockIdx.x) < n_work
-                           ? (n_work - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                                 static_cast<int>(gridDim.x)
-                           : 0;
+  const int my_tiles = unit < n_work ? (n_work - unit + n_units - 1) / n_units : 0;
   auto tile_of = [&](int tl, int& n0, int& m0) {
-    const int t = static_cast<int>(blockIdx.x) + tl * static_cast<int>(gridDim.x);
+    const int t = unit + tl * n_units;
     n0 = (t / m_tiles) * kTileN;
     m0 = (t % m_tiles) * BN;
   };
@@ -255,6 +273,8 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
       mbar_init(&accf[a], 1);
       mbar_init(&acce[a], 4);  // one arrival per epilogue warp
     }
+    mbar_init(ready, 1);
+    mbar_init(cons, 1);
     *s_abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -265,15 +285,20 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (KSPLIT == 2) {
+    // the peer's barriers are initialised before anything arrives on them
+    cluster_arrive();
+    cluster_wait();
+  }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == C::PRODUCER) {
     if (lane == 0) {
-      const int total = my_tiles * p.n_kb;
+      const int total = my_tiles * nkb;
       auto coords = [&](int it, int& n0, int& m0, int& kx) {
-        tile_of(it / p.n_kb, n0, m0);
-        kx = (it % p.n_kb) * kTileK;
+        tile_of(it / nkb, n0, m0);
+        kx = (kb0 + it % nkb) * kTileK;
       };
       // the weights do not depend on the predecessor: the first stages'
       // weight tiles go out before its completion, their activations after
@@ -328,7 +353,7 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
         }
         tc_fence_after();
         const uint32_t acc = tmem + static_cast<uint32_t>(a * C::ACC_COLS);
-        for (int kb = 0; kb < p.n_kb; ++kb, ++it) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::STAGES;
           if (*s_abort || !mbar_wait(&full[s], (it / C::STAGES) & 1, p.status)) {
             ok = false;
@@ -358,8 +383,9 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
       tile_of(tl, n0, m0);
       const int n = n0 + warp * 32 + lane;
       const bool nv = n < p.N;
-      for (int j = threadIdx.x; j < BN; j += kEpiThreads) {
-        const int m = m0 + j;
+      // row facts of the rows this CTA finishes (s_rs / s_ri index j of row r0 + j)
+      for (int j = threadIdx.x; j < ROWS; j += kEpiThreads) {
+        const int m = m0 + r0 + j;
         const bool ok = m < mv;
         if (p.epi.ss_in != nullptr) s_rs[j] = ok ? norm_row_scale(p.epi, m) : 0.f;
         if constexpr (LMHEAD) {
@@ -371,6 +397,10 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
       }
       const int a = tl & 1;
       live = live && !*s_abort && mbar_wait(&accf[a], (tl >> 1) & 1, p.status);
+      if constexpr (KSPLIT == 2) {
+        // the peer has read this CTA's previous tile
+        if (tl >= 1) live = live && !*s_abort && mbar_wait_cluster(cons, (tl - 1) & 1, p.status);
+      }
       if (!live) *s_abort = 1;
       __syncwarp();
       tc_fence_after();
@@ -383,16 +413,45 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
           tc_ld_32x32b_x16(tacc + c, v);
           tc_ld_32x32b_x16(tacc + BN + c, v2);
         }
+        const int cr = c - r0;  // LM head: the tile's rows are this CTA's (KSPLIT 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           float z = live ? v[j] + v2[j] : 0.f;
-          if constexpr (LMHEAD) z = nv ? (p.epi.ss_in != nullptr ? z * s_rs[c + j] : z) : -INFINITY;
+          if constexpr (LMHEAD) z = nv ? (p.epi.ss_in != nullptr ? z * s_rs[cr + j] : z) : -INFINITY;
           tile[(c + j) * C::LD + warp * 32 + lane] = z;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbarrier_arrive_one(&acce[a]);  // accumulator a may take the tile after next
+      float* mine = tile + r0 * C::LD;                 // the rows this CTA finishes
+      if constexpr (KSPLIT == 2) {
+        // both halves of the sum: the peer's tile complete, add its rows
+        // r0 .. r0 + 63 to ours (rank 0's term first), then let it reuse
+        // its tile
+        epi_sync();
+        if (threadIdx.x == 0) {
+          fence_acq_rel_cluster();
+          mbar_remote_arrive(ready, static_cast<uint32_t>(rank ^ 1));
+        }
+        live = live && !*s_abort && mbar_wait_cluster(ready, tl & 1, p.status);
+        if (!live) *s_abort = 1;
+        const uint32_t peer = dsmem_map(smem_u32(mine), static_cast<uint32_t>(rank ^ 1));
+        for (int e = threadIdx.x; e < ROWS * 32; e += kEpiThreads) {
+          const int j = e >> 5, c4 = (e & 31) * 4;
+          float4 own = *reinterpret_cast<const float4*>(mine + j * 128 + c4);
+          const float4 oth = live ? ld_dsmem_f4(peer + static_cast<uint32_t>((j * 128 + c4) * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 sum = rank == 0 ? make_float4(own.x + oth.x, own.y + oth.y, own.z + oth.z, own.w + oth.w)
+                                 : make_float4(oth.x + own.x, oth.y + own.y, oth.z + own.z, oth.w + own.w);
+          *reinterpret_cast<float4*>(mine + j * 128 + c4) = sum;
+        }
+        epi_sync();
+        if (threadIdx.x == 0) {
+          fence_acq_rel_cluster();
+          mbar_remote_arrive(cons, static_cast<uint32_t>(rank ^ 1));
+        }
+      }
+      const int rows = min(ROWS, mv - (m0 + r0));
       if constexpr (LMHEAD) {
         const bool bulk_out = p.logits != nullptr && p.logits_bulk && n0 + kTileN <= p.N;
         if (!bulk_out && p.logits != nullptr && nv)
@@ -451,23 +510,29 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
         }
         if (bulk_out && warp == 0) bulk_wait_read_all();  // the copies have read the tile
       } else {
-        epi_sync();  // the tile is complete
-        if (p.epi.kind == EPI_NONE) {
-          const int t = threadIdx.x;
-          for (int j = 0; j < BN && m0 + j < mv; ++j)
-            if (n0 + t < p.N) p.out[static_cast<long long>(m0 + j) * p.ldo + n0 + t] = tile[j * 128 + t];
-        } else if ((p.epi.kind == EPI_STORE || p.epi.kind == EPI_RESIDUAL) && p.N % 4 == 0) {
-          epilogue_rows_vec(p.epi, tile, m0, min(BN, mv - m0), n0, p.epi.ss_in != nullptr ? s_rs : nullptr);
-        } else if (p.epi.kind == EPI_QKV && p.N % 4 == 0 && p.epi.dh % 8 == 0) {
-          epilogue_qkv_vec(p.epi, tile, m0, min(BN, mv - m0), n0, p.epi.ss_in != nullptr ? s_rs : nullptr, s_ri);
-        } else {
-          EpiPre pre;
-          epilogue_preload<__nv_bfloat16>(p.epi, m0, BN, n0, s_ri, pre);
-          apply_epilogue<__nv_bfloat16, __half>(p.epi, tile, m0, BN, n0, p.epi.ss_in != nullptr ? s_rs : nullptr,
-                                                s_ri, red, &pre);
+        epi_sync();  // the rows are complete
+        const float* rs = p.epi.ss_in != nullptr ? s_rs : nullptr;
+        if (rows > 0) {
+          if (p.epi.kind == EPI_NONE) {
+            const int t = threadIdx.x;
+            for (int j = 0; j < rows; ++j)
+              if (n0 + t < p.N) p.out[static_cast<long long>(m0 + r0 + j) * p.ldo + n0 + t] = mine[j * 128 + t];
+          } else if ((p.epi.kind == EPI_STORE || p.epi.kind == EPI_RESIDUAL) && p.N % 4 == 0) {
+            epilogue_rows_vec(p.epi, mine, m0 + r0, rows, n0, rs);
+          } else if (p.epi.kind == EPI_QKV && p.N % 4 == 0 && p.epi.dh % 8 == 0) {
+            epilogue_qkv_vec(p.epi, mine, m0 + r0, rows, n0, rs, s_ri);
+          } else {
+            EpiPre pre;
+            epilogue_preload<__nv_bfloat16>(p.epi, m0 + r0, ROWS, n0, s_ri, pre);
+            apply_epilogue<__nv_bfloat16, __half>(p.epi, mine, m0 + r0, ROWS, n0, rs, s_ri, red, &pre);
+          }
         }
       }
       epi_sync();  // the tile, the row facts and the scratch are free again
+    }
+    if constexpr (KSPLIT == 2) {
+      // the peer has read the last tile before this CTA's shared memory goes
+      if (my_tiles > 0 && live && !*s_abort) mbar_wait_cluster(cons, (my_tiles - 1) & 1, p.status);
     }
   }
   tc_fence_before();
@@ -478,13 +543,40 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
   }
 }
 
-template <int BN, bool LM>
+// Cluster pairs of k_gemm_pers<128, false, 2> that fit at once (0 if the
+// query fails).
+inline int pers_split_clusters(int smem) {
+  static FuncAttr smem_attr;
+  if (smem_attr.ensure(smem, [](int v) {
+        return cudaFuncSetAttribute(k_gemm_pers<128, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+      }) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(2, 1, 1);
+  lc.blockDim = dim3(PersCfg<128, false>::THREADS);
+  lc.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pers<128, false, 2>, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int BN, bool LM, int KSPLIT>
 cudaError_t launch_pers(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& tw, const CUtensorMap& tx,
                         const CUtensorMap& txlo, cudaStream_t s) {
   using C = PersCfg<BN, LM>;
   static FuncAttr smem_attr;
   cudaError_t ae = smem_attr.ensure(C::SMEM, [](int v) {
-    return cudaFuncSetAttribute(k_gemm_pers<BN, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+    return cudaFuncSetAttribute(k_gemm_pers<BN, LM, KSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
   });
   if (ae != cudaSuccess) return ae;
   PersParams p{};
@@ -505,8 +597,15 @@ cudaError_t launch_pers(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& t
   p.logits_rows = g.logits_rows;
   p.logits_bulk = g.logits != nullptr && (reinterpret_cast<uintptr_t>(g.logits) & 15) == 0 && g.ld_logits % 4 == 0;
   const int work = p.n_tiles * p.m_tiles;
-  const int grid = std::max(1, std::min(work, c->num_sms));
-  return launch_k(k_gemm_pers<BN, LM>, dim3(grid), dim3(C::THREADS), C::SMEM, s, dim3(1), c->pdl, tw, tx, txlo, p);
+  int grid;
+  if (KSPLIT == 2) {
+    const int clusters = std::max(1, std::min(work, c->pers_split_clusters));
+    grid = 2 * clusters;
+  } else {
+    grid = std::max(1, std::min(work, c->num_sms));
+  }
+  return launch_k(k_gemm_pers<BN, LM, KSPLIT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, dim3(KSPLIT), c->pdl, tw, tx,
+                  txlo, p);
 }
 
 }  // namespace dflash

@@ -113,6 +113,7 @@ struct dflash_ctx {
   dflash_config cfg;
   int elem;  // bytes per element of the config dtype
   int num_sms = 0;  // 0: unknown (the persistent projection kernel is not used)
+  int pers_split_clusters = -1;  // cluster pairs of the split persistent kernel that fit at once (-1: not asked yet)
   // weights
   const void *w_fc, *g_fc, *embed, *g_final, *w_lm, *w_kv_inj;
   const float* key_offset;
@@ -218,9 +219,10 @@ cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s);
 int gemm_kb(int K);
 int gemm_bn(int M, bool split, bool w8 = false);
-// tile width (activation rows) of the persistent projection kernel for an
-// M x N projection with hi + lo activations, 0 where it does not apply
-int pers_bn(int M, int N, int num_sms);
+// The persistent projection kernel's plan for an M x N x K projection with
+// hi + lo activations: CTAs per tile (1, or 2 splitting K), 0 where the
+// kernel does not apply.  split_slots: cluster pairs that fit at once.
+int pers_plan(int M, int N, int K, int num_sms, int split_slots);
 int gemm_kb_per_split(int n_kb, int splits, bool w8);
 int gemm_normalize_splits(int n_kb, int splits, bool w8);
 int gemm_blocks_per_sm(int bn, bool split, bool w8);
