@@ -267,6 +267,14 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
   // are two O buffers).
   constexpr int RPT = C::RPT, OG = DH / 16;  // 8-column groups per half of the head dims
   constexpr bool ONE = NST == 1;
+  // Row-wise softmax (the pipelined 128-row variant): thread `lane` of warp
+  // w owns query row 32 (w % 4) + lane (its TMEM lane) for half w / 4 of each
+  // block's pages and of O's head dims; S and O come in with 32x32b loads, so
+  // the row's max and sum stay in the thread.  o_acc then holds the row's 32
+  // head dims (index j: o_acc[j / 8][j % 8]); m_run[0] and l_run[0] its
+  // running max and sum.
+  constexpr bool ROWT = C::M == 128 && C::PIPE && DH == 64;
+  static_assert(!ROWT || (!ONE && RPT * 2 * OG == 32), "a row-wise thread keeps 32 head dims");
   const int qd = warp & 3, hf = warp >> 2;
   const bool soft = warp < 8 && qd < C::QUADS;
   float o_acc[ONE ? 1 : RPT][ONE ? 1 : 2 * OG];
@@ -393,6 +401,121 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       }
     }
     __syncwarp();
+  } else if (soft && ROWT) {
+    // ---------------- row-wise softmax (see ROWT).  The two warps of a
+    // quadrant meet at named barriers, so both always run every block.
+    bool live = true;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+    const int r = 32 * qd + lane;
+    float m_r = -INFINITY, l_r = 0.f;
+    // O of block f into the registers: folded one block late, after the next
+    // block's rescale al is known, as o = (o + O_f) al; the last block adds
+    // O_f alone
+    auto fold_row = [&](int f, float al, bool last) {
+      const int ob = f % C::NO;
+      live = live && mbar_wait(&o_full[ob], (f / C::NO) & 1, p.status);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t v0[16], v1[16];
+      tc_ld_32x32b_x16_nw(tmem + lane_base + C::o_col(ob) + 32 * hf, v0);
+      tc_ld_32x32b_x16_nw(tmem + lane_base + C::o_col(ob) + 32 * hf + 16, v1);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float x = __uint_as_float(j < 16 ? v0[j] : v1[j - 16]);
+        float& o = o_acc[j >> 3][j & 7];
+        o = last ? o + x : (o + x) * al;
+      }
+      tc_fence_before();
+      mbarrier_arrive_one(&o_free[ob]);
+    };
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int npb = min(KBP, np - blk * KBP);
+      const int vp0 = vp_begin + blk * KBP;
+      const int pg_split = (npb + 1) >> 1;
+      const int pg_lo = hf == 0 ? 0 : pg_split, pg_hi = hf == 0 ? pg_split : npb;
+      constexpr int HP = (KBP + 1) / 2;
+      live = live && mbar_wait(&s_full[blk % C::NSB], (blk / C::NSB) & 1, p.status);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t sv[HP][16];
+#pragma unroll
+      for (int j = 0; j < HP; ++j)
+        if (pg_lo + j < pg_hi) tc_ld_32x32b_x16_nw(tmem + lane_base + C::s_col(blk % C::NSB) + (pg_lo + j) * 16, sv[j]);
+      tc_wait_ld();
+      // pass 1: the row's max over its valid keys (only the last context page is partial)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        const int pg = pg_lo + j;
+        if (pg >= pg_hi) break;
+        const int vp = vp0 + pg;
+        const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
+        if (nvalid == kPage) {
+          float a = fmaxf(__uint_as_float(sv[j][0]), __uint_as_float(sv[j][1]));
+          float c = fmaxf(__uint_as_float(sv[j][2]), __uint_as_float(sv[j][3]));
+#pragma unroll
+          for (int k = 4; k < 16; k += 2) {
+            a = fmaxf(a, __uint_as_float(sv[j][k]));
+            c = fmaxf(c, __uint_as_float(sv[j][k + 1]));
+          }
+          mx = fmaxf(mx, fmaxf(a, c));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (k < nvalid) mx = fmaxf(mx, __uint_as_float(sv[j][k]));
+        }
+      }
+      // the partner warp holds the row's other pages
+      s_red[(warp * 32 + lane) * RPT] = mx;
+      named_sync(1 + qd, 64);
+      mx = fmaxf(mx, s_red[(((warp + 4) & 7) * 32 + lane) * RPT]);
+      named_sync(1 + qd, 64);
+      const float m_new = fmaxf(m_r, mx * p.scale_log2);
+      const float alpha = m_r == -INFINITY ? 0.f : ex2_ftz(m_r - m_new);
+      m_r = m_new;
+      // pass 2: P = 2^(S scale - m) in fp16, a page's 16 keys as two 16-byte
+      // units of the row (128-byte swizzle: unit u of row r at u ^ (r & 7))
+      uint8_t* pbase = C::P_IN_K ? sKV + (blk % NST) * C::STAGE_BYTES : sP + C::p_off(blk);
+      float ls = 0.f;
+      const float mneg = -m_new;
+#pragma unroll
+      for (int j = 0; j < HP; ++j) {
+        const int pg = pg_lo + j;
+        if (pg >= pg_hi) break;
+        const int vp = vp0 + pg;
+        const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
+        uint32_t pk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float e0 = ex2_ftz(fmaf(__uint_as_float(sv[j][2 * k]), p.scale_log2, mneg));
+          float e1 = ex2_ftz(fmaf(__uint_as_float(sv[j][2 * k + 1]), p.scale_log2, mneg));
+          if (nvalid != kPage) {
+            e0 = 2 * k < nvalid ? e0 : 0.f;
+            e1 = 2 * k + 1 < nvalid ? e1 : 0.f;
+          }
+          ls += e0 + e1;
+          pk[k] = pack_half2(e0, e1);
+        }
+        uint8_t* prow = pbase + (pg >> 2) * C::P_CH + r * 128;
+        const int u0 = 2 * (pg & 3);
+        *reinterpret_cast<uint4*>(prow + ((u0 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+      l_r = l_r * alpha + ls;
+      fence_proxy_async_smem();  // P is read by the tensor cores
+      tc_fence_before();
+      mbarrier_arrive_one(&p_full[blk % C::NSB]);
+      if (blk > 0) fold_row(blk - 1, alpha, false);
+    }
+    if (nblk > 0) fold_row(nblk - 1, 0.f, true);
+    // the row's full sum: this half's plus the partner's
+    s_red[(warp * 32 + lane) * RPT] = l_r;
+    named_sync(1 + qd, 64);
+    l_r += s_red[(((warp + 4) & 7) * 32 + lane) * RPT];
+    named_sync(1 + qd, 64);
+    m_run[0] = m_r;
+    l_run[0] = l_r;
   } else if (soft) {
     // ---------------- softmax.  The two warps of a quadrant meet at named
     // barriers, so both always run every block: a wait that gives up only
@@ -590,7 +713,27 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     }
   };
   if (p.splits == 1) {
-    if (soft) {
+    if (soft && ROWT) {
+      // the row's 32 head dims of this half, 16-byte stores of both terms
+      const int r = 32 * qd + lane;
+      const float inv = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
+      const long long at = static_cast<long long>(b * kBlockK + (r & 15)) * q_dim + (kvh * G + (r >> 4)) * DH + 32 * hf;
+#pragma unroll
+      for (int j0 = 0; j0 < 32; j0 += 8) {
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = j0 + 2 * k;
+          const float v0 = o_acc[j >> 3][j & 7] * inv, v1 = o_acc[(j + 1) >> 3][(j + 1) & 7] * inv;
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+          const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - __low2float(h), v1 - __high2float(h));
+          hv[k] = *reinterpret_cast<const uint32_t*>(&h);
+          lv[k] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+        *reinterpret_cast<uint4*>(out.hi + at + j0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4*>(out.lo + at + j0) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      }
+    } else if (soft) {
       for_each_o([&](int i, int d, float o0, float o1) {
         const int r = row_of(i);
         if (r >= R) return;
@@ -619,7 +762,15 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     float* recv = stage + R * LD;                           // [S][rpr][LD]
     const int r0 = min(R, cr * rpr), r1 = min(R, r0 + rpr);
     __syncthreads();
-    if (soft) {
+    if (soft && ROWT) {
+      const int r = 32 * qd + lane;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(stage + r * LD + 32 * hf + j) =
+            make_float4(o_acc[j >> 3][j & 7], o_acc[(j + 1) >> 3][(j + 1) & 7], o_acc[(j + 2) >> 3][(j + 2) & 7],
+                        o_acc[(j + 3) >> 3][(j + 3) & 7]);
+      if (hf == 0) *reinterpret_cast<float2*>(stage + r * LD + DH) = make_float2(m_run[0], l_run[0]);
+    } else if (soft) {
       for_each_o([&](int i, int d, float o0, float o1) {
         const int r = row_of(i);
         if (r < R) *reinterpret_cast<float2*>(stage + r * LD + d) = make_float2(o0, o1);
