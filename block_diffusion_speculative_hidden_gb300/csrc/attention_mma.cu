@@ -420,11 +420,14 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       tc_ld_32x32b_x16_nw(tmem + lane_base + C::o_col(ob) + 32 * hf, v0);
       tc_ld_32x32b_x16_nw(tmem + lane_base + C::o_col(ob) + 32 * hf + 16, v1);
       tc_wait_ld();
+      // once the rows' maxima stop moving (al = 1 for the warp's 32 rows,
+      // exactly), the fold is an add
+      const bool add_only = last || __all_sync(0xffffffffu, al == 1.f);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float x = __uint_as_float(j < 16 ? v0[j] : v1[j - 16]);
         float& o = o_acc[j >> 3][j & 7];
-        o = last ? o + x : (o + x) * al;
+        o = add_only ? o + x : (o + x) * al;
       }
       tc_fence_before();
       mbarrier_arrive_one(&o_free[ob]);
