@@ -280,7 +280,7 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s) {
   const bool lm = g.lm.mx != nullptr;
   int plan = 0;
   if (!w8 && split && (g.splits == 1 || g.epi.kind != EPI_NONE) && g.M >= 256 && c->num_sms > 0) {
-    if (!lm && c->pers_split_clusters < 0) c->pers_split_clusters = pers_split_clusters(PersCfg<128, false>::SMEM);
+    if (!lm && c->pers_split_clusters < 0) c->pers_split_clusters = pers_split_clusters(PersCfg<128, false, 2>::SMEM);
     plan = pers_plan(g.M, g.N, g.K, c->num_sms, lm ? 0 : std::max(0, c->pers_split_clusters));
   }
   if (plan > 0) {

@@ -30,7 +30,11 @@
 
 namespace dflash {
 
-template <int BN, bool LMHEAD>
+// A CTA that owns its tile's whole reduction (KSPLIT 1) reads the
+// accumulator out 32 activation rows at a time, so its staging tile is a
+// quarter of the tile and the ring has room for a fourth stage (the loads
+// are latency-bound with three); a split pair exchanges whole tiles.
+template <int BN, bool LMHEAD, int KSPLIT = 1>
 struct PersCfg {
   static constexpr int W_BYTES = kTileN * kTileK * 2;          // 16 KB
   static constexpr int X_BOX = BN * kTileK * 2;                 // one activation term, 64 k
@@ -39,7 +43,8 @@ struct PersCfg {
   static constexpr int ACC_COLS = NMMA;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;                // two accumulators
   static constexpr int LD = LMHEAD ? kLmLd : 128;               // epilogue tile row stride (floats)
-  static constexpr int EPI_BYTES = BN * LD * 4;
+  static constexpr int CH = KSPLIT == 1 ? 32 : BN;              // activation rows a readout chunk
+  static constexpr int EPI_BYTES = CH * LD * 4;
   static constexpr int AUX_BYTES = 256 /*barriers*/ + BN * 4 * 4 /*red*/ + BN * 4 /*row scales*/ + BN * 16;
   static constexpr int SMEM_MAX = 232448;                       // 227 KB a CTA
   static constexpr int STAGES_RAW = (SMEM_MAX - 1024 - EPI_BYTES - AUX_BYTES) / STAGE_BYTES;
@@ -215,15 +220,15 @@ __device__ __forceinline__ void epilogue_qkv_vec(const EpiArgs& e, const float* 
 // `ready` (the peer's tile is complete), `cons` (the peer has read this
 // CTA's tile, which may then take the next one).
 template <int BN, bool LMHEAD, int KSPLIT>
-__global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
+__global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
     k_gemm_pers(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ CUtensorMap tmXlo, const __grid_constant__ PersParams p) {
-  using C = PersCfg<BN, LMHEAD>;
+  using C = PersCfg<BN, LMHEAD, KSPLIT>;
   static_assert(KSPLIT == 1 || (KSPLIT == 2 && !LMHEAD && BN == 128), "split tiles: 128-row projections");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;                                         // [STAGES][W | X hi | X lo]
-  float* tile = reinterpret_cast<float*>(smem + C::RING_BYTES);  // [BN][LD] epilogue tile
+  float* tile = reinterpret_cast<float*>(smem + C::RING_BYTES);  // [CH][LD] epilogue tile (a readout chunk)
   uint8_t* aux = smem + C::RING_BYTES + C::EPI_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(aux);            // [STAGES] stage landed
   uint64_t* empty = full + C::STAGES;                           // [STAGES] stage consumed by the MMAs
@@ -406,129 +411,146 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD>::THREADS, 1)
       tc_fence_after();
       epi_sync();  // the row facts are complete
       const uint32_t tacc = tquad + static_cast<uint32_t>(a * C::ACC_COLS);
+      constexpr int CH = C::CH;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        float v[16], v2[16];
-        if (live) {
-          tc_ld_32x32b_x16(tacc + c, v);
-          tc_ld_32x32b_x16(tacc + BN + c, v2);
-        }
-        const int cr = c - r0;  // LM head: the tile's rows are this CTA's (KSPLIT 1)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float z = live ? v[j] + v2[j] : 0.f;
-          if constexpr (LMHEAD) z = nv ? (p.epi.ss_in != nullptr ? z * s_rs[cr + j] : z) : -INFINITY;
-          tile[(c + j) * C::LD + warp * 32 + lane] = z;
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbarrier_arrive_one(&acce[a]);  // accumulator a may take the tile after next
-      float* mine = tile + r0 * C::LD;                 // the rows this CTA finishes
-      if constexpr (KSPLIT == 2) {
-        // both halves of the sum: the peer's tile complete, add its rows
-        // r0 .. r0 + 63 to ours (rank 0's term first), then let it reuse
-        // its tile
-        epi_sync();
-        if (threadIdx.x == 0) {
-          fence_acq_rel_cluster();
-          mbar_remote_arrive(ready, static_cast<uint32_t>(rank ^ 1));
-        }
-        live = live && !*s_abort && mbar_wait_cluster(ready, tl & 1, p.status);
-        if (!live) *s_abort = 1;
-        const uint32_t peer = dsmem_map(smem_u32(mine), static_cast<uint32_t>(rank ^ 1));
-        for (int e = threadIdx.x; e < ROWS * 32; e += kEpiThreads) {
-          const int j = e >> 5, c4 = (e & 31) * 4;
-          float4 own = *reinterpret_cast<const float4*>(mine + j * 128 + c4);
-          const float4 oth = live ? ld_dsmem_f4(peer + static_cast<uint32_t>((j * 128 + c4) * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          float4 sum = rank == 0 ? make_float4(own.x + oth.x, own.y + oth.y, own.z + oth.z, own.w + oth.w)
-                                 : make_float4(oth.x + own.x, oth.y + own.y, oth.z + own.z, oth.w + own.w);
-          *reinterpret_cast<float4*>(mine + j * 128 + c4) = sum;
-        }
-        epi_sync();
-        if (threadIdx.x == 0) {
-          fence_acq_rel_cluster();
-          mbar_remote_arrive(cons, static_cast<uint32_t>(rank ^ 1));
-        }
-      }
-      const int rows = min(ROWS, mv - (m0 + r0));
-      if constexpr (LMHEAD) {
-        const bool bulk_out = p.logits != nullptr && p.logits_bulk && n0 + kTileN <= p.N;
-        if (!bulk_out && p.logits != nullptr && nv)
-          for (int j = 0; j < BN; ++j)
-            if (s_ri[j].w != 0) __stcs(p.logits + s_ri[j].x * p.ld_logits + n, tile[j * C::LD + warp * 32 + lane]);
-        if (bulk_out) fence_proxy_async_smem();
-        epi_sync();
-        if (bulk_out && warp == 0) {
-          const uint64_t pol = l2_policy_evict_first();
-          for (int j = lane; j < BN; j += 32)
-            if (s_ri[j].w != 0)
-              bulk_store_global(p.logits + s_ri[j].x * p.ld_logits + n0, smem_u32(tile + j * C::LD), kTileN * 4, pol);
-          bulk_commit();
-        }
-        // (max, lowest argmax, sum of exp(z - max)) of each row over the
-        // tile's 128 columns: 8 threads a row, 16 rows at a time
-        const int seg = threadIdx.x & 7;
-        const int ntile = n0 / kTileN;
+      for (int c0 = 0; c0 < BN; c0 += CH) {
+        // activation rows c0 .. c0 + CH - 1 of the tile into the staging tile
 #pragma unroll 1
-        for (int rb = 0; rb < BN; rb += kEpiThreads >> 3) {
-          const int j = rb + (threadIdx.x >> 3);
-          const float* row = tile + j * C::LD;
-          float z[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) z[k] = row[seg + 8 * k];
-          float mx = z[0];
-          int ix = seg;
-#pragma unroll
-          for (int k = 1; k < 16; ++k)
-            if (z[k] > mx) {
-              mx = z[k];
-              ix = seg + 8 * k;
-            }
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) {
-            const float om = __shfl_xor_sync(0xffffffffu, mx, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
-            if (om > mx || (om == mx && oi < ix)) {
-              mx = om;
-              ix = oi;
-            }
+        for (int c = c0; c < c0 + CH; c += 16) {
+          float v[16], v2[16];
+          if (live) {
+            tc_ld_32x32b_x16(tacc + c, v);
+            tc_ld_32x32b_x16(tacc + BN + c, v2);
           }
-          float se = 0.f;
-          if (mx > -INFINITY)
 #pragma unroll
-            for (int k = 0; k < 16; ++k) se += expf(z[k] - mx);
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
-          const int m = m0 + j;
-          if (seg == 0 && m < mv) {
-            const long long o = static_cast<long long>(m) * p.lm.n_tiles + ntile;
-            p.lm.mx[o] = mx;
-            p.lm.se[o] = se;
-            p.lm.idx[o] = n0 + ix;
+          for (int j = 0; j < 16; ++j) {
+            float z = live ? v[j] + v2[j] : 0.f;
+            if constexpr (LMHEAD) z = nv ? (p.epi.ss_in != nullptr ? z * s_rs[c + j] : z) : -INFINITY;
+            tile[(c - c0 + j) * C::LD + warp * 32 + lane] = z;
           }
         }
-        if (bulk_out && warp == 0) bulk_wait_read_all();  // the copies have read the tile
-      } else {
-        epi_sync();  // the rows are complete
-        const float* rs = p.epi.ss_in != nullptr ? s_rs : nullptr;
-        if (rows > 0) {
-          if (p.epi.kind == EPI_NONE) {
-            const int t = threadIdx.x;
-            for (int j = 0; j < rows; ++j)
-              if (n0 + t < p.N) p.out[static_cast<long long>(m0 + r0 + j) * p.ldo + n0 + t] = mine[j * 128 + t];
-          } else if ((p.epi.kind == EPI_STORE || p.epi.kind == EPI_RESIDUAL) && p.N % 4 == 0) {
-            epilogue_rows_vec(p.epi, mine, m0 + r0, rows, n0, rs);
-          } else if (p.epi.kind == EPI_QKV && p.N % 4 == 0 && p.epi.dh % 8 == 0) {
-            epilogue_qkv_vec(p.epi, mine, m0 + r0, rows, n0, rs, s_ri);
-          } else {
-            EpiPre pre;
-            epilogue_preload<__nv_bfloat16>(p.epi, m0 + r0, ROWS, n0, s_ri, pre);
-            apply_epilogue<__nv_bfloat16, __half>(p.epi, mine, m0 + r0, ROWS, n0, rs, s_ri, red, &pre);
+        if (c0 + CH == BN) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbarrier_arrive_one(&acce[a]);  // accumulator a may take the tile after next
+        }
+        // the rows this CTA finishes from this chunk: a chunk of its own
+        // tile (KSPLIT 1), or its half of the pair's sum (KSPLIT 2); fr: the
+        // first one's index in the row facts
+        float* mine = tile;
+        int fr = c0;
+        if constexpr (KSPLIT == 2) {
+          // both halves of the sum: the peer's tile complete, add its rows
+          // r0 .. r0 + 63 to ours (rank 0's term first), then let it reuse
+          // its tile
+          mine = tile + r0 * C::LD;
+          fr = 0;
+          epi_sync();
+          if (threadIdx.x == 0) {
+            fence_acq_rel_cluster();
+            mbar_remote_arrive(ready, static_cast<uint32_t>(rank ^ 1));
+          }
+          live = live && !*s_abort && mbar_wait_cluster(ready, tl & 1, p.status);
+          if (!live) *s_abort = 1;
+          const uint32_t peer = dsmem_map(smem_u32(mine), static_cast<uint32_t>(rank ^ 1));
+          for (int e = threadIdx.x; e < ROWS * 32; e += kEpiThreads) {
+            const int j = e >> 5, c4 = (e & 31) * 4;
+            float4 own = *reinterpret_cast<const float4*>(mine + j * 128 + c4);
+            const float4 oth =
+                live ? ld_dsmem_f4(peer + static_cast<uint32_t>((j * 128 + c4) * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 sum = rank == 0 ? make_float4(own.x + oth.x, own.y + oth.y, own.z + oth.z, own.w + oth.w)
+                                   : make_float4(oth.x + own.x, oth.y + own.y, oth.z + own.z, oth.w + own.w);
+            *reinterpret_cast<float4*>(mine + j * 128 + c4) = sum;
+          }
+          epi_sync();
+          if (threadIdx.x == 0) {
+            fence_acq_rel_cluster();
+            mbar_remote_arrive(cons, static_cast<uint32_t>(rank ^ 1));
           }
         }
+        const int mr0 = KSPLIT == 2 ? m0 + r0 : m0 + c0;  // first output row of `mine`
+        constexpr int NR = KSPLIT == 2 ? ROWS : CH;
+        const int rows = min(NR, mv - mr0);
+        if constexpr (LMHEAD) {
+          const bool bulk_out = p.logits != nullptr && p.logits_bulk && n0 + kTileN <= p.N;
+          if (!bulk_out && p.logits != nullptr && nv)
+            for (int j = 0; j < CH; ++j)
+              if (s_ri[c0 + j].w != 0)
+                __stcs(p.logits + s_ri[c0 + j].x * p.ld_logits + n, tile[j * C::LD + warp * 32 + lane]);
+          if (bulk_out) fence_proxy_async_smem();
+          epi_sync();
+          if (bulk_out && warp == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            for (int j = lane; j < CH; j += 32)
+              if (s_ri[c0 + j].w != 0)
+                bulk_store_global(p.logits + s_ri[c0 + j].x * p.ld_logits + n0, smem_u32(tile + j * C::LD), kTileN * 4,
+                                  pol);
+            bulk_commit();
+          }
+          // (max, lowest argmax, sum of exp(z - max)) of each row over the
+          // tile's 128 columns: 8 threads a row, 16 rows at a time
+          const int seg = threadIdx.x & 7;
+          const int ntile = n0 / kTileN;
+#pragma unroll 1
+          for (int rb = 0; rb < CH; rb += kEpiThreads >> 3) {
+            const int j = rb + (threadIdx.x >> 3);
+            const float* row = tile + j * C::LD;
+            float z[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) z[k] = row[seg + 8 * k];
+            float mx = z[0];
+            int ix = seg;
+#pragma unroll
+            for (int k = 1; k < 16; ++k)
+              if (z[k] > mx) {
+                mx = z[k];
+                ix = seg + 8 * k;
+              }
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) {
+              const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+              const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+              if (om > mx || (om == mx && oi < ix)) {
+                mx = om;
+                ix = oi;
+              }
+            }
+            float se = 0.f;
+            if (mx > -INFINITY)
+#pragma unroll
+              for (int k = 0; k < 16; ++k) se += expf(z[k] - mx);
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+            const int m = mr0 + j;
+            if (seg == 0 && m < mv) {
+              const long long o = static_cast<long long>(m) * p.lm.n_tiles + ntile;
+              p.lm.mx[o] = mx;
+              p.lm.se[o] = se;
+              p.lm.idx[o] = n0 + ix;
+            }
+          }
+          if (bulk_out && warp == 0) bulk_wait_read_all();  // the copies have read the chunk
+        } else {
+          epi_sync();  // the rows are complete
+          const float* rs = p.epi.ss_in != nullptr ? s_rs + fr : nullptr;
+          if (rows > 0) {
+            if (p.epi.kind == EPI_NONE) {
+              const int t = threadIdx.x;
+              for (int j = 0; j < rows; ++j)
+                if (n0 + t < p.N) p.out[static_cast<long long>(mr0 + j) * p.ldo + n0 + t] = mine[j * 128 + t];
+            } else if ((p.epi.kind == EPI_STORE || p.epi.kind == EPI_RESIDUAL) && p.N % 4 == 0) {
+              epilogue_rows_vec(p.epi, mine, mr0, rows, n0, rs);
+            } else if (p.epi.kind == EPI_QKV && p.N % 4 == 0 && p.epi.dh % 8 == 0) {
+              epilogue_qkv_vec(p.epi, mine, mr0, rows, n0, rs, s_ri + fr);
+            } else {
+              EpiPre pre;
+              epilogue_preload<__nv_bfloat16>(p.epi, mr0, NR, n0, s_ri + fr, pre);
+              apply_epilogue<__nv_bfloat16, __half>(p.epi, mine, mr0, NR, n0, rs, s_ri + fr, red, &pre);
+            }
+          }
+        }
+        epi_sync();  // the staging tile is free again
       }
-      epi_sync();  // the tile, the row facts and the scratch are free again
     }
     if constexpr (KSPLIT == 2) {
       // the peer has read the last tile before this CTA's shared memory goes
@@ -553,7 +575,7 @@ inline int pers_split_clusters(int smem) {
     return 0;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(2, 1, 1);
-  lc.blockDim = dim3(PersCfg<128, false>::THREADS);
+  lc.blockDim = dim3(PersCfg<128, false, 2>::THREADS);
   lc.dynamicSmemBytes = smem;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -573,7 +595,7 @@ inline int pers_split_clusters(int smem) {
 template <int BN, bool LM, int KSPLIT>
 cudaError_t launch_pers(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& tw, const CUtensorMap& tx,
                         const CUtensorMap& txlo, cudaStream_t s) {
-  using C = PersCfg<BN, LM>;
+  using C = PersCfg<BN, LM, KSPLIT>;
   static FuncAttr smem_attr;
   cudaError_t ae = smem_attr.ensure(C::SMEM, [](int v) {
     return cudaFuncSetAttribute(k_gemm_pers<BN, LM, KSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
