@@ -89,7 +89,11 @@ struct MmaAttnLayout {
   // otherwise it has a buffer per O buffer (P of the next block is written
   // while the P V product of this one may still read its buffer)
   static constexpr bool P_IN_K = P_BYTES <= KV_BYTES;
-  static constexpr int NPB = P_IN_K ? 0 : NO;
+  // the pipelined 128-row variant (row-wise softmax) keeps P in TMEM instead:
+  // each page's 16 fp16 values a row over the first 8 of that page's own S
+  // columns, the P V product's A operand
+  static constexpr bool P_TMEM = M == 128 && PIPE && DH == 64;
+  static constexpr int NPB = P_IN_K || P_TMEM ? 0 : NO;
   __host__ __device__ static constexpr int p_off(int blk) { return NPB > 1 ? (blk % (NPB > 1 ? NPB : 1)) * P_BYTES : 0; }
   static constexpr int OFF_P = Q_BYTES;
   static constexpr int OFF_KV = OFF_P + NPB * P_BYTES;
@@ -101,9 +105,9 @@ struct MmaAttnLayout {
   // following buffers, never past the allocation
   static constexpr bool q_padding_inside = (NCH - 1) * Q_CH + M * 128 <= OFF_BAR + BAR_BYTES;
   static constexpr bool p_padding_inside =
-      (P_IN_K ? OFF_KV + (NST - 1) * STAGE_BYTES : OFF_P + (NPB - 1) * P_BYTES) + (P_CHUNKS - 1) * P_CH +
-          M * 128 <=
-      OFF_BAR + BAR_BYTES;
+      P_TMEM || (P_IN_K ? OFF_KV + (NST - 1) * STAGE_BYTES : OFF_P + (NPB - 1) * P_BYTES) + (P_CHUNKS - 1) * P_CH +
+                        M * 128 <=
+                    OFF_BAR + BAR_BYTES;
   // a split merge stages its rows [R][DH + 4] and receives the partials
   // [splits][rows per split][DH + 4] in Q, P and the ring: the largest split
   // count (at most kMergeMax) whose merge fits (one split needs no merge)
@@ -361,14 +365,19 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     // of O(j - 1), once the softmax has folded it), PV(j) once P(j) is
     // written.  Pipelined: tensor-pipe order S(0), S(1), PV(0), S(2), PV(1),
     // ...; S(j) reuses the buffer of S(j - 2), whose P was waited for before
-    // PV(j - 2), and PV(j) the O buffer of PV(j - 2), once the softmax has
-    // folded that.
+    // PV(j - 2) (and, P in TMEM, PV(j - 2) itself), and PV(j) the O buffer of
+    // PV(j - 2), once the softmax has folded that.
     if (lane == 0) {
       const uint32_t aq = smem_u32(sQ);
       auto issue_s = [&](int j) {
         const int s = j % NST, npb = min(KBP, np - j * KBP);
         if (!mbar_wait(&kv_full[s], (j / NST) & 1, p.status)) return false;
         if (!C::PIPE && j > 0 && !mbar_wait(&o_free[0], (j - 1) & 1, p.status)) return false;
+        // with P in TMEM, S(j) overwrites P(j - 2): MMAs into different
+        // accumulators are not ordered, so wait for the P V product of j - 2
+        // (its commit to o_full; only this thread advances that barrier)
+        if (C::P_TMEM && j >= 2 && !mbar_wait(&o_full[(j - 2) % C::NO], ((j - 2) / C::NO) & 1, p.status))
+          return false;
         tc_fence_after();
         const uint32_t ak = smem_u32(sKV + s * C::STAGE_BYTES);
         const uint32_t id_s = mma_idesc_f16_f32(C::M, 16 * npb, false);
@@ -392,9 +401,16 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         const uint32_t av = ak + C::KV_BYTES;
         const uint32_t ap = C::P_IN_K ? ak : smem_u32(sP + C::p_off(blk));
         const uint32_t id_o = mma_idesc_f16_f32(C::M, DH, true);
-        for (int k16 = 0; k16 < npb; ++k16)
-          tc_mma_bf16(tmem + C::o_col(ob), sw128_desc(ap + (k16 >> 2) * C::P_CH + (k16 & 3) * 32, 16, 1024),
-                      sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, k16 > 0 ? 1u : 0u);
+        if constexpr (C::P_TMEM) {
+          // A = P from TMEM: page k16's 16 keys in the first 8 columns of its S columns
+          for (int k16 = 0; k16 < npb; ++k16)
+            tc_mma_bf16_ts(tmem + C::o_col(ob), tmem + C::s_col(blk % C::NSB) + 16 * k16,
+                           sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, k16 > 0 ? 1u : 0u);
+        } else {
+          for (int k16 = 0; k16 < npb; ++k16)
+            tc_mma_bf16(tmem + C::o_col(ob), sw128_desc(ap + (k16 >> 2) * C::P_CH + (k16 & 3) * 32, 16, 1024),
+                        sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, k16 > 0 ? 1u : 0u);
+        }
         tc_commit(&o_full[ob]);
         tc_commit(&kv_empty[s]);
         if (!C::PIPE && blk + 1 < nblk && !issue_s(blk + 1)) break;
@@ -477,9 +493,10 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       const float m_new = fmaxf(m_r, mx * p.scale_log2);
       const float alpha = m_r == -INFINITY ? 0.f : ex2_ftz(m_r - m_new);
       m_r = m_new;
-      // pass 2: P = 2^(S scale - m) in fp16, a page's 16 keys as two 16-byte
-      // units of the row (128-byte swizzle: unit u of row r at u ^ (r & 7))
-      uint8_t* pbase = C::P_IN_K ? sKV + (blk % NST) * C::STAGE_BYTES : sP + C::p_off(blk);
+      // pass 2: P = 2^(S scale - m) in fp16 into TMEM, a page's 16 keys as
+      // 8 packed columns over the start of that page's own S columns (this
+      // thread read them above; the MMA thread issues S of block + 2 into
+      // this buffer only after the P V product that reads P)
       float ls = 0.f;
       const float mneg = -m_new;
 #pragma unroll
@@ -500,13 +517,10 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
           ls += e0 + e1;
           pk[k] = pack_half2(e0, e1);
         }
-        uint8_t* prow = pbase + (pg >> 2) * C::P_CH + r * 128;
-        const int u0 = 2 * (pg & 3);
-        *reinterpret_cast<uint4*>(prow + ((u0 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        tc_st_32x32b_x8(tmem + lane_base + C::s_col(blk % C::NSB) + 16 * pg, pk);
       }
       l_r = l_r * alpha + ls;
-      fence_proxy_async_smem();  // P is read by the tensor cores
+      tc_wait_st();  // P is in TMEM before the MMA thread hears of it
       tc_fence_before();
       mbarrier_arrive_one(&p_full[blk % C::NSB]);
       if (blk > 0) fold_row(blk - 1, alpha, false);
@@ -1013,6 +1027,9 @@ constexpr bool narrow_fits() {
 template <int DH, int G>
 constexpr int narrow_stages() {
   using L3 = MmaAttnLayout<DH, G, 4, 3>;
+  using L5 = MmaAttnLayout<DH, G, 4, 5>;
+  // with P in TMEM the shared memory of the P buffers holds two more stages
+  if constexpr (L5::P_TMEM && L5::q_padding_inside && L5::SMEM_FIXED <= 104 * 1024) return 5;
   return L3::PIPE && L3::q_padding_inside && L3::p_padding_inside && L3::SMEM_FIXED <= 104 * 1024 ? 3 : 2;
 }
 
