@@ -182,6 +182,15 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// how far (log2 units) a row's max may pass the one its P is taken against
+// before O is rescaled (row-wise variant): P stays at most 2^8 in fp16
+constexpr float kLazyRescale = 8.f;
+// the three-input maximum of sm_100 and later (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -273,10 +282,10 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
   constexpr bool ONE = NST == 1;
   // Row-wise softmax (the pipelined 128-row variant): thread `lane` of warp
   // w owns query row 32 (w % 4) + lane (its TMEM lane) for half w / 4 of each
-  // block's pages and of O's head dims; S and O come in with 32x32b loads, so
-  // the row's max and sum stay in the thread.  o_acc then holds the row's 32
-  // head dims (index j: o_acc[j / 8][j % 8]); m_run[0] and l_run[0] its
-  // running max and sum.
+  // block's pages and of O's head dims; S comes in with 32x32b loads, so
+  // the row's max and sum stay in the thread, P goes back into TMEM and O
+  // accumulates there.  o_acc then holds the row's 32 head dims (index j:
+  // o_acc[j / 8][j % 8]); m_run[0] and l_run[0] its max and sum.
   constexpr bool ROWT = C::M == 128 && C::PIPE && DH == 64;
   static_assert(!ROWT || (!ONE && RPT * 2 * OG == 32), "a row-wise thread keeps 32 head dims");
   const int qd = warp & 3, hf = warp >> 2;
@@ -366,7 +375,9 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     // written.  Pipelined: tensor-pipe order S(0), S(1), PV(0), S(2), PV(1),
     // ...; S(j) reuses the buffer of S(j - 2), whose P was waited for before
     // PV(j - 2) (and, P in TMEM, PV(j - 2) itself), and PV(j) the O buffer of
-    // PV(j - 2), once the softmax has folded that.
+    // PV(j - 2), once the softmax has folded that (P in TMEM: every PV adds
+    // into the one O in TMEM, which the softmax rescales there before it
+    // signals P).
     if (lane == 0) {
       const uint32_t aq = smem_u32(sQ);
       auto issue_s = [&](int j) {
@@ -395,17 +406,18 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         if (C::PIPE && blk + 1 < nblk && !issue_s(blk + 1)) break;
         const int s = blk % NST, npb = min(KBP, np - blk * KBP), ob = blk % C::NO;
         if (!mbar_wait(&p_full[blk % C::NSB], (blk / C::NSB) & 1, p.status)) break;
-        if (C::PIPE && blk >= 2 && !mbar_wait(&o_free[ob], ((blk - 2) / 2) & 1, p.status)) break;
+        if (C::PIPE && !C::P_TMEM && blk >= 2 && !mbar_wait(&o_free[ob], ((blk - 2) / 2) & 1, p.status)) break;
         tc_fence_after();
         const uint32_t ak = smem_u32(sKV + s * C::STAGE_BYTES);
         const uint32_t av = ak + C::KV_BYTES;
         const uint32_t ap = C::P_IN_K ? ak : smem_u32(sP + C::p_off(blk));
         const uint32_t id_o = mma_idesc_f16_f32(C::M, DH, true);
         if constexpr (C::P_TMEM) {
-          // A = P from TMEM: page k16's 16 keys in the first 8 columns of its S columns
+          // A = P from TMEM: page k16's 16 keys in the first 8 columns of its
+          // S columns; O accumulates over the blocks in one TMEM buffer
           for (int k16 = 0; k16 < npb; ++k16)
-            tc_mma_bf16_ts(tmem + C::o_col(ob), tmem + C::s_col(blk % C::NSB) + 16 * k16,
-                           sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, k16 > 0 ? 1u : 0u);
+            tc_mma_bf16_ts(tmem + C::o_col(0), tmem + C::s_col(blk % C::NSB) + 16 * k16,
+                           sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, (blk | k16) > 0 ? 1u : 0u);
         } else {
           for (int k16 = 0; k16 < npb; ++k16)
             tc_mma_bf16(tmem + C::o_col(ob), sw128_desc(ap + (k16 >> 2) * C::P_CH + (k16 & 3) * 32, 16, 1024),
@@ -422,31 +434,27 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     // quadrant meet at named barriers, so both always run every block.
     bool live = true;
     const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-    const int r = 32 * qd + lane;
+    const uint32_t o_half = tmem + lane_base + C::o_col(0) + 32 * hf;  // this warp's 32 head dims of O
     float m_r = -INFINITY, l_r = 0.f;
-    // O of block f into the registers: folded one block late, after the next
-    // block's rescale al is known, as o = (o + O_f) al; the last block adds
-    // O_f alone
-    auto fold_row = [&](int f, float al, bool last) {
-      const int ob = f % C::NO;
-      live = live && mbar_wait(&o_full[ob], (f / C::NO) & 1, p.status);
+    // O accumulates in TMEM (the P V products add up); m_r is the max P is
+    // taken against, and it moves only when the row's max passes it by more
+    // than kLazyRescale (log2 units), so P stays at most 2^kLazyRescale and
+    // O is rescaled, in TMEM, only then (once P V of the previous block is done)
+    auto rescale_o = [&](int blk, float al) {
+      live = live && mbar_wait(&o_full[(blk - 1) % C::NO], ((blk - 1) / C::NO) & 1, p.status);
       __syncwarp();
       tc_fence_after();
       uint32_t v0[16], v1[16];
-      tc_ld_32x32b_x16_nw(tmem + lane_base + C::o_col(ob) + 32 * hf, v0);
-      tc_ld_32x32b_x16_nw(tmem + lane_base + C::o_col(ob) + 32 * hf + 16, v1);
+      tc_ld_32x32b_x16_nw(o_half, v0);
+      tc_ld_32x32b_x16_nw(o_half + 16, v1);
       tc_wait_ld();
-      // once the rows' maxima stop moving (al = 1 for the warp's 32 rows,
-      // exactly), the fold is an add
-      const bool add_only = last || __all_sync(0xffffffffu, al == 1.f);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float x = __uint_as_float(j < 16 ? v0[j] : v1[j - 16]);
-        float& o = o_acc[j >> 3][j & 7];
-        o = add_only ? o + x : (o + x) * al;
+      for (int j = 0; j < 16; ++j) {
+        v0[j] = __float_as_uint(__uint_as_float(v0[j]) * al);
+        v1[j] = __float_as_uint(__uint_as_float(v1[j]) * al);
       }
-      tc_fence_before();
-      mbarrier_arrive_one(&o_free[ob]);
+      tc_st_32x32b_x16(o_half, v0);
+      tc_st_32x32b_x16(o_half + 16, v1);
     };
     for (int blk = 0; blk < nblk; ++blk) {
       const int npb = min(KBP, np - blk * KBP);
@@ -471,14 +479,15 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         const int vp = vp0 + pg;
         const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
         if (nvalid == kPage) {
-          float a = fmaxf(__uint_as_float(sv[j][0]), __uint_as_float(sv[j][1]));
-          float c = fmaxf(__uint_as_float(sv[j][2]), __uint_as_float(sv[j][3]));
+          float a = fmax3(__uint_as_float(sv[j][0]), __uint_as_float(sv[j][1]), __uint_as_float(sv[j][2]));
+          float c = fmax3(__uint_as_float(sv[j][3]), __uint_as_float(sv[j][4]), __uint_as_float(sv[j][5]));
 #pragma unroll
-          for (int k = 4; k < 16; k += 2) {
-            a = fmaxf(a, __uint_as_float(sv[j][k]));
-            c = fmaxf(c, __uint_as_float(sv[j][k + 1]));
+          for (int k = 6; k < 14; k += 4) {
+            a = fmax3(a, __uint_as_float(sv[j][k]), __uint_as_float(sv[j][k + 1]));
+            c = fmax3(c, __uint_as_float(sv[j][k + 2]), __uint_as_float(sv[j][k + 3]));
           }
-          mx = fmaxf(mx, fmaxf(a, c));
+          a = fmax3(a, __uint_as_float(sv[j][14]), __uint_as_float(sv[j][15]));
+          mx = fmax3(mx, a, c);
         } else {
 #pragma unroll
           for (int k = 0; k < 16; ++k)
@@ -490,15 +499,18 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       named_sync(1 + qd, 64);
       mx = fmaxf(mx, s_red[(((warp + 4) & 7) * 32 + lane) * RPT]);
       named_sync(1 + qd, 64);
-      const float m_new = fmaxf(m_r, mx * p.scale_log2);
-      const float alpha = m_r == -INFINITY ? 0.f : ex2_ftz(m_r - m_new);
-      m_r = m_new;
+      const float m_cand = mx * p.scale_log2;
+      const bool move = m_cand > m_r + kLazyRescale;  // (always on the first block)
+      const float alpha = !move ? 1.f : m_r == -INFINITY ? 0.f : ex2_ftz(m_r - m_cand);
+      if (move) m_r = m_cand;
+      const float m_new = m_r;
       // pass 2: P = 2^(S scale - m) in fp16 into TMEM, a page's 16 keys as
       // 8 packed columns over the start of that page's own S columns (this
       // thread read them above; the MMA thread issues S of block + 2 into
       // this buffer only after the P V product that reads P)
-      float ls = 0.f;
-      const float mneg = -m_new;
+      // (the scale and the sum as packed fp32 pairs)
+      float2 ls2 = make_float2(0.f, 0.f);
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), mneg2 = make_float2(-m_new, -m_new);
 #pragma unroll
       for (int j = 0; j < HP; ++j) {
         const int pg = pg_lo + j;
@@ -508,24 +520,39 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         uint32_t pk[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          float e0 = ex2_ftz(fmaf(__uint_as_float(sv[j][2 * k]), p.scale_log2, mneg));
-          float e1 = ex2_ftz(fmaf(__uint_as_float(sv[j][2 * k + 1]), p.scale_log2, mneg));
+          const float2 t = __ffma2_rn(make_float2(__uint_as_float(sv[j][2 * k]), __uint_as_float(sv[j][2 * k + 1])),
+                                      sc2, mneg2);
+          float e0 = ex2_ftz(t.x), e1 = ex2_ftz(t.y);
           if (nvalid != kPage) {
             e0 = 2 * k < nvalid ? e0 : 0.f;
             e1 = 2 * k + 1 < nvalid ? e1 : 0.f;
           }
-          ls += e0 + e1;
+          ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
           pk[k] = pack_half2(e0, e1);
         }
         tc_st_32x32b_x8(tmem + lane_base + C::s_col(blk % C::NSB) + 16 * pg, pk);
       }
-      l_r = l_r * alpha + ls;
-      tc_wait_st();  // P is in TMEM before the MMA thread hears of it
+      l_r = l_r * alpha + (ls2.x + ls2.y);
+      if (blk > 0 && __any_sync(0xffffffffu, move)) rescale_o(blk, alpha);
+      tc_wait_st();  // P (and a rescaled O) is in TMEM before the MMA thread hears of it
       tc_fence_before();
       mbarrier_arrive_one(&p_full[blk % C::NSB]);
-      if (blk > 0) fold_row(blk - 1, alpha, false);
     }
-    if (nblk > 0) fold_row(nblk - 1, 0.f, true);
+    if (nblk > 0) {
+      // O of every block, once the last P V product is done
+      live = live && mbar_wait(&o_full[(nblk - 1) % C::NO], ((nblk - 1) / C::NO) & 1, p.status);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t v0[16], v1[16];
+      tc_ld_32x32b_x16_nw(o_half, v0);
+      tc_ld_32x32b_x16_nw(o_half + 16, v1);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o_acc[j >> 3][j & 7] = __uint_as_float(j < 16 ? v0[j] : v1[j - 16]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o_acc[j >> 3][j & 7] = 0.f;
+    }
     // the row's full sum: this half's plus the partner's
     s_red[(warp * 32 + lane) * RPT] = l_r;
     named_sync(1 + qd, 64);

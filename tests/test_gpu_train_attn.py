@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 TOL = 3e-3
 
 
-def _setup(name, S, NB, seed):
+def _setup(name, S, NB, seed, ramp=0.0):
     import torch
     from block_diffusion_speculative_hidden_gb300 import Drafter, weights_to_device
     cfg = synth.get_config(name).replace(n_layers=2)
@@ -33,8 +33,16 @@ def _setup(name, S, NB, seed):
                  max_pages_per_seq=mpps, n_pages=S * mpps, max_rows=17, max_inject_rows=NB * 17)
     Kp, Vp = dr.pool_kv()                       # [L, pages, Hkv, 16, dh] fp16
     layer = 1
-    ctx_k = [rng.standard_normal((t, Hkv, dh)).astype(np.float16) for t in T]
+    ctx_k = [rng.standard_normal((t, Hkv, dh)) for t in T]
     ctx_v = [rng.standard_normal((t, Hkv, dh)).astype(np.float16) for t in T]
+    u = rng.standard_normal((Hkv, dh))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    if ramp > 0:
+        # keys grow along u with their position, so a query row's scores
+        # climb by 4 ramp / sqrt(dh) nats a position (with the +4 u added to q below)
+        for s in range(S):
+            ctx_k[s] += ramp * np.arange(T[s])[:, None, None] * u[None]
+    ctx_k = [k.astype(np.float16) for k in ctx_k]
     pt = np.full((NB, mpps), -1, np.int32)
     for s in range(S):
         n = -(-int(T[s]) // 16)
@@ -56,7 +64,10 @@ def _setup(name, S, NB, seed):
         ctx_len[j] = min(c, int(T[2]))
     seq[4], ctx_len[4] = 0, T[0]                 # the whole one-page context
     seq[5], ctx_len[5] = 3, T[3]                 # a whole multi-page context
-    q = (rng.standard_normal((NB, 16, Hq, dh)) * 2.0).astype(np.float16)
+    q = rng.standard_normal((NB, 16, Hq, dh)) * 2.0
+    if ramp > 0:
+        q += 4.0 * np.repeat(u, Hq // Hkv, axis=0)[None, None]
+    q = q.astype(np.float16)
     kb = rng.standard_normal((NB, 16, Hkv, dh)).astype(np.float16)
     vb = rng.standard_normal((NB, 16, Hkv, dh)).astype(np.float16)
     torch.cuda.synchronize()
@@ -70,6 +81,22 @@ def _setup(name, S, NB, seed):
 def test_block_attention_matches_oracle(name, NB):
     import torch
     dr, layer, ctx_k, ctx_v, seq, ctx_len, q, kb, vb, T = _setup(name, S=5, NB=NB, seed=31)
+    c = lambda a: torch.from_numpy(a).cuda()
+    out = dr.block_attention(layer, c(seq), c(ctx_len), c(q), c(kb), c(vb))
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    ref = O.block_attention_train(q, kb, vb, ctx_k, ctx_v, seq, ctx_len)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() < TOL, (err.max(), np.unravel_index(err.argmax(), err.shape))
+
+
+# scores that climb about 6 nats a page: the running max passes the one P is
+# taken against, by far, at most key blocks, so the O accumulator is
+# rescaled over and over (in the 128-row variant, in TMEM)
+@pytest.mark.parametrize("name", ["mini_a", "mini_b"])
+def test_block_attention_with_a_climbing_max(name):
+    import torch
+    dr, layer, ctx_k, ctx_v, seq, ctx_len, q, kb, vb, T = _setup(name, S=5, NB=80, seed=33, ramp=0.75)
     c = lambda a: torch.from_numpy(a).cuda()
     out = dr.block_attention(layer, c(seq), c(ctx_len), c(q), c(kb), c(vb))
     torch.cuda.synchronize()
