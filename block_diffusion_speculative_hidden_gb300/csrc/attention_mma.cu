@@ -73,10 +73,16 @@ struct MmaAttnLayout {
   static constexpr int SW = 16 * KBP;              // S columns of a key block
   static constexpr int TMEM_COLS = 256;
   static constexpr bool PIPE = !ONE && KBP <= 4 && 2 * SW + 2 * DH <= TMEM_COLS;
-  static constexpr int NSB = PIPE ? 2 : 1;         // S buffers
-  static constexpr int NO = PIPE ? 2 : 1;          // O buffers
+  // the pipelined 128-row variant (row-wise softmax) keeps P in TMEM: each
+  // page's 16 fp16 values a row over the first 8 of that page's own S
+  // columns, the P V product's A operand; O accumulates in one TMEM buffer,
+  // so three S buffers fit (S of the next block never waits for the P V
+  // product of the previous one)
+  static constexpr bool P_TMEM = M == 128 && PIPE && DH == 64 && 3 * SW + DH <= TMEM_COLS;
+  static constexpr int NSB = P_TMEM ? 3 : PIPE ? 2 : 1;  // S buffers
+  static constexpr int NO = PIPE ? 2 : 1;          // O buffers (P in TMEM: one, two commit barriers)
   __host__ __device__ static constexpr int s_col(int j) { return PIPE ? j * SW : 0; }
-  __host__ __device__ static constexpr int o_col(int j) { return PIPE ? 2 * SW + j * DH : 0; }
+  __host__ __device__ static constexpr int o_col(int j) { return PIPE ? NSB * SW + j * DH : 0; }
   static constexpr int Q_CH = R * 128;             // stride of the Q chunks (real rows only)
   static constexpr int Q_BYTES = NCH * Q_CH;
   static constexpr int P_CHUNKS = (KBP * 16 + 63) / 64;
@@ -89,10 +95,6 @@ struct MmaAttnLayout {
   // otherwise it has a buffer per O buffer (P of the next block is written
   // while the P V product of this one may still read its buffer)
   static constexpr bool P_IN_K = P_BYTES <= KV_BYTES;
-  // the pipelined 128-row variant (row-wise softmax) keeps P in TMEM instead:
-  // each page's 16 fp16 values a row over the first 8 of that page's own S
-  // columns, the P V product's A operand
-  static constexpr bool P_TMEM = M == 128 && PIPE && DH == 64;
   static constexpr int NPB = P_IN_K || P_TMEM ? 0 : NO;
   __host__ __device__ static constexpr int p_off(int blk) { return NPB > 1 ? (blk % (NPB > 1 ? NPB : 1)) * P_BYTES : 0; }
   static constexpr int OFF_P = Q_BYTES;
@@ -125,9 +127,11 @@ template <int DH, int G, int KBP, int NST>
 struct MmaAttnCfg : MmaAttnLayout<DH, G, KBP, NST> {
   using L = MmaAttnLayout<DH, G, KBP, NST>;
   static_assert(KBP * 16 <= 256 && DH <= 256, "one MMA's N");
-  static_assert(L::PIPE ? 2 * L::SW + 2 * DH <= L::TMEM_COLS : KBP * 16 <= L::TMEM_COLS && DH <= L::TMEM_COLS,
+  static_assert(L::P_TMEM   ? 3 * L::SW + DH <= L::TMEM_COLS
+                : L::PIPE ? 2 * L::SW + 2 * DH <= L::TMEM_COLS
+                          : KBP * 16 <= L::TMEM_COLS && DH <= L::TMEM_COLS,
                 "S and O buffers fit the allocation");
-  static_assert((2 * NST + 11) * 8 <= L::BAR_AREA, "barriers fit their area");
+  static_assert((2 * NST + 13) * 8 <= L::BAR_AREA, "barriers fit their area");
   static_assert(L::q_padding_inside, "Q padding rows stay inside");
   static_assert(L::p_padding_inside, "P padding rows stay inside");
   // the 8-page variants merge any split count
@@ -217,12 +221,12 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_empty = kv_full + NST;
   uint64_t* q_full = kv_empty + NST;
-  uint64_t* s_full = q_full + 1;  // [2]: per S buffer
-  uint64_t* p_full = q_full + 3;  // [2]: per S buffer (P of the block in it is written)
-  uint64_t* o_full = q_full + 5;  // [2]: per O buffer
-  uint64_t* o_free = q_full + 7;  // [2]: per O buffer (folded into registers)
-  uint64_t* recv_bar = q_full + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 10);
+  uint64_t* s_full = q_full + 1;  // [3]: per S buffer
+  uint64_t* p_full = q_full + 4;  // [3]: per S buffer (P of the block in it is written)
+  uint64_t* o_full = q_full + 7;  // [2]: per O buffer (P in TMEM: by the block's parity)
+  uint64_t* o_free = q_full + 9;  // [2]: per O buffer (folded into registers)
+  uint64_t* recv_bar = q_full + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 12);
   float* s_red = reinterpret_cast<float*>(smem + C::OFF_BAR + C::BAR_AREA);  // [8 warps][32 lanes][RPT] pair exchange
   int* s_pages = reinterpret_cast<int*>(smem + C::OFF_BAR + C::BAR_BYTES);
 
@@ -244,9 +248,11 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(q_full, 1);
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < 3; ++j) {
       mbar_init(&s_full[j], 1);
       mbar_init(&p_full[j], SOFT);
+    }
+    for (int j = 0; j < 2; ++j) {
       mbar_init(&o_full[j], 1);
       mbar_init(&o_free[j], SOFT);
     }
@@ -374,20 +380,22 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
     // of O(j - 1), once the softmax has folded it), PV(j) once P(j) is
     // written.  Pipelined: tensor-pipe order S(0), S(1), PV(0), S(2), PV(1),
     // ...; S(j) reuses the buffer of S(j - 2), whose P was waited for before
-    // PV(j - 2) (and, P in TMEM, PV(j - 2) itself), and PV(j) the O buffer of
-    // PV(j - 2), once the softmax has folded that (P in TMEM: every PV adds
-    // into the one O in TMEM, which the softmax rescales there before it
-    // signals P).
+    // PV(j - 2), and PV(j) the O buffer of PV(j - 2), once the softmax has
+    // folded that.  P in TMEM: S(j) reuses the buffer of S(j - 3) once PV(j - 3)
+    // is done, and every PV adds into the one O in TMEM, which the softmax
+    // rescales there (when it must) before it signals P.
     if (lane == 0) {
       const uint32_t aq = smem_u32(sQ);
       auto issue_s = [&](int j) {
         const int s = j % NST, npb = min(KBP, np - j * KBP);
         if (!mbar_wait(&kv_full[s], (j / NST) & 1, p.status)) return false;
         if (!C::PIPE && j > 0 && !mbar_wait(&o_free[0], (j - 1) & 1, p.status)) return false;
-        // with P in TMEM, S(j) overwrites P(j - 2): MMAs into different
-        // accumulators are not ordered, so wait for the P V product of j - 2
-        // (its commit to o_full; only this thread advances that barrier)
-        if (C::P_TMEM && j >= 2 && !mbar_wait(&o_full[(j - 2) % C::NO], ((j - 2) / C::NO) & 1, p.status))
+        // with P in TMEM, S(j) overwrites P(j - 3): MMAs into different
+        // accumulators are not ordered, so wait for the P V product of j - 3
+        // (its commit to o_full; only this thread advances that barrier, and
+        // PV(j - 1), the next commit there, is issued after this)
+        if (C::P_TMEM && j >= C::NSB &&
+            !mbar_wait(&o_full[(j - C::NSB) % C::NO], ((j - C::NSB) / C::NO) & 1, p.status))
           return false;
         tc_fence_after();
         const uint32_t ak = smem_u32(sKV + s * C::STAGE_BYTES);
@@ -470,70 +478,105 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       for (int j = 0; j < HP; ++j)
         if (pg_lo + j < pg_hi) tc_ld_32x32b_x16_nw(tmem + lane_base + C::s_col(blk % C::NSB) + (pg_lo + j) * 16, sv[j]);
       tc_wait_ld();
-      // pass 1: the row's max over its valid keys (only the last context page is partial)
-      float mx = -INFINITY;
+      // P = 2^(S scale - m_r) in fp16 into TMEM, a page's 16 keys as 8
+      // packed columns over the start of that page's own S columns (this
+      // thread read them above; S of this buffer is recomputed only after
+      // the P V product that reads P), the row sum as packed fp32 pairs;
+      // with_max: the valid keys' max as well (only the last context page is
+      // partial)
+      float2 ls2;
+      auto make_p = [&](bool with_max, float& mx) {
+        ls2 = make_float2(0.f, 0.f);
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), mneg2 = make_float2(-m_r, -m_r);
 #pragma unroll
-      for (int j = 0; j < HP; ++j) {
-        const int pg = pg_lo + j;
-        if (pg >= pg_hi) break;
-        const int vp = vp0 + pg;
-        const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
-        if (nvalid == kPage) {
-          float a = fmax3(__uint_as_float(sv[j][0]), __uint_as_float(sv[j][1]), __uint_as_float(sv[j][2]));
-          float c = fmax3(__uint_as_float(sv[j][3]), __uint_as_float(sv[j][4]), __uint_as_float(sv[j][5]));
+        for (int j = 0; j < HP; ++j) {
+          const int pg = pg_lo + j;
+          if (pg >= pg_hi) break;
+          const int vp = vp0 + pg;
+          const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
+          uint32_t pk[8];
+          if (nvalid == kPage) {  // (no key mask)
+            if (with_max) {
+              float a = fmax3(__uint_as_float(sv[j][0]), __uint_as_float(sv[j][1]), __uint_as_float(sv[j][2]));
+              float c = fmax3(__uint_as_float(sv[j][3]), __uint_as_float(sv[j][4]), __uint_as_float(sv[j][5]));
 #pragma unroll
-          for (int k = 6; k < 14; k += 4) {
-            a = fmax3(a, __uint_as_float(sv[j][k]), __uint_as_float(sv[j][k + 1]));
-            c = fmax3(c, __uint_as_float(sv[j][k + 2]), __uint_as_float(sv[j][k + 3]));
+              for (int k = 6; k < 14; k += 4) {
+                a = fmax3(a, __uint_as_float(sv[j][k]), __uint_as_float(sv[j][k + 1]));
+                c = fmax3(c, __uint_as_float(sv[j][k + 2]), __uint_as_float(sv[j][k + 3]));
+              }
+              a = fmax3(a, __uint_as_float(sv[j][14]), __uint_as_float(sv[j][15]));
+              mx = fmax3(mx, a, c);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float2 t = __ffma2_rn(
+                  make_float2(__uint_as_float(sv[j][2 * k]), __uint_as_float(sv[j][2 * k + 1])), sc2, mneg2);
+              const float e0 = ex2_ftz(t.x), e1 = ex2_ftz(t.y);
+              ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
+              pk[k] = pack_half2(e0, e1);
+            }
+          } else {
+            if (with_max) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                if (k < nvalid) mx = fmaxf(mx, __uint_as_float(sv[j][k]));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float2 t = __ffma2_rn(
+                  make_float2(__uint_as_float(sv[j][2 * k]), __uint_as_float(sv[j][2 * k + 1])), sc2, mneg2);
+              const float e0 = 2 * k < nvalid ? ex2_ftz(t.x) : 0.f, e1 = 2 * k + 1 < nvalid ? ex2_ftz(t.y) : 0.f;
+              ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
+              pk[k] = pack_half2(e0, e1);
+            }
           }
-          a = fmax3(a, __uint_as_float(sv[j][14]), __uint_as_float(sv[j][15]));
-          mx = fmax3(mx, a, c);
-        } else {
+          tc_st_32x32b_x8(tmem + lane_base + C::s_col(blk % C::NSB) + 16 * pg, pk);
+        }
+      };
+      // the row's max over this half's keys, then over both halves (the
+      // partner warp holds the row's other pages)
+      auto pair_max = [&](float mx) {
+        s_red[(warp * 32 + lane) * RPT] = mx;
+        named_sync(1 + qd, 64);
+        mx = fmaxf(mx, s_red[(((warp + 4) & 7) * 32 + lane) * RPT]);
+        named_sync(1 + qd, 64);
+        return mx;
+      };
+      float mx = -INFINITY, alpha;
+      bool move;
+      if (m_r == -INFINITY) {
+        // the first block (every row at once): the max first, then P
+#pragma unroll
+        for (int j = 0; j < HP; ++j) {
+          const int pg = pg_lo + j;
+          if (pg >= pg_hi) break;
+          const int vp = vp0 + pg;
+          const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             if (k < nvalid) mx = fmaxf(mx, __uint_as_float(sv[j][k]));
         }
-      }
-      // the partner warp holds the row's other pages
-      s_red[(warp * 32 + lane) * RPT] = mx;
-      named_sync(1 + qd, 64);
-      mx = fmaxf(mx, s_red[(((warp + 4) & 7) * 32 + lane) * RPT]);
-      named_sync(1 + qd, 64);
-      const float m_cand = mx * p.scale_log2;
-      const bool move = m_cand > m_r + kLazyRescale;  // (always on the first block)
-      const float alpha = !move ? 1.f : m_r == -INFINITY ? 0.f : ex2_ftz(m_r - m_cand);
-      if (move) m_r = m_cand;
-      const float m_new = m_r;
-      // pass 2: P = 2^(S scale - m) in fp16 into TMEM, a page's 16 keys as
-      // 8 packed columns over the start of that page's own S columns (this
-      // thread read them above; the MMA thread issues S of block + 2 into
-      // this buffer only after the P V product that reads P)
-      // (the scale and the sum as packed fp32 pairs)
-      float2 ls2 = make_float2(0.f, 0.f);
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), mneg2 = make_float2(-m_new, -m_new);
-#pragma unroll
-      for (int j = 0; j < HP; ++j) {
-        const int pg = pg_lo + j;
-        if (pg >= pg_hi) break;
-        const int vp = vp0 + pg;
-        const int nvalid = vp < n_ctx_pages ? min(kPage, T - vp * kPage) : kPage;
-        uint32_t pk[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 t = __ffma2_rn(make_float2(__uint_as_float(sv[j][2 * k]), __uint_as_float(sv[j][2 * k + 1])),
-                                      sc2, mneg2);
-          float e0 = ex2_ftz(t.x), e1 = ex2_ftz(t.y);
-          if (nvalid != kPage) {
-            e0 = 2 * k < nvalid ? e0 : 0.f;
-            e1 = 2 * k + 1 < nvalid ? e1 : 0.f;
-          }
-          ls2 = __fadd2_rn(ls2, make_float2(e0, e1));
-          pk[k] = pack_half2(e0, e1);
+        m_r = pair_max(mx) * p.scale_log2;
+        alpha = 0.f;
+        move = true;
+        make_p(false, mx);
+      } else {
+        // P against the current m_r while the block's max is taken; only if
+        // a row's max passes m_r by more than kLazyRescale is m_r moved and
+        // P taken again (the S values are still in registers)
+        make_p(true, mx);
+        const float m_cand = pair_max(mx) * p.scale_log2;
+        move = m_cand > m_r + kLazyRescale;
+        alpha = move ? ex2_ftz(m_r - m_cand) : 1.f;
+        if (__any_sync(0xffffffffu, move)) {
+          if (move) m_r = m_cand;
+          float unused = -INFINITY;
+          tc_wait_st();  // the first P stores have landed before they are overwritten
+          make_p(false, unused);
+          rescale_o(blk, alpha);
         }
-        tc_st_32x32b_x8(tmem + lane_base + C::s_col(blk % C::NSB) + 16 * pg, pk);
       }
       l_r = l_r * alpha + (ls2.x + ls2.y);
-      if (blk > 0 && __any_sync(0xffffffffu, move)) rescale_o(blk, alpha);
       tc_wait_st();  // P (and a rescaled O) is in TMEM before the MMA thread hears of it
       tc_fence_before();
       mbarrier_arrive_one(&p_full[blk % C::NSB]);
