@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
   // accumulates there.  o_acc then holds the row's 32 head dims (index j:
   // o_acc[j / 8][j % 8]); m_run[0] and l_run[0] its max and sum.
   constexpr bool ROWT = C::M == 128 && C::PIPE && DH == 64;
-  static_assert(!ROWT || (!ONE && RPT * 2 * OG == 32), "a row-wise thread keeps 32 head dims");
+  static_assert(!ROWT || (!ONE && RPT * 2 * OG == 32 && RPT >= 3), "a row-wise thread keeps 32 head dims");
   const int qd = warp & 3, hf = warp >> 2;
   const bool soft = warp < 8 && qd < C::QUADS;
   float o_acc[ONE ? 1 : RPT][ONE ? 1 : 2 * OG];
@@ -534,13 +534,13 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         }
       };
       // the row's max over this half's keys, then over both halves (the
-      // partner warp holds the row's other pages)
+      // partner warp holds the row's other pages).  One barrier: the slot
+      // alternates by block, and a slot is written again only after the
+      // next block's barrier, which the partner passes after its read.
       auto pair_max = [&](float mx) {
-        s_red[(warp * 32 + lane) * RPT] = mx;
+        s_red[(warp * 32 + lane) * RPT + (blk & 1)] = mx;
         named_sync(1 + qd, 64);
-        mx = fmaxf(mx, s_red[(((warp + 4) & 7) * 32 + lane) * RPT]);
-        named_sync(1 + qd, 64);
-        return mx;
+        return fmaxf(mx, s_red[(((warp + 4) & 7) * 32 + lane) * RPT + (blk & 1)]);
       };
       float mx = -INFINITY, alpha;
       bool move;
@@ -596,11 +596,11 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
 #pragma unroll
       for (int j = 0; j < 32; ++j) o_acc[j >> 3][j & 7] = 0.f;
     }
-    // the row's full sum: this half's plus the partner's
-    s_red[(warp * 32 + lane) * RPT] = l_r;
+    // the row's full sum: this half's plus the partner's (slot 2: the
+    // block slots may still be read)
+    s_red[(warp * 32 + lane) * RPT + 2] = l_r;
     named_sync(1 + qd, 64);
-    l_r += s_red[(((warp + 4) & 7) * 32 + lane) * RPT];
-    named_sync(1 + qd, 64);
+    l_r += s_red[(((warp + 4) & 7) * 32 + lane) * RPT + 2];
     m_run[0] = m_r;
     l_run[0] = l_r;
   } else if (soft) {
