@@ -50,6 +50,11 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's view of global memory (generic proxy) before its
+// later async-proxy accesses of it (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
@@ -190,6 +195,15 @@ __device__ __forceinline__ void bulk_copy_smem_to_rank(uint32_t dst_local, uint3
           dsmem_map(dst_local, rank)),
       "r"(src_local), "r"(bytes), "r"(dsmem_map(smem_u32(bar), rank))
       : "memory");
+}
+// Bulk copy global memory -> this CTA's shared memory (16-byte aligned
+// addresses, a multiple of 16 bytes), completing as transaction bytes on
+// the mbarrier `bar`.
+__device__ __forceinline__ void bulk_load_global(uint32_t dst_local, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_local),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 // Bulk copy shared memory -> global memory (the copy engine reads the
 // source asynchronously; 16-byte aligned addresses, a multiple of 16 bytes),

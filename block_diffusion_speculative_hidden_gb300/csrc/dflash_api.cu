@@ -170,6 +170,10 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
   void* ac_lo = lo ? w.take(Mc * d * e) : nullptr;
   auto ss_c = lo ? static_cast<float*>(w.take(sizeof(float) * d_tiles * Mc)) : nullptr;
   auto crow = lo ? static_cast<int32_t*>(w.take(sizeof(int32_t) * Mc)) : nullptr;
+  // the persistent projection kernel's split tail (it serves 256 rows and more)
+  const bool pers = g.dtype == DFLASH_BF16 && std::max(R, M) >= 256;
+  auto pers_ws = pers ? static_cast<float*>(w.take(sizeof(float) * num_sms * 128 * 128)) : nullptr;
+  auto pers_cnt = pers ? static_cast<int*>(w.take(sizeof(int) * num_sms)) : nullptr;
   if (c != nullptr) {
     c->status = status;
     c->scal = status + 4;
@@ -209,6 +213,8 @@ size_t layout(const dflash_config& g, int num_sms, dflash_ctx* c, char* base) {
     c->ac_lo = ac_lo;
     c->ss_c = ss_c;
     c->crow = crow;
+    c->pers_ws = pers_ws;
+    c->pers_cnt = pers_cnt;
   }
   return w.off;
 }
@@ -449,6 +455,7 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, v
   // zero the pool once: attention multiplies masked (zero-probability) slots
   // by their values, which must therefore be finite
   if (cudaMemsetAsync(kv_pool, 0, dflash_kv_pool_size(cfg), nullptr) != cudaSuccess ||
+      (c->pers_cnt != nullptr && cudaMemsetAsync(c->pers_cnt, 0, sizeof(int) * sms, nullptr) != cudaSuccess) ||
       launch_rope_table(c, nullptr) != cudaSuccess || launch_reset(c, nullptr) != cudaSuccess ||
       cudaStreamSynchronize(nullptr) != cudaSuccess) {
     delete c;
@@ -476,6 +483,8 @@ dflash_status dflash_destroy(dflash_ctx* ctx) {
 dflash_status dflash_reset(dflash_ctx* ctx, dflash_stream stream) {
   if (ctx == nullptr) return DFLASH_ERR_INVALID_ARG;
   DF_CHECK(launch_reset(ctx, stream));
+  if (ctx->pers_cnt != nullptr)
+    DF_CHECK(cudaMemsetAsync(ctx->pers_cnt, 0, sizeof(int) * ctx->num_sms, static_cast<cudaStream_t>(stream)));
   return DFLASH_OK;
 }
 

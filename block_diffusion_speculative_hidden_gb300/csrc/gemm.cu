@@ -234,7 +234,7 @@ bool gemm_l2_plan(dflash_ctx* c, const NextGemm& nx, L2Plan* pl, CUtensorMap* ma
   return true;
 }
 
-int pers_plan(int M, int N, int K, int num_sms, int split_slots) {
+int pers_plan(int M, int N, int K, int num_sms, int split_slots, bool split_tail) {
   // the persistent kernel serves the tensor-bound sizes (at least 256
   // activation rows) with 128 x 128 tiles, one CTA a tile or a cluster pair
   // splitting K (each half a tile's time, a small price for the exchange);
@@ -244,7 +244,15 @@ int pers_plan(int M, int N, int K, int num_sms, int split_slots) {
   if (M < 256 || num_sms < 1) return 0;
   const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + 127) / 128);
   const double ideal = static_cast<double>(tiles) / num_sms;  // in full-K tile times
-  const double t1 = static_cast<double>((tiles + num_sms - 1) / num_sms);
+  double t1 = static_cast<double>((tiles + num_sms - 1) / num_sms);
+  // the split tail: the last, partial round's tiles split in K among up to
+  // kPersMaxSeg CTAs each (plus the partial tiles' write-out and sum)
+  const long long rem = tiles % num_sms;
+  const int n_kb = gemm_kb(K);
+  if (split_tail && tiles > num_sms && rem > 0) {
+    const int seg = static_cast<int>(std::min<long long>(kPersMaxSeg, num_sms / rem));
+    if (seg >= 2) t1 = static_cast<double>(tiles / num_sms) + static_cast<double>((n_kb + seg - 1) / seg) / n_kb + 0.05;
+  }
   double best_eff = tiles >= num_sms ? ideal / t1 : 0.0;
   int best = 1;
   double ok_eff = best_eff;
@@ -285,7 +293,7 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s) {
   int plan = 0;
   if (!w8 && split && (g.splits == 1 || g.epi.kind != EPI_NONE) && g.M >= 256 && c->num_sms > 0) {
     if (!lm && c->pers_split_clusters < 0) c->pers_split_clusters = pers_split_clusters(PersCfg<128, false, 2>::SMEM);
-    plan = pers_plan(g.M, g.N, g.K, c->num_sms, lm ? 0 : std::max(0, c->pers_split_clusters));
+    plan = pers_plan(g.M, g.N, g.K, c->num_sms, lm ? 0 : std::max(0, c->pers_split_clusters), !lm && c->pers_ws != nullptr);
   }
   if (plan > 0) {
     // many activation rows: the persistent kernel (a tile's reduction stays

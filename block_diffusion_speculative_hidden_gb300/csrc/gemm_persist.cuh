@@ -72,7 +72,14 @@ struct PersParams {
   const int* skip_rows;
   const int* logits_rows;
   int logits_bulk;
+  // split tail (single-CTA projections): fp32 partial tiles [grid][BN][128]
+  // and one arrival counter per tail tile (zero between launches), or null
+  float* ws;
+  int* ws_cnt;
 };
+
+// The most CTAs that share one tile of the last, partial round.
+constexpr int kPersMaxSeg = 8;
 
 // STORE / RESIDUAL epilogue of one tile, row-major: warp w finishes rows
 // w, w + 4, ... and lane l the columns n0 + 4l .. n0 + 4l + 3 (128-bit loads
@@ -211,6 +218,15 @@ __device__ __forceinline__ void epilogue_qkv_vec(const EpiArgs& e, const float* 
   }
 }
 
+// Split tail (KSPLIT = 1 projections, given a workspace): the tiles are
+// dealt round-robin in whole rounds of one tile a CTA, and the R < grid
+// tiles of the last, partial round are each split in K among s =
+// min(kPersMaxSeg, grid / R) CTAs (when that is at least 2), CTA u taking
+// k-segment u % s of tail tile u / s; it writes its partial tile to its own
+// workspace slot and counts itself in; the last of the s to arrive sums the
+// s slots in segment order (the same order whoever is last) and runs the
+// fused epilogue, then resets the count.  Nobody waits for another CTA.
+//
 // KSPLIT = 2: the two CTAs of a cluster share each tile, CTA r multiplying
 // the k-blocks of half r (rank 0 takes the larger half).  Both read their
 // accumulator out into their own tile, then CTA r sums rows 64 r .. 64 r + 63
@@ -236,9 +252,12 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
   uint64_t* acce = accf + 2;                                    // [2] accumulator read out
   uint64_t* ready = acce + 2;                                   // KSPLIT 2: the peer's tile is complete
   uint64_t* cons = ready + 1;                                   // KSPLIT 2: the peer has read this tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cons + 1);
+  uint64_t* fixb = cons + 1;                                    // split tail: the partial tiles' chunk landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixb + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  static_assert((2 * C::STAGES + 6) * 8 + 8 <= 256, "barrier area");
+  volatile int* s_last = s_abort + 1;  // split tail: this CTA finishes its tail tile
+  static_assert((2 * C::STAGES + 7) * 8 + 12 <= 256, "barrier area");
+  static_assert(KSPLIT != 1 || LMHEAD || kPersMaxSeg * C::CH * 128 * 4 <= C::RING_BYTES, "a chunk of every partial fits the ring");
   float* red = reinterpret_cast<float*>(aux + 256);             // [BN][4]
   float* s_rs = red + 4 * BN;                                   // folded-RMSNorm row scales
   int4* s_ri = reinterpret_cast<int4*>(s_rs + BN);              // per-row epilogue facts
@@ -259,9 +278,25 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
   const int mv = p.m_valid != nullptr ? min(p.M, __ldg(p.m_valid)) : p.M;
   const int m_tiles = min(p.m_tiles, (mv + BN - 1) / BN);
   const int n_work = p.n_tiles * m_tiles;
-  const int my_tiles = unit < n_work ? (n_work - unit + n_units - 1) / n_units : 0;
-  auto tile_of = [&](int tl, int& n0, int& m0) {
-    const int t = unit + tl * n_units;
+  // the split tail: n_full whole rounds, then rem tiles in n_seg segments each
+  const int n_full = n_work / n_units, rem = n_work - n_full * n_units;
+  const int n_seg = KSPLIT == 1 && !LMHEAD && p.ws != nullptr && rem > 0 ? min(kPersMaxSeg, n_units / rem) : 1;
+  const bool split_tail = n_seg >= 2;
+  const int my_tiles = split_tail ? n_full + (unit < rem * n_seg ? 1 : 0)
+                       : unit < n_work ? (n_work - unit + n_units - 1) / n_units
+                                       : 0;
+  const int tail_idx = unit / n_seg;  // (split tail) this CTA's tail tile, after the n_full rounds
+  // tile tl of this CTA: its corner and its k-blocks [ka, kz)
+  auto tile_of = [&](int tl, int& n0, int& m0, int& ka, int& kz) {
+    int t = unit + tl * n_units;
+    ka = kb0;
+    kz = kb1;
+    if (split_tail && tl == n_full) {
+      const int sg = unit % n_seg;
+      t = n_full * n_units + tail_idx;
+      ka = kb0 + sg * nkb / n_seg;
+      kz = kb0 + (sg + 1) * nkb / n_seg;
+    }
     n0 = (t / m_tiles) * kTileN;
     m0 = (t % m_tiles) * BN;
   };
@@ -280,6 +315,7 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
     }
     mbar_init(ready, 1);
     mbar_init(cons, 1);
+    mbar_init(fixb, 1);
     *s_abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -300,28 +336,37 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
 
   if (warp == C::PRODUCER) {
     if (lane == 0) {
-      const int total = my_tiles * nkb;
-      auto coords = [&](int it, int& n0, int& m0, int& kx) {
-        tile_of(it / nkb, n0, m0);
-        kx = (kb0 + it % nkb) * kTileK;
+      // a cursor over (tile, k-block) in issue order
+      int total = 0;
+      for (int tl = 0; tl < my_tiles; ++tl) {
+        int n0, m0, ka, kz;
+        tile_of(tl, n0, m0, ka, kz);
+        total += kz - ka;
+      }
+      int c_tl = 0, c_kb = 0, c_kz = 0, c_n0 = 0, c_m0 = 0;
+      if (my_tiles > 0) tile_of(0, c_n0, c_m0, c_kb, c_kz);
+      auto coords = [&](int& n0, int& m0, int& kx) {  // the cursor's stage, then advance
+        n0 = c_n0;
+        m0 = c_m0;
+        kx = c_kb * kTileK;
+        if (++c_kb == c_kz && ++c_tl < my_tiles) tile_of(c_tl, c_n0, c_m0, c_kb, c_kz);
       };
       // the weights do not depend on the predecessor: the first stages'
       // weight tiles go out before its completion, their activations after
       const int pre = min(total, C::STAGES);
+      int pm0[C::STAGES], pkx[C::STAGES];
       for (int it = 0; it < pre; ++it) {
-        int n0, m0, kx;
-        coords(it, n0, m0, kx);
+        int n0;
+        coords(n0, pm0[it], pkx[it]);
         mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
-        tma_load_2d(ring + it * C::STAGE_BYTES, &tmW, &full[it], kx, n0);
+        tma_load_2d(ring + it * C::STAGE_BYTES, &tmW, &full[it], pkx[it], n0);
       }
       pdl_wait();
       pdl_trigger();
       for (int it = 0; it < pre; ++it) {
-        int n0, m0, kx;
-        coords(it, n0, m0, kx);
         uint8_t* st = ring + it * C::STAGE_BYTES;
-        tma_load_2d(st + C::W_BYTES, &tmX, &full[it], kx, m0);
-        tma_load_2d(st + C::W_BYTES + C::X_BOX, &tmXlo, &full[it], kx, m0);
+        tma_load_2d(st + C::W_BYTES, &tmX, &full[it], pkx[it], pm0[it]);
+        tma_load_2d(st + C::W_BYTES + C::X_BOX, &tmXlo, &full[it], pkx[it], pm0[it]);
       }
       int issued = pre;
       for (int it = pre; it < total; ++it) {
@@ -331,7 +376,7 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
           break;
         }
         int n0, m0, kx;
-        coords(it, n0, m0, kx);
+        coords(n0, m0, kx);
         uint8_t* st = ring + s * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         tma_load_2d(st, &tmW, &full[s], kx, n0);
@@ -358,7 +403,9 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
         }
         tc_fence_after();
         const uint32_t acc = tmem + static_cast<uint32_t>(a * C::ACC_COLS);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        int n0, m0, ka, kz;
+        tile_of(tl, n0, m0, ka, kz);
+        for (int kb = 0; kb < kz - ka; ++kb, ++it) {
           const int s = it % C::STAGES;
           if (*s_abort || !mbar_wait(&full[s], (it / C::STAGES) & 1, p.status)) {
             ok = false;
@@ -384,104 +431,28 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
     bool live = true;
     const uint32_t tquad = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     for (int tl = 0; tl < my_tiles; ++tl) {
-      int n0, m0;
-      tile_of(tl, n0, m0);
+      int n0, m0, ka, kz;
+      tile_of(tl, n0, m0, ka, kz);
+      const bool seg_tile = split_tail && tl == n_full;  // a k-segment of a tail tile
       const int n = n0 + warp * 32 + lane;
       const bool nv = n < p.N;
-      // row facts of the rows this CTA finishes (s_rs / s_ri index j of row r0 + j)
-      for (int j = threadIdx.x; j < ROWS; j += kEpiThreads) {
-        const int m = m0 + r0 + j;
-        const bool ok = m < mv;
-        if (p.epi.ss_in != nullptr) s_rs[j] = ok ? norm_row_scale(p.epi, m) : 0.f;
-        if constexpr (LMHEAD) {
-          const int orow = ok ? (p.logits_rows != nullptr ? p.logits_rows[m] : m) : -1;
-          s_ri[j] = make_int4(orow, 0, 0, orow >= 0 && (p.skip_rows == nullptr || p.skip_rows[m] == 0) ? 1 : 0);
-        } else {
-          s_ri[j] = ok ? epi_row_info(p.epi, m) : make_int4(0, 0, 0, 0);
-        }
-      }
-      const int a = tl & 1;
-      live = live && !*s_abort && mbar_wait(&accf[a], (tl >> 1) & 1, p.status);
-      if constexpr (KSPLIT == 2) {
-        // the peer has read this CTA's previous tile
-        if (tl >= 1) live = live && !*s_abort && mbar_wait_cluster(cons, (tl - 1) & 1, p.status);
-      }
-      if (!live) *s_abort = 1;
-      __syncwarp();
-      tc_fence_after();
-      epi_sync();  // the row facts are complete
-      const uint32_t tacc = tquad + static_cast<uint32_t>(a * C::ACC_COLS);
-      constexpr int CH = C::CH;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += CH) {
-        // activation rows c0 .. c0 + CH - 1 of the tile into the staging tile
-#pragma unroll 1
-        for (int c = c0; c < c0 + CH; c += 16) {
-          float v[16], v2[16];
-          if (live) {
-            tc_ld_32x32b_x16(tacc + c, v);
-            tc_ld_32x32b_x16(tacc + BN + c, v2);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float z = live ? v[j] + v2[j] : 0.f;
-            if constexpr (LMHEAD) z = nv ? (p.epi.ss_in != nullptr ? z * s_rs[c + j] : z) : -INFINITY;
-            tile[(c - c0 + j) * C::LD + warp * 32 + lane] = z;
-          }
-        }
-        if (c0 + CH == BN) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbarrier_arrive_one(&acce[a]);  // accumulator a may take the tile after next
-        }
-        // the rows this CTA finishes from this chunk: a chunk of its own
-        // tile (KSPLIT 1), or its half of the pair's sum (KSPLIT 2); fr: the
-        // first one's index in the row facts
-        float* mine = tile;
-        int fr = c0;
-        if constexpr (KSPLIT == 2) {
-          // both halves of the sum: the peer's tile complete, add its rows
-          // r0 .. r0 + 63 to ours (rank 0's term first), then let it reuse
-          // its tile
-          mine = tile + r0 * C::LD;
-          fr = 0;
-          epi_sync();
-          if (threadIdx.x == 0) {
-            fence_acq_rel_cluster();
-            mbar_remote_arrive(ready, static_cast<uint32_t>(rank ^ 1));
-          }
-          live = live && !*s_abort && mbar_wait_cluster(ready, tl & 1, p.status);
-          if (!live) *s_abort = 1;
-          const uint32_t peer = dsmem_map(smem_u32(mine), static_cast<uint32_t>(rank ^ 1));
-          for (int e = threadIdx.x; e < ROWS * 32; e += kEpiThreads) {
-            const int j = e >> 5, c4 = (e & 31) * 4;
-            float4 own = *reinterpret_cast<const float4*>(mine + j * 128 + c4);
-            const float4 oth =
-                live ? ld_dsmem_f4(peer + static_cast<uint32_t>((j * 128 + c4) * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 sum = rank == 0 ? make_float4(own.x + oth.x, own.y + oth.y, own.z + oth.z, own.w + oth.w)
-                                   : make_float4(oth.x + own.x, oth.y + own.y, oth.z + own.z, oth.w + own.w);
-            *reinterpret_cast<float4*>(mine + j * 128 + c4) = sum;
-          }
-          epi_sync();
-          if (threadIdx.x == 0) {
-            fence_acq_rel_cluster();
-            mbar_remote_arrive(cons, static_cast<uint32_t>(rank ^ 1));
-          }
-        }
+      // the fused epilogue of activation rows c0 .. of the tile, staged in
+      // `mine` (fr: the first one's index in the row facts)
+      auto finish = [&](int c0, float* mine, int fr) {
         const int mr0 = KSPLIT == 2 ? m0 + r0 : m0 + c0;  // first output row of `mine`
-        constexpr int NR = KSPLIT == 2 ? ROWS : CH;
+        constexpr int NR = KSPLIT == 2 ? ROWS : C::CH;
         const int rows = min(NR, mv - mr0);
         if constexpr (LMHEAD) {
           const bool bulk_out = p.logits != nullptr && p.logits_bulk && n0 + kTileN <= p.N;
           if (!bulk_out && p.logits != nullptr && nv)
-            for (int j = 0; j < CH; ++j)
+            for (int j = 0; j < C::CH; ++j)
               if (s_ri[c0 + j].w != 0)
                 __stcs(p.logits + s_ri[c0 + j].x * p.ld_logits + n, tile[j * C::LD + warp * 32 + lane]);
           if (bulk_out) fence_proxy_async_smem();
           epi_sync();
           if (bulk_out && warp == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            for (int j = lane; j < CH; j += 32)
+            for (int j = lane; j < C::CH; j += 32)
               if (s_ri[c0 + j].w != 0)
                 bulk_store_global(p.logits + s_ri[c0 + j].x * p.ld_logits + n0, smem_u32(tile + j * C::LD), kTileN * 4,
                                   pol);
@@ -492,7 +463,7 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
           const int seg = threadIdx.x & 7;
           const int ntile = n0 / kTileN;
 #pragma unroll 1
-          for (int rb = 0; rb < CH; rb += kEpiThreads >> 3) {
+          for (int rb = 0; rb < C::CH; rb += kEpiThreads >> 3) {
             const int j = rb + (threadIdx.x >> 3);
             const float* row = tile + j * C::LD;
             float z[16];
@@ -549,7 +520,144 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
             }
           }
         }
+      };
+      // row facts of the rows this CTA finishes (s_rs / s_ri index j of row r0 + j)
+      for (int j = threadIdx.x; j < ROWS; j += kEpiThreads) {
+        const int m = m0 + r0 + j;
+        const bool ok = m < mv;
+        if (p.epi.ss_in != nullptr) s_rs[j] = ok ? norm_row_scale(p.epi, m) : 0.f;
+        if constexpr (LMHEAD) {
+          const int orow = ok ? (p.logits_rows != nullptr ? p.logits_rows[m] : m) : -1;
+          s_ri[j] = make_int4(orow, 0, 0, orow >= 0 && (p.skip_rows == nullptr || p.skip_rows[m] == 0) ? 1 : 0);
+        } else {
+          s_ri[j] = ok ? epi_row_info(p.epi, m) : make_int4(0, 0, 0, 0);
+        }
+      }
+      const int a = tl & 1;
+      live = live && !*s_abort && mbar_wait(&accf[a], (tl >> 1) & 1, p.status);
+      if constexpr (KSPLIT == 2) {
+        // the peer has read this CTA's previous tile
+        if (tl >= 1) live = live && !*s_abort && mbar_wait_cluster(cons, (tl - 1) & 1, p.status);
+      }
+      if (!live) *s_abort = 1;
+      __syncwarp();
+      tc_fence_after();
+      epi_sync();  // the row facts are complete
+      const uint32_t tacc = tquad + static_cast<uint32_t>(a * C::ACC_COLS);
+      constexpr int CH = C::CH;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += CH) {
+        // activation rows c0 .. c0 + CH - 1 of the tile into the staging tile
+#pragma unroll 1
+        for (int c = c0; c < c0 + CH; c += 16) {
+          float v[16], v2[16];
+          if (live) {
+            tc_ld_32x32b_x16(tacc + c, v);
+            tc_ld_32x32b_x16(tacc + BN + c, v2);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float z = live ? v[j] + v2[j] : 0.f;
+            if constexpr (LMHEAD) z = nv ? (p.epi.ss_in != nullptr ? z * s_rs[c + j] : z) : -INFINITY;
+            tile[(c - c0 + j) * C::LD + warp * 32 + lane] = z;
+          }
+        }
+        if (c0 + CH == BN) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbarrier_arrive_one(&acce[a]);  // accumulator a may take the tile after next
+        }
+        if (seg_tile) {
+          // a k-segment's partial: the chunk into this CTA's workspace slot
+          epi_sync();
+          float* slot = p.ws + static_cast<long long>(unit) * BN * 128;
+          for (int e = threadIdx.x; e < CH * 32; e += kEpiThreads) {
+            const int j = e >> 5, c4 = (e & 31) * 4;
+            __stcg(reinterpret_cast<float4*>(slot + (c0 + j) * 128 + c4),
+                   *reinterpret_cast<const float4*>(tile + j * C::LD + c4));
+          }
+          epi_sync();  // the staging tile is free again
+          continue;
+        }
+        // the rows this CTA finishes from this chunk: a chunk of its own
+        // tile (KSPLIT 1), or its half of the pair's sum (KSPLIT 2); fr: the
+        // first one's index in the row facts
+        float* mine = tile;
+        int fr = c0;
+        if constexpr (KSPLIT == 2) {
+          // both halves of the sum: the peer's tile complete, add its rows
+          // r0 .. r0 + 63 to ours (rank 0's term first), then let it reuse
+          // its tile
+          mine = tile + r0 * C::LD;
+          fr = 0;
+          epi_sync();
+          if (threadIdx.x == 0) {
+            fence_acq_rel_cluster();
+            mbar_remote_arrive(ready, static_cast<uint32_t>(rank ^ 1));
+          }
+          live = live && !*s_abort && mbar_wait_cluster(ready, tl & 1, p.status);
+          if (!live) *s_abort = 1;
+          const uint32_t peer = dsmem_map(smem_u32(mine), static_cast<uint32_t>(rank ^ 1));
+          for (int e = threadIdx.x; e < ROWS * 32; e += kEpiThreads) {
+            const int j = e >> 5, c4 = (e & 31) * 4;
+            float4 own = *reinterpret_cast<const float4*>(mine + j * 128 + c4);
+            const float4 oth =
+                live ? ld_dsmem_f4(peer + static_cast<uint32_t>((j * 128 + c4) * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 sum = rank == 0 ? make_float4(own.x + oth.x, own.y + oth.y, own.z + oth.z, own.w + oth.w)
+                                   : make_float4(oth.x + own.x, oth.y + own.y, oth.z + own.z, oth.w + own.w);
+            *reinterpret_cast<float4*>(mine + j * 128 + c4) = sum;
+          }
+          epi_sync();
+          if (threadIdx.x == 0) {
+            fence_acq_rel_cluster();
+            mbar_remote_arrive(cons, static_cast<uint32_t>(rank ^ 1));
+          }
+        }
+        finish(c0, mine, fr);
         epi_sync();  // the staging tile is free again
+      }
+      if (seg_tile) {
+        // count this segment in; the last of the tile's n_seg sums their
+        // slots in segment order and finishes the tile
+        __threadfence();
+        epi_sync();
+        if (threadIdx.x == 0) *s_last = atomicAdd(&p.ws_cnt[tail_idx], 1) == n_seg - 1 ? 1 : 0;
+        epi_sync();
+        if (*s_last) {
+          // chunk by chunk, the n_seg partials' rows come into the ring (idle:
+          // this is the CTA's last tile) by bulk copies, are summed in segment
+          // order into the staging tile and finished
+          __threadfence();
+          if (threadIdx.x == 0) fence_proxy_async_global();
+          const float* base = p.ws + static_cast<long long>(tail_idx) * n_seg * BN * 128;
+          const float* part = reinterpret_cast<const float*>(ring);  // [n_seg][CH][128]
+          constexpr uint32_t CHUNK = CH * 128 * 4;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += CH) {
+            if (threadIdx.x == 0) {
+              mbar_arrive_expect_tx(fixb, static_cast<uint32_t>(n_seg) * CHUNK);
+              for (int sg = 0; sg < n_seg; ++sg)
+                bulk_load_global(smem_u32(ring) + sg * CHUNK, base + (static_cast<long long>(sg) * BN + c0) * 128, CHUNK,
+                                 fixb);
+            }
+            live = live && mbar_wait(fixb, (c0 / CH) & 1, p.status);
+            for (int e = threadIdx.x; e < CH * 32; e += kEpiThreads) {
+              const int j = e >> 5, c4 = (e & 31) * 4;
+              float4 acc = *reinterpret_cast<const float4*>(part + j * 128 + c4);
+              for (int sg = 1; sg < n_seg; ++sg) {
+                const float4 v = *reinterpret_cast<const float4*>(part + (sg * CH + j) * 128 + c4);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+              }
+              *reinterpret_cast<float4*>(tile + j * C::LD + c4) = acc;
+            }
+            finish(c0, tile, c0);  // (its first step is a barrier: the chunk is complete, the ring read)
+            epi_sync();            // the staging tile is free again
+          }
+          if (threadIdx.x == 0) p.ws_cnt[tail_idx] = 0;  // for the next launch
+        }
       }
     }
     if constexpr (KSPLIT == 2) {
@@ -618,6 +726,10 @@ cudaError_t launch_pers(dflash_ctx* c, const GemmLaunch& g, const CUtensorMap& t
   p.skip_rows = g.skip_rows;
   p.logits_rows = g.logits_rows;
   p.logits_bulk = g.logits != nullptr && (reinterpret_cast<uintptr_t>(g.logits) & 15) == 0 && g.ld_logits % 4 == 0;
+  if (KSPLIT == 1 && !LM && c->pers_ws != nullptr && BN == 128) {
+    p.ws = c->pers_ws;  // one slot per CTA: the grid is at most num_sms
+    p.ws_cnt = c->pers_cnt;
+  }
   const int work = p.n_tiles * p.m_tiles;
   int grid;
   if (KSPLIT == 2) {

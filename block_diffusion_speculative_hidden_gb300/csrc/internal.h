@@ -162,6 +162,11 @@ struct dflash_ctx {
   void *ac = nullptr, *ac_lo = nullptr;
   float* ss_c = nullptr;
   int32_t* crow = nullptr;  // compact row -> block row ([max_batch * K/2])
+  // persistent projections, split tail: a partial tile per CTA
+  // [num_sms][128][128] fp32 and an arrival count per tail tile [num_sms]
+  // (zero between launches); null where the persistent kernel never runs
+  float* pers_ws = nullptr;
+  int* pers_cnt = nullptr;
   // stream being recorded into a graph (dflash_graph_begin), else null
   cudaStream_t capture = nullptr;
   bool capturing = false;
@@ -222,7 +227,7 @@ int gemm_bn(int M, bool split, bool w8 = false);
 // The persistent projection kernel's plan for an M x N x K projection with
 // hi + lo activations: CTAs per tile (1, or 2 splitting K), 0 where the
 // kernel does not apply.  split_slots: cluster pairs that fit at once.
-int pers_plan(int M, int N, int K, int num_sms, int split_slots);
+int pers_plan(int M, int N, int K, int num_sms, int split_slots, bool split_tail);
 int gemm_kb_per_split(int n_kb, int splits, bool w8);
 int gemm_normalize_splits(int n_kb, int splits, bool w8);
 int gemm_blocks_per_sm(int bn, bool split, bool w8);
