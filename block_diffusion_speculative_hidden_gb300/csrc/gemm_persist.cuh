@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
       int issued = pre;
       for (int it = pre; it < total; ++it) {
         const int s = it % C::STAGES;
-        if (*s_abort || !mbar_wait(&empty[s], ((it / C::STAGES) & 1) ^ 1, p.status)) {
+        if (*s_abort || !mbar_wait_spin(&empty[s], ((it / C::STAGES) & 1) ^ 1, p.status)) {
           *s_abort = 1;
           break;
         }
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
         tile_of(tl, n0, m0, ka, kz);
         for (int kb = 0; kb < kz - ka; ++kb, ++it) {
           const int s = it % C::STAGES;
-          if (*s_abort || !mbar_wait(&full[s], (it / C::STAGES) & 1, p.status)) {
+          if (*s_abort || !mbar_wait_spin(&full[s], (it / C::STAGES) & 1, p.status)) {
             ok = false;
             break;
           }
