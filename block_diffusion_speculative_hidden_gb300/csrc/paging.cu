@@ -62,24 +62,31 @@ __global__ void k_truncate(int b, int new_len, int* scal, int32_t* free_ring, in
   seq_len[b] = new_len;
 }
 
-// One CTA.  Thread 0 plans the whole append serially (B is small); the row
-// map of the compacted rows is then written by all threads.
+// One CTA.  The threads bring every sequence's row count and length into
+// shared memory, thread 0 plans the append from there (prefix sums of rows
+// and of new pages, the checks), and the threads then write the page-table
+// entries, the row map of the compacted rows and the lengths in parallel.
 __global__ void k_alloc(const int32_t* __restrict__ n_rows, int first_seq, int B, int max_rows, int P, int max_pages,
                         int32_t* seq_len, int32_t* page_table, int32_t* free_ring, int* scal, int32_t* row_seq,
                         int32_t* row_pos, int32_t* row_src, int* status) {
-  extern __shared__ int s_off[];  // [B + 1] row offsets, then [B] old lengths
+  extern __shared__ int s_off[];  // [B + 1] row offsets, [B] old lengths, [B] row counts, [B] new-page offsets
   int* s_len = s_off + B + 1;
-  __shared__ int s_ok;
+  int* s_n = s_len + B;
+  int* s_pg = s_n + B;
+  __shared__ int s_ok, s_head;
   pdl_wait();
   pdl_trigger();
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    s_n[i] = n_rows[i];
+    s_len[i] = seq_len[first_seq + i];
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int bad = 0, total_need = 0, rows = 0;
     for (int i = 0; i < B; ++i) {
-      const int b = first_seq + i;
-      const int n = n_rows[i];
-      const int len = seq_len[b];
+      const int n = s_n[i], len = s_len[i];
       s_off[i] = rows;
-      s_len[i] = len;
+      s_pg[i] = total_need;
       if (n < 0 || n > max_rows) {
         bad |= ST_BAD_ROWS;
         continue;
@@ -97,21 +104,22 @@ __global__ void k_alloc(const int32_t* __restrict__ n_rows, int first_seq, int B
       scal[0] = 0;
       s_ok = 0;
     } else {
-      int k = 0;
-      for (int i = 0; i < B; ++i) {
-        const int b = first_seq + i;
-        const int len = s_len[i], n = n_rows[i];
-        const int p_old = (len + kPage - 1) / kPage, p_new = (len + n + kPage - 1) / kPage;
-        for (int j = p_old; j < p_new; ++j) page_table[b * max_pages + j] = free_ring[(head + k++) % P];
-      }
       scal[1] = (head + total_need) % P;
       scal[2] = count - total_need;
       scal[0] = rows;
+      s_head = head;
       s_ok = 1;
     }
   }
   __syncthreads();
   if (!s_ok) return;
+  // sequence i's new pages take the free ring's entries from head + s_pg[i] on
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    const int b = first_seq + i, len = s_len[i], n = s_n[i];
+    const int p_old = (len + kPage - 1) / kPage, p_new = (len + n + kPage - 1) / kPage;
+    for (int j = p_old; j < p_new; ++j)
+      page_table[b * max_pages + j] = free_ring[(s_head + s_pg[i] + (j - p_old)) % P];
+  }
   for (int i = 0; i < B; ++i) {
     const int n = s_off[i + 1] - s_off[i];
     for (int j = threadIdx.x; j < n; j += blockDim.x) {
@@ -156,7 +164,7 @@ cudaError_t launch_truncate(dflash_ctx* c, int b, int new_len, cudaStream_t s) {
 }
 
 cudaError_t launch_alloc(dflash_ctx* c, const int32_t* n_rows, int first_seq, int B, int max_rows, cudaStream_t s) {
-  const size_t smem = sizeof(int) * (2 * B + 1);
+  const size_t smem = sizeof(int) * (4 * B + 1);
   return launch_k(k_alloc, dim3(1), dim3(256), smem, s, dim3(1), c->pdl, n_rows, first_seq, B, max_rows,
                   c->cfg.n_pages, c->cfg.max_pages_per_seq, c->seq_len, c->page_table, c->free_ring, c->scal,
                   c->row_seq, c->row_pos, c->row_src, c->status);

@@ -37,25 +37,46 @@ __global__ void k_gather_rows(const T* __restrict__ feats, T* __restrict__ out, 
 // Block input: x[m] = E[token] (token = [MASK], or in pass 2 the committed
 // pass-1 token).  Also the first layer's pre-norm in folded form (see
 // epilogue.cuh): a[m] = g_in . x[m] and the per-128-column sums of x^2.
-// One CTA of 128 threads per (column tile, row).
+// One CTA of 128 threads per row, a warp per 128-column tile (four columns
+// a lane).
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+  const float4 t = *reinterpret_cast<const float4*>(p);
+  v[0] = t.x;
+  v[1] = t.y;
+  v[2] = t.z;
+  v[3] = t.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 t = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
+  v[0] = a.x;
+  v[1] = a.y;
+  v[2] = b.x;
+  v[3] = b.y;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128) k_embed(const T* __restrict__ embed, const T* __restrict__ gain,
                                                float* __restrict__ x, ActOut<T> a, float* __restrict__ ss, int ss_ld,
                                                int d, int mask_id, int vocab, const int32_t* commit,
                                                const int32_t* tok1, int* status, const int32_t* seq_len,
                                                int32_t* order, int B) {
-  __shared__ float red[4];
   pdl_wait();
   pdl_trigger();
-  const int tile = blockIdx.x, m = blockIdx.y, n = tile * 128 + threadIdx.x;
-  if (order != nullptr && tile == 0 && m == 0) {
+  const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (order != nullptr && m == 0) {
     // the attention's launch order: sequences by context length, longest
     // first (ties by index), so that the long ones do not start last
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
-      const int lb = seq_len[b];
+      const int lb = __ldg(seq_len + b);
       int rank = 0;
       for (int u = 0; u < B; ++u) {
-        const int lu = seq_len[u];
+        const int lu = __ldg(seq_len + u);
         rank += lu > lb || (lu == lb && u < b);
       }
       order[rank] = b;
@@ -64,20 +85,29 @@ __global__ void __launch_bounds__(128) k_embed(const T* __restrict__ embed, cons
   int tok = mask_id;
   if (commit != nullptr && commit[m] != 0) tok = tok1[m];
   if (tok < 0 || tok >= vocab) {
-    if (threadIdx.x == 0 && tile == 0) atomicOr(status, ST_BAD_TOKEN);
+    if (threadIdx.x == 0) atomicOr(status, ST_BAD_TOKEN);
     tok = mask_id;
   }
-  float v = 0.f;
-  if (n < d) {
-    v = to_f32(embed[static_cast<long long>(tok) * d + n]);
-    const long long e = static_cast<long long>(m) * d + n;
-    x[e] = v;
-    a.put(e, v * to_f32(gain[n]));
+  const T* row = embed + static_cast<long long>(tok) * d;
+  // warp w: the 128-column tiles w, w + 4, ...; lane l: their columns 4l .. 4l + 3
+  for (int tile = warp; tile * 128 < d; tile += 4) {
+    const int n = tile * 128 + 4 * lane;
+    float q = 0.f;
+    if (n < d) {  // d % 4 == 0: the four columns are valid together
+      float v[4], g[4];
+      load4(row + n, v);
+      load4(gain + n, g);
+      const long long e = static_cast<long long>(m) * d + n;
+      *reinterpret_cast<float4*>(x + e) = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a.put(e + k, v[k] * g[k]);
+        q += v[k] * v[k];
+      }
+    }
+    q = warp_sum(q);
+    if (lane == 0) ss[static_cast<long long>(tile) * ss_ld + m] = q;
   }
-  const float q = warp_sum(v * v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = q;
-  __syncthreads();
-  if (threadIdx.x == 0) ss[static_cast<long long>(tile) * ss_ld + m] = (red[0] + red[1]) + (red[2] + red[3]);
 }
 
 // fp32 path: per (row, 128-column tile) max / argmax / sum-exp of the logits,
@@ -273,7 +303,7 @@ cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, cudaS
 
 cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, int32_t* order, cudaStream_t s) {
   const auto& g = c->cfg;
-  const dim3 grid((g.hidden + 127) / 128, M);
+  const dim3 grid(M);
   DFLASH_DISPATCH(c, return launch_k(k_embed<T>, grid, dim3(128), 0, s, dim3(1), c->pdl,
                                      static_cast<const T*>(c->embed), static_cast<const T*>(c->g_in[0]), c->x,
                                      act_out<T>(c->a, c->a_lo), c->ss_x, g.max_batch * kBlockK, g.hidden,
