@@ -836,7 +836,7 @@ def mean_context(res) -> float:
 
 
 def roofline_block(cfg, res, hbm, tc, peak_kind):
-    """The dominant kernel's roofline (k_gemm_tc: projections + LM head) and
+    """The dominant kernel's roofline (the projections and LM head) and
     the per-class figures, from the profiled (second) timed region."""
     ab = algorithmic_bytes(cfg)
     fl = gemm_flops(cfg)
@@ -865,7 +865,11 @@ def roofline_block(cfg, res, hbm, tc, peak_kind):
         per_class["accept"]["frac_hbm"] = per_class["accept"]["GB_per_s"] / hbm
     per_class["synthetic_target"] = {"ms_per_step": res["target_ms"] / steps,
                                      "what": "torch ops that form the target's verify output; not this library's"}
-    common = {"kernel": "k_gemm_tc (tcgen05 projections + LM head)",
+    # the projections and LM head of 256 block rows and more run on the
+    # persistent kernel (k_gemm_pers), fewer on the single-tile one
+    kname = ("k_gemm_pers" if cfg.dtype == "bf16" and cfg.weight_format != "e4m3" and cfg.batch * K_BLOCK >= 256
+             else "k_gemm_tc")
+    common = {"kernel": f"{kname} (tcgen05 projections + LM head)",
               "launches_per_step": gemm_launches / steps,
               "timed_in": "second timed region of the same loop, per-launch CUDA events"}
     if tensor_bound(cfg):

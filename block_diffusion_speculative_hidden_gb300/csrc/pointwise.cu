@@ -37,8 +37,9 @@ __global__ void k_gather_rows(const T* __restrict__ feats, T* __restrict__ out, 
 // Block input: x[m] = E[token] (token = [MASK], or in pass 2 the committed
 // pass-1 token).  Also the first layer's pre-norm in folded form (see
 // epilogue.cuh): a[m] = g_in . x[m] and the per-128-column sums of x^2.
-// One CTA of 128 threads per row, a warp per 128-column tile (four columns
-// a lane).
+// CTAs of 128 threads per row, a warp per 128-column tile (four columns a
+// lane); a row's tiles in one CTA when there are many rows, four a CTA when
+// there are few.
 template <typename T>
 __device__ __forceinline__ void load4(const T* p, float (&v)[4]);
 template <>
@@ -65,11 +66,11 @@ __global__ void __launch_bounds__(128) k_embed(const T* __restrict__ embed, cons
                                                float* __restrict__ x, ActOut<T> a, float* __restrict__ ss, int ss_ld,
                                                int d, int mask_id, int vocab, const int32_t* commit,
                                                const int32_t* tok1, int* status, const int32_t* seq_len,
-                                               int32_t* order, int B) {
+                                               int32_t* order, int B, int tiles_per_cta) {
   pdl_wait();
   pdl_trigger();
-  const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (order != nullptr && m == 0) {
+  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (order != nullptr && m == 0 && blockIdx.x == 0) {
     // the attention's launch order: sequences by context length, longest
     // first (ties by index), so that the long ones do not start last
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
@@ -85,12 +86,14 @@ __global__ void __launch_bounds__(128) k_embed(const T* __restrict__ embed, cons
   int tok = mask_id;
   if (commit != nullptr && commit[m] != 0) tok = tok1[m];
   if (tok < 0 || tok >= vocab) {
-    if (threadIdx.x == 0) atomicOr(status, ST_BAD_TOKEN);
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, ST_BAD_TOKEN);
     tok = mask_id;
   }
   const T* row = embed + static_cast<long long>(tok) * d;
-  // warp w: the 128-column tiles w, w + 4, ...; lane l: their columns 4l .. 4l + 3
-  for (int tile = warp; tile * 128 < d; tile += 4) {
+  // this CTA's 128-column tiles t0 .. t1 - 1; warp w takes t0 + w, t0 + w + 4,
+  // ...; lane l their columns 4l .. 4l + 3
+  const int t0 = blockIdx.x * tiles_per_cta, t1 = min(t0 + tiles_per_cta, (d + 127) / 128);
+  for (int tile = t0 + warp; tile < t1; tile += 4) {
     const int n = tile * 128 + 4 * lane;
     float q = 0.f;
     if (n < d) {  // d % 4 == 0: the four columns are valid together
@@ -303,12 +306,13 @@ cudaError_t launch_gather_rows(dflash_ctx* c, const void* feats, int rows, cudaS
 
 cudaError_t launch_embed(dflash_ctx* c, int M, bool second_pass, int32_t* order, cudaStream_t s) {
   const auto& g = c->cfg;
-  const dim3 grid(M);
+  const int n_tiles = (g.hidden + 127) / 128, per = M >= 512 ? n_tiles : 4;
+  const dim3 grid((n_tiles + per - 1) / per, M);
   DFLASH_DISPATCH(c, return launch_k(k_embed<T>, grid, dim3(128), 0, s, dim3(1), c->pdl,
                                      static_cast<const T*>(c->embed), static_cast<const T*>(c->g_in[0]), c->x,
                                      act_out<T>(c->a, c->a_lo), c->ss_x, g.max_batch * kBlockK, g.hidden,
                                      g.mask_id, g.vocab, second_pass ? c->commit : nullptr, c->tok1, c->status,
-                                     c->seq_len, order, M / kBlockK));
+                                     c->seq_len, order, M / kBlockK, per));
 }
 
 cudaError_t launch_logits_tiles(dflash_ctx* c, int M, float* user_logits, const int32_t* skip, const EpiArgs& norm,
