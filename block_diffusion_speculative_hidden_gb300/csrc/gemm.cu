@@ -250,7 +250,7 @@ int pers_plan(int M, int N, int K, int num_sms, int split_slots, bool split_tail
   const long long rem = tiles % num_sms;
   const int n_kb = gemm_kb(K);
   if (split_tail && tiles > num_sms && rem > 0) {
-    const int seg = static_cast<int>(std::min<long long>(kPersMaxSeg, num_sms / rem));
+    const int seg = static_cast<int>(std::min<long long>(std::min<long long>(kPersMaxSeg, num_sms / rem), n_kb));
     if (seg >= 2) t1 = static_cast<double>(tiles / num_sms) + static_cast<double>((n_kb + seg - 1) / seg) / n_kb + 0.05;
   }
   double best_eff = tiles >= num_sms ? ideal / t1 : 0.0;

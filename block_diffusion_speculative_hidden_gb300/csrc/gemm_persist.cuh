@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
   const int n_work = p.n_tiles * m_tiles;
   // the split tail: n_full whole rounds, then rem tiles in n_seg segments each
   const int n_full = n_work / n_units, rem = n_work - n_full * n_units;
-  const int n_seg = KSPLIT == 1 && !LMHEAD && p.ws != nullptr && rem > 0 ? min(kPersMaxSeg, n_units / rem) : 1;
+  // (at least one k-block a segment)
+  const int n_seg = KSPLIT == 1 && !LMHEAD && p.ws != nullptr && rem > 0 ? min(min(kPersMaxSeg, n_units / rem), nkb) : 1;
   const bool split_tail = n_seg >= 2;
   const int my_tiles = split_tail ? n_full + (unit < rem * n_seg ? 1 : 0)
                        : unit < n_work ? (n_work - unit + n_units - 1) / n_units
