@@ -157,6 +157,14 @@ MINI_CONFIGS: Dict[str, DraftConfig] = {
                             hidden=384, n_q_heads=16, n_kv_heads=2, head_dim=64,
                             ffn=784, vocab=3001, n_taps=3, tap_width=384,
                             s_passes=2, accept="stochastic", rounds=3, seed=2006, weight_format="e4m3"),
+    # a serving-size batch (16 sequences = 256 block rows) with a wide FFN:
+    # the gate/up projection (160 tiles of 128 x 128 on 152 SMs) runs on the
+    # persistent kernel, whose 8 tiles of the last, partial round are split
+    # in K 8 ways (one 64-k block a segment)
+    "mini_d": DraftConfig("mini_d", batch=16, ctx_lo=3, ctx_hi=120, n_layers=1,
+                          hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                          ffn=5120, vocab=3000, n_taps=2, tap_width=512,
+                          match_prob=0.8, rounds=3, seed=2007),
     # fp32 mini: ragged, several pages, G = 2
     "mini_f32": DraftConfig("mini_f32", batch=2, ctx_lo=17, ctx_hi=90, n_layers=2,
                             hidden=192, n_q_heads=6, n_kv_heads=3, head_dim=32,

@@ -13,7 +13,7 @@ from harness import Pair
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["c1", "mini_f32", "mini_a", "mini_b", "mini_c", "mini_w8", "mini_w8b"])
+@pytest.mark.parametrize("name", ["c1", "mini_f32", "mini_a", "mini_b", "mini_c", "mini_d", "mini_w8", "mini_w8b"])
 def test_chain_parity(name):
     import torch
     cfg = synth.get_config(name)
