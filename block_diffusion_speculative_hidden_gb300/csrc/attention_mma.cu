@@ -81,8 +81,13 @@ struct MmaAttnLayout {
   static constexpr bool P_TMEM = M == 128 && PIPE && DH == 64 && 3 * SW + DH <= TMEM_COLS;
   static constexpr int NSB = P_TMEM ? 3 : PIPE ? 2 : 1;  // S buffers
   static constexpr int NO = PIPE ? 2 : 1;          // O buffers (P in TMEM: one, two commit barriers)
+  // the serial multi-block variants keep S and O in columns of their own: O
+  // accumulates over the blocks in TMEM (rescaled there only when a row's
+  // max moves, as in the row-wise variant), so S of the next block waits
+  // neither for the P V product nor for a fold
+  static constexpr bool SEPO = !ONE && !PIPE;
   __host__ __device__ static constexpr int s_col(int j) { return PIPE ? j * SW : 0; }
-  __host__ __device__ static constexpr int o_col(int j) { return PIPE ? NSB * SW + j * DH : 0; }
+  __host__ __device__ static constexpr int o_col(int j) { return PIPE ? NSB * SW + j * DH : SEPO ? SW : 0; }
   static constexpr int Q_CH = R * 128;             // stride of the Q chunks (real rows only)
   static constexpr int Q_BYTES = NCH * Q_CH;
   static constexpr int P_CHUNKS = (KBP * 16 + 63) / 64;
@@ -129,6 +134,7 @@ struct MmaAttnCfg : MmaAttnLayout<DH, G, KBP, NST> {
   static_assert(KBP * 16 <= 256 && DH <= 256, "one MMA's N");
   static_assert(L::P_TMEM   ? 3 * L::SW + DH <= L::TMEM_COLS
                 : L::PIPE ? 2 * L::SW + 2 * DH <= L::TMEM_COLS
+                : L::SEPO ? L::SW + DH <= L::TMEM_COLS
                           : KBP * 16 <= L::TMEM_COLS && DH <= L::TMEM_COLS,
                 "S and O buffers fit the allocation");
   static_assert((2 * NST + 13) * 8 <= L::BAR_AREA, "barriers fit their area");
@@ -176,6 +182,15 @@ __device__ __forceinline__ void tc_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[1
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
@@ -389,7 +404,7 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       auto issue_s = [&](int j) {
         const int s = j % NST, npb = min(KBP, np - j * KBP);
         if (!mbar_wait(&kv_full[s], (j / NST) & 1, p.status)) return false;
-        if (!C::PIPE && j > 0 && !mbar_wait(&o_free[0], (j - 1) & 1, p.status)) return false;
+        if (!C::PIPE && !C::SEPO && j > 0 && !mbar_wait(&o_free[0], (j - 1) & 1, p.status)) return false;
         // with P in TMEM, S(j) overwrites P(j - 3): MMAs into different
         // accumulators are not ordered, so wait for the P V product of j - 3
         // (its commit to o_full; only this thread advances that barrier, and
@@ -429,7 +444,7 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         } else {
           for (int k16 = 0; k16 < npb; ++k16)
             tc_mma_bf16(tmem + C::o_col(ob), sw128_desc(ap + (k16 >> 2) * C::P_CH + (k16 & 3) * 32, 16, 1024),
-                        sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, k16 > 0 ? 1u : 0u);
+                        sw128_desc(av + k16 * 2048, C::KV_CH, 1024), id_o, (C::SEPO ? (blk | k16) : k16) > 0 ? 1u : 0u);
         }
         tc_commit(&o_full[ob]);
         tc_commit(&kv_empty[s]);
@@ -700,11 +715,23 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       }
       pair_combine(mx, true);
       float m_new[RPT];
+      bool moved = false;
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
-        m_new[i] = fmaxf(m_run[i], mx[i] * p.scale_log2);
-        alpha[i] = m_run[i] == -INFINITY ? 0.f : ex2_ftz(m_run[i] - m_new[i]);
-        m_run[i] = m_new[i];
+        if constexpr (C::SEPO) {
+          // O accumulates in TMEM: m_run moves only when passed by more than
+          // kLazyRescale, and O is rescaled in TMEM then (below)
+          const float mc = mx[i] * p.scale_log2;
+          const bool mv = mc > m_run[i] + kLazyRescale;
+          alpha[i] = !mv ? 1.f : m_run[i] == -INFINITY ? 0.f : ex2_ftz(m_run[i] - mc);
+          if (mv) m_run[i] = mc;
+          moved = moved || mv;
+          m_new[i] = m_run[i];
+        } else {
+          m_new[i] = fmaxf(m_run[i], mx[i] * p.scale_log2);
+          alpha[i] = m_run[i] == -INFINITY ? 0.f : ex2_ftz(m_run[i] - m_new[i]);
+          m_run[i] = m_new[i];
+        }
         lsum[i] = 0.f;
       }
       // pass 2: P = 2^(S scale - m) in fp16 into the swizzled A operand
@@ -743,6 +770,32 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
       }
 #pragma unroll
       for (int i = 0; i < RPT; ++i) l_run[i] = l_run[i] * alpha[i] + lsum[i];
+      if constexpr (C::SEPO) {
+        // a row's max moved: O (this warp's half of the head dims) times
+        // alpha, in TMEM.  P V of the previous block is done (S of this
+        // block, whose completion this thread waited for, was issued after
+        // it) and P V of this block waits for p_full.
+        if (blk > 0 && __any_sync(0xffffffffu, moved)) {
+#pragma unroll
+          for (int sb = 0; sb < C::SUB; ++sb)
+#pragma unroll
+            for (int d0 = 0; d0 < DH / 2; d0 += 32) {
+              const uint32_t ta = tmem + lanes_of(sb) + C::o_col(0) + hf * (DH / 2) + d0;
+              uint32_t v[16];
+              tc_ld_16x256b_x4(ta, v);
+              tc_wait_ld();
+#pragma unroll
+              for (int gq = 0; gq < 4; ++gq)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int e = 0; e < 2; ++e)
+                    v[4 * gq + 2 * h + e] = __float_as_uint(__uint_as_float(v[4 * gq + 2 * h + e]) * alpha[2 * sb + h]);
+              tc_st_16x256b_x4(ta, v);
+            }
+          tc_wait_st();
+        }
+      }
       fence_proxy_async_smem();  // P is read by the tensor cores
       tc_fence_before();
       mbarrier_arrive_one(&p_full[blk % C::NSB]);
@@ -752,6 +805,8 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         __syncwarp();
         tc_fence_after();
         break;
+      } else if constexpr (C::SEPO) {
+        // (O stays in TMEM until the last block)
       } else if constexpr (C::NO == 1) {
         fold(blk, alpha, false);
       } else if (blk > 0) {
@@ -759,7 +814,9 @@ __global__ void __launch_bounds__(kAttnThreads, KBP <= 4 ? 2 : 1) k_attn_mma(con
         fold(blk - 1, alpha, false);
       }
     }
-    if constexpr (!ONE && C::NO == 2) {
+    if constexpr (!ONE && (C::NO == 2 || C::SEPO)) {
+      // the last O into the registers (SEPO: all blocks' O, accumulated in
+      // TMEM; the wait is for P V of the last block)
       if (nblk > 0) fold(nblk - 1, l_run, true);  // (no rescale: al unused)
     }
     // full row sums: over the 4 threads of each row, then the warp pair
