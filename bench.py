@@ -169,8 +169,13 @@ def barrier(world: int):
         dist.barrier()
 
 
-GEMM_PROFILE = os.path.join(ROOT, "profiles", "k_gemm_tc_c2_layer.md")
+# Per-launch DRAM traffic of the projection + LM-head launches, measured by
+# ncu at full size: (profile file, the sources whose text it was taken on)
 GEMM_SOURCES = ("gemm_kernel.cuh", "gemm.cu", "epilogue.cuh", "common.cuh")
+TRAFFIC_PROFILES = {
+    "c2_qwen3_8b_shaped": ("k_gemm_tc_c2_layer.md", GEMM_SOURCES),
+    "c5_gpt_oss_120b_shaped": ("k_gemm_pers_c5_traffic.md", ("gemm_persist.cuh",) + GEMM_SOURCES),
+}
 
 
 def code_text(src: str) -> str:
@@ -184,18 +189,22 @@ def code_text(src: str) -> str:
 
 
 def gemm_traffic(cfg):
-    """DRAM bytes per k_gemm_tc launch measured by ncu for the c2 round (see
-    the profile file), or None when the workload differs or the GEMM sources
-    changed since the capture."""
+    """DRAM bytes per projection / LM-head launch measured by ncu for this
+    workload (see the profile file), or None when there is no capture for it
+    or the GEMM sources changed since."""
     import hashlib
-    if cfg.name != "c2_qwen3_8b_shaped" or not os.path.exists(GEMM_PROFILE):
+    if cfg.name not in TRAFFIC_PROFILES:
+        return None
+    fname, sources = TRAFFIC_PROFILES[cfg.name]
+    path = os.path.join(ROOT, "profiles", fname)
+    if not os.path.exists(path):
         return None
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "block_diffusion_speculative_hidden_gb300", "csrc", f)) as fh:
             h.update(code_text(fh.read()).encode())
     fields = {}
-    for line in open(GEMM_PROFILE):
+    for line in open(path):
         if ":" in line and line.split(":")[0] in ("traffic_per_launch_bytes", "source_fingerprint"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
@@ -208,7 +217,8 @@ def algorithmic_bytes(cfg):
     """Bytes the hot path must move per round (B sequences), by kernel class.
 
     Projections: bf16 weights once + activations in (hi+lo bf16, 4 B/elem) +
-    fp32 results out.  Attention (kv_bytes): the K/V of every layer once.
+    fp32 results out; the LM head's logits out where the accept reads them.
+    Attention (kv_bytes): the K/V of every layer once.
     Inject: FC and K/V weights + the new rows; accept: tokens only."""
     B, d, F, V, L = cfg.batch, cfg.hidden, cfg.ffn, cfg.vocab, cfg.n_layers
     qd, kvd = cfg.q_dim, cfg.kv_dim
@@ -224,9 +234,11 @@ def algorithmic_bytes(cfg):
 
     Fp = 64 * -(-F // 64)                     # gate/up rows are packed in groups of 64
     per_layer = proj(qd + 2 * kvd, d) + proj(d, qd) + proj(2 * Fp, d) + proj(d, F)
+    lm_rows = M + (cfg.s_passes - 1) * (M // 2)  # S = 2: the second LM head runs on the K/2 uncommitted rows
     return {"proj": L * per_layer * cfg.s_passes,
-            # S = 2: the second LM head reads the K/2 uncommitted rows of each block
-            "lm_head": wbytes(V, d) * cfg.s_passes + (M + (cfg.s_passes - 1) * (M // 2)) * d * 4,
+            # stochastic workloads also write the rows' fp32 logits (the accept reads them)
+            "lm_head": wbytes(V, d) * cfg.s_passes + lm_rows * d * 4
+                       + (lm_rows * V * 4 if cfg.accept == "stochastic" else 0),
             "inject_weights": wbytes(d, cfg.feat_dim) + wbytes(2 * L * kvd, d)}
 
 
@@ -903,9 +915,13 @@ def roofline_block(cfg, res, hbm, tc, peak_kind):
     if tensor_bound(cfg):
         flops = (fl["proj"] + fl["lm_head"]) * steps
         achieved = flops / (gemm_ms / 1e3) / 1e12
+        tf = gemm_traffic(cfg)
         roof = dict(common, bound="tensor", achieved=achieved, peak=tc, unit="TFLOP/s", frac=achieved / tc,
                     peak_kind=f"{peak_kind} bf16_tflops_sustained (kernels timed inside a seconds-long loop)",
-                    flops_per_step=fl["proj"] + fl["lm_head"], traffic=None,
+                    flops_per_step=fl["proj"] + fl["lm_head"], traffic=tf,
+                    traffic_unit=(f"bytes per launch (ncu dram read+write at full size; profiles/"
+                                  f"{TRAFFIC_PROFILES[cfg.name][0]})") if tf is not None else None,
+                    algorithmic_bytes_per_launch=(ab["proj"] + ab["lm_head"]) * steps / max(gemm_launches, 1),
                     issued={"achieved": achieved * fl["issued_factor"], "frac": achieved * fl["issued_factor"] / tc,
                             "what": "both bf16 activation terms (hi + lo) multiplied: twice the method's flops"})
         return roof, per_class
@@ -913,7 +929,8 @@ def roofline_block(cfg, res, hbm, tc, peak_kind):
     achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
     roof = dict(common, bound="hbm", achieved=achieved, peak=hbm, unit="GB/s", frac=achieved / hbm,
                 peak_kind=f"{peak_kind} hbm_gbs", traffic=gemm_traffic(cfg),
-                traffic_unit="bytes per launch (ncu dram read+write; profiles/k_gemm_tc_c2_layer.md)",
+                traffic_unit=(f"bytes per launch (ncu dram read+write at full size; profiles/"
+                              f"{TRAFFIC_PROFILES[cfg.name][0]})") if cfg.name in TRAFFIC_PROFILES else None,
                 algorithmic_bytes_per_launch=(ab["proj"] + ab["lm_head"]) * steps / max(gemm_launches, 1),
                 bytes_per_step=ab["proj"] + ab["lm_head"])
     return roof, per_class
