@@ -175,6 +175,8 @@ GEMM_SOURCES = ("gemm_kernel.cuh", "gemm.cu", "epilogue.cuh", "common.cuh")
 TRAFFIC_PROFILES = {
     "c2_qwen3_8b_shaped": ("k_gemm_tc_c2_layer.md", GEMM_SOURCES),
     "c5_gpt_oss_120b_shaped": ("k_gemm_pers_c5_traffic.md", ("gemm_persist.cuh",) + GEMM_SOURCES),
+    "c3_serving_batch32": ("gemm_traffic_c3.md", ("gemm_persist.cuh",) + GEMM_SOURCES),
+    "c4_long_context_32k": ("gemm_traffic_c4.md", ("gemm_persist.cuh",) + GEMM_SOURCES),
 }
 
 
