@@ -218,6 +218,79 @@ __device__ __forceinline__ void epilogue_qkv_vec(const EpiArgs& e, const float* 
   }
 }
 
+// KV_INJECT epilogue of one tile, row-major like epilogue_qkv_vec: lane l
+// takes columns n0 + 4l .. n0 + 4l + 3, which lie in one head of one layer's
+// K or V (4 divides dh).  K gets the optional key offset and RoPE at the
+// row's position (cos / sin of its four frequencies as 128-bit loads), then
+// the four values go to the row's page slot as one 8-byte fp16 store.  The
+// same function as apply_epilogue's KV_INJECT branch (e.N and dh multiples
+// of 4).
+__device__ __forceinline__ void epilogue_kvinj_vec(const EpiArgs& e, const float* tile, int m0, int rows, int n0,
+                                                   const float* rs, const int4* ri) {
+  constexpr int B = 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = 4 * lane, n = n0 + t;
+  if (n >= e.N) return;  // per lane; no collective operations below
+  const int kvd = e.Hkv * e.dh, half = e.dh / 2;
+  const int l = n / (2 * kvd), w = n % (2 * kvd);
+  const bool is_k = w < kvd;
+  const int head = (is_k ? w : w - kvd) / e.dh, i = w % e.dh;
+  const int jr = i < half ? i : i - half;  // first of the four RoPE frequencies
+  const int base = t - i;                  // tile column of the head's element 0
+  float olo[4] = {0.f, 0.f, 0.f, 0.f}, ohi[4] = {0.f, 0.f, 0.f, 0.f};
+  if (is_k && e.key_offset != nullptr) {
+    const float* ko = e.key_offset + (static_cast<long long>(l) * e.Hkv + head) * e.dh;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      olo[k] = ko[jr + k];
+      ohi[k] = ko[jr + k + half];
+    }
+  }
+  __half* dst = static_cast<__half*>(is_k ? e.pool_k : e.pool_v) + static_cast<long long>(l) * e.layer_stride;
+  for (int j0 = warp; j0 < rows; j0 += 4 * B) {
+    float4 cs[B], sn[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int j = j0 + 4 * u;
+      cs[u] = sn[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (is_k && j < rows) {
+        const long long o = static_cast<long long>(ri[j].x) * half + jr;
+        cs[u] = *reinterpret_cast<const float4*>(e.rope_cos + o);
+        sn[u] = *reinterpret_cast<const float4*>(e.rope_sin + o);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int j = j0 + 4 * u;
+      if (j >= rows) break;
+      const float* row = tile + j * 128;
+      const float sc = rs != nullptr ? rs[j] : 1.f;
+      float r[4];
+      if (!is_k) {
+        const float4 v = *reinterpret_cast<const float4*>(row + t);
+        r[0] = v.x * sc;
+        r[1] = v.y * sc;
+        r[2] = v.z * sc;
+        r[3] = v.w * sc;
+      } else {
+        const float4 x1 = *reinterpret_cast<const float4*>(row + base + jr);
+        const float4 x2 = *reinterpret_cast<const float4*>(row + base + jr + half);
+        const float a1[4] = {x1.x * sc + olo[0], x1.y * sc + olo[1], x1.z * sc + olo[2], x1.w * sc + olo[3]};
+        const float a2[4] = {x2.x * sc + ohi[0], x2.y * sc + ohi[1], x2.z * sc + ohi[2], x2.w * sc + ohi[3]};
+        const float c[4] = {cs[u].x, cs[u].y, cs[u].z, cs[u].w};
+        const float s[4] = {sn[u].x, sn[u].y, sn[u].z, sn[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = i < half ? a1[k] * c[k] - a2[k] * s[k] : a2[k] * c[k] + a1[k] * s[k];
+      }
+      const __half2 h01 = __floats2half2_rn(r[0], r[1]), h23 = __floats2half2_rn(r[2], r[3]);
+      uint2 pkd;
+      pkd.x = *reinterpret_cast<const uint32_t*>(&h01);
+      pkd.y = *reinterpret_cast<const uint32_t*>(&h23);
+      *reinterpret_cast<uint2*>(dst + pool_index(ri[j].y, head, ri[j].z, i, e.Hkv, e.dh)) = pkd;
+    }
+  }
+}
+
 // Split tail (KSPLIT = 1 projections, given a workspace): the tiles are
 // dealt round-robin in whole rounds of one tile a CTA, and the R < grid
 // tiles of the last, partial round are each split in K among s =
@@ -514,6 +587,8 @@ __global__ void __launch_bounds__(PersCfg<BN, LMHEAD, KSPLIT>::THREADS, 1)
               epilogue_rows_vec(p.epi, mine, mr0, rows, n0, rs);
             } else if (p.epi.kind == EPI_QKV && p.N % 4 == 0 && p.epi.dh % 8 == 0) {
               epilogue_qkv_vec(p.epi, mine, mr0, rows, n0, rs, s_ri + fr);
+            } else if (p.epi.kind == EPI_KV_INJECT && p.N % 4 == 0 && p.epi.dh % 8 == 0) {
+              epilogue_kvinj_vec(p.epi, mine, mr0, rows, n0, rs, s_ri + fr);
             } else {
               EpiPre pre;
               epilogue_preload<__nv_bfloat16>(p.epi, mr0, NR, n0, s_ri + fr, pre);
