@@ -306,10 +306,7 @@ cudaError_t gemm_launch(dflash_ctx* c, const GemmLaunch& g, cudaStream_t s) {
     return plan == 2 ? launch_pers<128, false, 2>(c, g, tw, tx, txlo, s)
                      : launch_pers<128, false, 1>(c, g, tw, tx, txlo, s);
   }
-  // a row count known only on the device (m_valid: an injection's new rows)
-  // is usually far below the allocation: tiles of at most 128 rows, so that
-  // a CTA does not stream an activation tile of mostly unused rows
-  const int bn = gemm_bn(g.m_valid != nullptr ? std::min(g.M, 128) : g.M, split, w8);
+  const int bn = gemm_bn(g.M, split, w8);
   CUtensorMap tw, tx, txlo;
   if (!get_tmap(c, g.W, g.N, g.K, kTileN, &tw, w8 ? 1 : 0) || !get_tmap(c, g.X, g.M_alloc, g.K, bn, &tx))
     return cudaErrorInvalidValue;
