@@ -27,3 +27,38 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_roofline_traffic_only_with_a_matching_capture(tmp_path, monkeypatch):
+    """The bench reports a kernel class's measured DRAM traffic only from a
+    capture taken on the current GEMM sources: a record whose fingerprint
+    no longer matches (the kernel changed since) gives null, and so does a
+    workload without a record."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    cfg = synth.get_config("c5")
+    fname, sources = bench.TRAFFIC_PROFILES[cfg.name]
+    text = open(os.path.join(ROOT, "profiles", fname)).read()
+    fields = dict(l.split(":", 1) for l in text.splitlines()
+                  if l.split(":")[0] in ("traffic_per_launch_bytes", "source_fingerprint"))
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the same sources under the temporary root
+    csrc = tmp_path / "block_diffusion_speculative_hidden_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in sources:
+        src = open(os.path.join(ROOT, "block_diffusion_speculative_hidden_gb300", "csrc", f)).read()
+        (csrc / f).write_text(src)
+    (tmp_path / "profiles" / fname).write_text(text)
+    got = bench.gemm_traffic(cfg)
+    # a record matching the sources is read back as recorded; one that does not gives null
+    if got is not None:
+        assert got == float(fields["traffic_per_launch_bytes"].strip())
+    first = open(os.path.join(ROOT, "block_diffusion_speculative_hidden_gb300", "csrc", sources[0])).read()
+    (csrc / sources[0]).write_text(first + "\nint an_edit_of_the_kernel;\n")
+    assert bench.gemm_traffic(cfg) is None
+    # a comment-only edit keeps the record valid
+    (csrc / sources[0]).write_text(first + "\n// a note\n")
+    assert bench.gemm_traffic(cfg) == got
+    assert bench.gemm_traffic(synth.get_config("c1")) is None
