@@ -318,11 +318,11 @@ cudaError_t launch_accept_stochastic(int B, int K, int V, const int32_t* d, cons
                                      int32_t* tau, int32_t* emitted, int32_t* n_emit, int num_sms, bool pdl,
                                      cudaStream_t s) {
   const uint2 key = make_uint2(static_cast<uint32_t>(seed & 0xffffffffu), static_cast<uint32_t>(seed >> 32));
-  // CTAs per sequence: enough clusters to cover every SM about twice, at
+  // CTAs per sequence: enough clusters to cover every SM about four times, at
   // most 8 (a portable cluster), each slice at least 512 groups
   const int n_groups = (V + 3) / 4;
   int C = 1;
-  while (C < 8 && B * C < 2 * num_sms && n_groups / (2 * C) >= 512) C *= 2;
+  while (C < 8 && B * C < 4 * num_sms && n_groups / (2 * C) >= 512) C *= 2;
   const int per = (n_groups + C - 1) / C;
   return launch_k(k_accept_stochastic, dim3(B * C), dim3(kAccThreads), 0, s, dim3(C), pdl, K, V, per, d, z, q,
                   1.0f / temperature, key, static_cast<uint32_t>(round & 0xffffffffu), round_ctr, tau, emitted,
