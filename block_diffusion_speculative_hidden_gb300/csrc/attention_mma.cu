@@ -15,13 +15,21 @@
 //     an NST-deep ring of K / V tiles (4-D TMA, 128-byte swizzle);
 //   - S = Q K^T is one MMA chain per key block (query rows on M = 64 or
 //     128, keys on N, accumulated in TMEM); the softmax threads read S, form
-//     the block's row max, P = 2^(S*scale - max) in fp16 (written over the
-//     block's K tile, the A operand of the next MMA) and the running sums;
-//     O_blk = P V reuses the same TMEM columns (V enters as an MN-major
-//     operand); the threads fold O_blk into fp32 registers with the
-//     online-softmax rescale; in the pipelined variants (4-page blocks,
-//     dh 64: two S and two O buffers in TMEM) S of the next block and P V of
-//     this one run while the softmax works, and O is folded a block late;
+//     the block's row max, P = 2^(S*scale - max) in fp16 and the running
+//     sums, and O_blk = P V follows (V enters as an MN-major operand).  Three
+//     schedules:
+//       * one key block (ONE): O over the columns of S, read out at the end;
+//       * serial blocks (SEPO): S and O in TMEM columns of their own, P over
+//         the block's K tile, O accumulated in TMEM over the blocks and
+//         rescaled there only when a row's max passes the one P is taken
+//         against by more than 2^8, so S of the next block waits for
+//         neither P V nor a fold;
+//       * pipelined 4-page blocks (PIPE, dh 64): two S and two O buffers, S
+//         of the next block and P V of this one under the softmax, O folded
+//         into registers a block late; the 128-row case (row-wise softmax,
+//         one query row a thread) keeps P in TMEM over its S columns as the
+//         P V product's A operand, three S buffers and one O accumulated in
+//         TMEM with the same lazy rescale;
 //   - only the real query rows of Q and P are stored: the MMA's padding rows
 //     (G*16 .. 127) read whatever follows in shared memory, and the results
 //     in those rows are never used;
@@ -55,12 +63,13 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9;
 // thread t of the warp gets rows t/4 and t/4 + 8 of the block, columns
 // 2*(t%4) and 2*(t%4) + 1 of every 8-column group.
 //
-// Columns (256 a CTA, two CTAs an SM): S at column 0 and O = P V over it,
-// folded into registers before the next block's S, except in the pipelined
-// variants (4-page key blocks whose two S and two O buffers fit: dh 64).
-// There S of the next key block is computed while the softmax turns this
-// block's S into P, and O of a block is folded one block late (after the
-// next block's P is written), so the P V product runs under the softmax too.
+// Columns (256 a CTA, two CTAs an SM): one key block — S at column 0 and O
+// = P V over it; serial blocks — S at column 0, O after it; pipelined
+// 4-page blocks (two S and two O buffers fit: dh 64) — S of the next key
+// block is computed while the softmax turns this block's S into P, and O of
+// a block is folded one block late (after the next block's P is written),
+// so the P V product runs under the softmax too; with 128 rows, three S
+// buffers and one O (see P_TMEM below).
 template <int DH, int G, int KBP, int NST>
 struct MmaAttnLayout {
   static constexpr int R = G * 16;                 // real query rows
