@@ -16,10 +16,13 @@
 //     activation tiles lie back to back, so one MMA yields W.hi and W.lo
 //     side by side) into one of two TMEM accumulators, alternating by tile;
 //     warp 5 owns the TMEM allocation;
-//   - warps 0-3 (TMEM lane quadrants 0-3): read an accumulator out into a
-//     shared-memory tile of their own, release the accumulator (so the MMAs
-//     of the tile after next may start), then run the same fused epilogue
-//     as the single-tile kernel while the MMAs of the next tile proceed.
+//   - warps 0-3 (TMEM lane quadrants 0-3): read an accumulator out, 32
+//     activation rows at a time, into a shared-memory tile of their own and
+//     run the fused epilogue on each chunk; the accumulator is released
+//     after its last chunk is read (so the MMAs of the tile after next may
+//     start), all while the MMAs of the next tile proceed;
+//   - the tiles of the last, partial round may be split in K among several
+//     CTAs (the split tail, below).
 //
 // Every wait is bounded; after a wait gives up the CTA marks the status
 // word, the roles stop waiting on one another (a shared abort flag) and the
