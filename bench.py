@@ -574,6 +574,7 @@ def run_e2e(wl, args, device):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(gs)
+        cs.wait_event(e0)  # the first copy starts inside the region too
         issue_copy(0)
         for i in range(n):
             if i + 1 < n:
